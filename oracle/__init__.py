@@ -1,0 +1,172 @@
+"""CPU oracle of the MoE layer forward pass (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The product path (the CUDA library and its
+binding) never loads it. ``build()`` compiles ``moe_oracle.cpp`` with the host
+compiler into ``liboracle.so`` next to this file.
+
+All functions take and return numpy arrays (fp32 / int32, C-contiguous).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_f = ctypes.POINTER(ctypes.c_float)
+_i = ctypes.POINTER(ctypes.c_int32)
+_L = ctypes.c_int64
+
+
+def build(force: bool = False, extra_flags=()) -> str:
+    """Compile the oracle (g++ -O2 -fopenmp, IEEE semantics: no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-std=c++17", "-O2", "-fopenmp", "-fPIC", "-shared",
+               "-ffp-contract=off", *extra_flags, _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _declare(lib):
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_router_logits.argtypes = [_f, _f, _f, _L, _L, _L, _f]
+    lib.oracle_route.argtypes = [_f, _L, _L, _L, ctypes.c_int, _i, _f]
+    lib.oracle_permute.argtypes = [_i, _L, _L, _L, ctypes.c_int, _i, _i, _i]
+    lib.oracle_expert_h.argtypes = [_f, _i, _i, _f, _f, _L, _L, _L, _L, _L, _f, _f, _f, _L, _f]
+    lib.oracle_down_combine.argtypes = [_f, _i, _i, _i, _f, _f, _L, _L, _L, _L, _L, _f, _f,
+                                        _L, _f]
+    lib.oracle_ffn_combine.argtypes = [_f, _i, _f, _f, _f, _f, _L, _L, _L, _L, _L, _f, _f,
+                                       _f, _L, _f]
+    lib.oracle_moe_forward.argtypes = [_f, _f, _f, _f, _f, _f, _f, _f, _f, _L, _L, _L, _L, _L,
+                                       _L, ctypes.c_int, _f, _f, _i, _f]
+    for n in ("oracle_router_logits", "oracle_route", "oracle_permute", "oracle_expert_h",
+              "oracle_down_combine", "oracle_ffn_combine", "oracle_moe_forward"):
+        getattr(lib, n).restype = None
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) and return the ctypes library."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    if _lib is None:
+        build()
+        _lib = _declare(ctypes.CDLL(_LIB))
+    return _lib
+
+
+class Oracle:
+    """numpy-facing wrapper around one loaded oracle library."""
+
+    def __init__(self, lib=None):
+        self.lib = lib if lib is not None else load()
+
+    @staticmethod
+    def _pf(a):
+        if a is None:
+            return None
+        assert a.dtype == np.float32 and a.flags.c_contiguous, (a.dtype, a.flags)
+        return a.ctypes.data_as(_f)
+
+    @staticmethod
+    def _pi(a):
+        assert a.dtype == np.int32 and a.flags.c_contiguous
+        return a.ctypes.data_as(_i)
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def router_logits(self, x, Wr, bias=None):
+        T, H = x.shape
+        E = Wr.shape[0]
+        out = np.empty((T, E), np.float32)
+        self.lib.oracle_router_logits(self._pf(x), self._pf(Wr), self._pf(bias), T, H, E,
+                                      self._pf(out))
+        return out
+
+    def route(self, logits, k, renorm=1):
+        T, E = logits.shape
+        ids = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float32)
+        self.lib.oracle_route(self._pf(logits), T, E, k, int(renorm), self._pi(ids),
+                              self._pf(w))
+        return ids, w
+
+    def permute(self, ids, E, has_shared=0):
+        T, k = ids.shape
+        offsets = np.empty(E + 2, np.int32)
+        gather_idx = np.empty(T * k, np.int32)
+        slot_pos = np.empty(T * k, np.int32)
+        self.lib.oracle_permute(self._pi(np.ascontiguousarray(ids)), T, E, k, int(has_shared),
+                                self._pi(offsets), self._pi(gather_idx), self._pi(slot_pos))
+        return offsets, gather_idx, slot_pos
+
+    def expert_h(self, x, offsets, gather_idx, Wg, Wu, k, Wsg=None, Wsu=None):
+        T, H = x.shape
+        E, I, _ = Wg.shape
+        Is = 0 if Wsg is None else Wsg.shape[0]
+        h = np.empty((T * k, I), np.float32)
+        hs = np.empty((T, Is), np.float32) if Is else None
+        self.lib.oracle_expert_h(self._pf(x), self._pi(offsets), self._pi(gather_idx),
+                                 self._pf(Wg), self._pf(Wu), T, H, E, k, I, self._pf(h),
+                                 self._pf(Wsg), self._pf(Wsu), Is, self._pf(hs))
+        return h, hs
+
+    def down_combine(self, h, offsets, slot_pos, ids, w, Wd, hs=None, Wsd=None):
+        T, k = ids.shape
+        E, H, I = Wd.shape
+        Is = 0 if Wsd is None else Wsd.shape[1]
+        y = np.empty((T, H), np.float32)
+        self.lib.oracle_down_combine(self._pf(h), self._pi(offsets), self._pi(slot_pos),
+                                     self._pi(ids), self._pf(w), self._pf(Wd), T, H, E, k, I,
+                                     self._pf(hs), self._pf(Wsd), Is, self._pf(y))
+        return y
+
+    def ffn_combine(self, x, ids, w, Wg, Wu, Wd, Wsg=None, Wsu=None, Wsd=None):
+        T, H = x.shape
+        k = ids.shape[1]
+        E, I, _ = Wg.shape
+        Is = 0 if Wsg is None else Wsg.shape[0]
+        y = np.empty((T, H), np.float32)
+        self.lib.oracle_ffn_combine(self._pf(x), self._pi(ids), self._pf(w), self._pf(Wg),
+                                    self._pf(Wu), self._pf(Wd), T, H, E, k, I, self._pf(Wsg),
+                                    self._pf(Wsu), self._pf(Wsd), Is, self._pf(y))
+        return y
+
+    def forward(self, x, Wr, bias, Wg, Wu, Wd, k, renorm=1, Wsg=None, Wsu=None, Wsd=None,
+                want_intermediates=False):
+        T, H = x.shape
+        E, I, _ = Wg.shape
+        Is = 0 if Wsg is None else Wsg.shape[0]
+        y = np.empty((T, H), np.float32)
+        logits = np.empty((T, E), np.float32)
+        ids = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float32)
+        self.lib.oracle_moe_forward(self._pf(x), self._pf(Wr), self._pf(bias), self._pf(Wg),
+                                    self._pf(Wu), self._pf(Wd), self._pf(Wsg), self._pf(Wsu),
+                                    self._pf(Wsd), T, H, E, k, I, Is, int(renorm),
+                                    self._pf(y), self._pf(logits), self._pi(ids), self._pf(w))
+        if want_intermediates:
+            return y, dict(logits=logits, ids=ids, w=w)
+        return y
+
+
+def to_np(t):
+    """torch tensor (any device, bf16/fp32/int) -> C-contiguous numpy fp32/int32."""
+    if t is None:
+        return None
+    import torch
+    t = t.detach().cpu()
+    if t.dtype in (torch.bfloat16, torch.float16, torch.float32, torch.float64):
+        return np.ascontiguousarray(t.to(torch.float32).numpy())
+    return np.ascontiguousarray(t.to(torch.int32).numpy())

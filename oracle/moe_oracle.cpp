@@ -1,0 +1,248 @@
+// CPU oracle for the Mixture-of-Experts FFN layer forward pass.
+//
+// TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the benchmark's
+// CPU-baseline leg may load this library. It shares no code with the CUDA path
+// and neither side includes the other.
+//
+// It is the plain definition, written as slow loops in the order the pages
+// state the layer:
+//   1. router logits            l[t][e] = sum_h x[t][h] * Wr[e][h] (+ b[e])
+//      ("Lower latency and higher throughput with multi-node DeepSeek
+//      deployment", five-stage layer breakdown: the "Gate" ends stage 2).
+//   2. top-k on the logits, lowest expert index first among equals, then the
+//      softmax gate weights, renormalised over the k chosen experts
+//      (same page, section "MoE Router": top-K indices and scores).
+//   3. a stable counting sort of the (token, rank) slots by expert: per-expert
+//      counts, offsets and a unique position for every slot ("CuTeDSL at
+//      Perplexity", section "Mixture-of-Experts Dispatch/Combine", "Local").
+//   4. per routed position, the SwiGLU expert FFN: silu(x Wg^T) * (x Wu^T),
+//      then the down projection (Qwen3.5-397B on TPU v7x write-up, section
+//      4.2.2: gate and up projections with the SwiGLU activation fused).
+//   5. the gate-weighted sum of each token's expert outputs, plus the shared
+//      expert's output with weight 1 (DeepSeek page, "Expert Parallelism").
+//
+// Precision: all data are fp32 (bf16 inputs are widened exactly by the
+// caller); every sum is accumulated in fp64 in natural index order and rounded
+// to fp32 where a stage stores its result (logits, weights, h, y). Selection
+// (top-k) compares the stored fp32 logits.
+//
+// Parity pins (tests/test_oracle.py, CPU only): float64 library matmul for
+// the logits; a stable library sort for top-k ids; softmax identities for the
+// weights; bijection / stability / library argsort for the permutation;
+// brute-force dense evaluation of every expert, the k=E uniform-weight mean of
+// experts, the E=1 dense FFN in torch float64, token-permutation equivariance,
+// and a hand-derived closed-form case (tests/golden/).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+inline double silu(double z) { return z / (1.0 + std::exp(-z)); }
+
+// One routed or shared FFN evaluation for one token row.
+// Wg, Wu: [I][H]; Wd: [H][I]. h_out (nullable) receives fp32 h; o_out: [H] fp64.
+void expert_ffn(const float* xr, const float* Wg, const float* Wu, const float* Wd,
+                int64_t H, int64_t I, float* h_out, double* o_out) {
+  std::vector<float> h(I);
+  for (int64_t i = 0; i < I; ++i) {
+    const float* wg = Wg + i * H;
+    const float* wu = Wu + i * H;
+    double g = 0.0, u = 0.0;
+    for (int64_t c = 0; c < H; ++c) {
+      g += (double)xr[c] * (double)wg[c];
+      u += (double)xr[c] * (double)wu[c];
+    }
+    h[i] = (float)(silu(g) * u);
+  }
+  if (h_out) std::memcpy(h_out, h.data(), sizeof(float) * I);
+  if (o_out) {
+    for (int64_t c = 0; c < H; ++c) {
+      const float* wd = Wd + c * I;
+      double o = 0.0;
+      for (int64_t i = 0; i < I; ++i) o += (double)h[i] * (double)wd[i];
+      o_out[c] = o;
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+// Step 1: logits [T][E] = x [T][H] . Wr[E][H]^T (+ bias[E]); fp64 sums, fp32 out.
+void oracle_router_logits(const float* x, const float* Wr, const float* bias,
+                          int64_t T, int64_t H, int64_t E, float* logits) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int64_t c = 0; c < H; ++c) s += (double)x[t * H + c] * (double)Wr[e * H + c];
+      if (bias) s += (double)bias[e];
+      logits[t * E + e] = (float)s;
+    }
+  }
+}
+
+// Step 2: for each token, k rounds of "largest not yet chosen logit, lowest
+// index among equals"; ids come out in descending score order. Weights are
+// p_e = exp(l_e - l_max); S = sum over the chosen p (renorm != 0) or over all E
+// (renorm == 0); w = p / S.
+void oracle_route(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
+                  int32_t* ids, float* w) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    const float* l = logits + t * E;
+    std::vector<char> taken(E, 0);
+    for (int64_t r = 0; r < k; ++r) {
+      int64_t best = -1;
+      for (int64_t e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || l[e] > l[best]) best = e;  // strict '>' keeps the lower index
+      }
+      taken[best] = 1;
+      ids[t * k + r] = (int32_t)best;
+    }
+    const double m = (double)l[ids[t * k]];
+    double S = 0.0;
+    if (renorm) {
+      for (int64_t r = 0; r < k; ++r) S += std::exp((double)l[ids[t * k + r]] - m);
+    } else {
+      for (int64_t e = 0; e < E; ++e) S += std::exp((double)l[e] - m);
+    }
+    for (int64_t r = 0; r < k; ++r)
+      w[t * k + r] = (float)(std::exp((double)l[ids[t * k + r]] - m) / S);
+  }
+}
+
+// Step 3: counting sort of slots s = t*k + r by expert, stable in s.
+// offsets[0..E] = exclusive prefix of the counts; offsets[E+1] = offsets[E]
+// + (has_shared ? T : 0) closes the shared segment, whose position T*k + t is
+// token t. gather_idx[p] = slot at position p; slot_pos[s] = position of slot s.
+void oracle_permute(const int32_t* ids, int64_t T, int64_t E, int64_t k, int has_shared,
+                    int32_t* offsets, int32_t* gather_idx, int32_t* slot_pos) {
+  std::vector<int64_t> cnt(E, 0);
+  for (int64_t s = 0; s < T * k; ++s) cnt[ids[s]] += 1;
+  offsets[0] = 0;
+  for (int64_t e = 0; e < E; ++e) offsets[e + 1] = (int32_t)(offsets[e] + cnt[e]);
+  offsets[E + 1] = (int32_t)(offsets[E] + (has_shared ? T : 0));
+  std::vector<int64_t> fill(E, 0);
+  for (int64_t s = 0; s < T * k; ++s) {
+    const int64_t e = ids[s];
+    const int64_t p = offsets[e] + fill[e]++;
+    gather_idx[p] = (int32_t)s;
+    slot_pos[s] = (int32_t)p;
+  }
+}
+
+// Step 4a: h for every routed position (and the shared rows). x [T][H];
+// Wg, Wu [E][I][H]; h [T*k][I]; shared: Wsg, Wsu [Is][H], hs [T][Is].
+void oracle_expert_h(const float* x, const int32_t* offsets, const int32_t* gather_idx,
+                     const float* Wg, const float* Wu, int64_t T, int64_t H, int64_t E,
+                     int64_t k, int64_t I, float* h, const float* Wsg, const float* Wsu,
+                     int64_t Is, float* hs) {
+  const int64_t P = (int64_t)offsets[E];
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t p = 0; p < P; ++p) {
+    int64_t e = 0;
+    while (!(p >= offsets[e] && p < offsets[e + 1])) ++e;
+    const int64_t t = gather_idx[p] / k;
+    expert_ffn(x + t * H, Wg + e * I * H, Wu + e * I * H, nullptr, H, I, h + p * I, nullptr);
+  }
+  if (Is > 0 && hs) {
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t)
+      expert_ffn(x + t * H, Wsg, Wsu, nullptr, H, Is, hs + t * Is, nullptr);
+  }
+}
+
+// Step 4b + 5 from given h: y[t][c] = sum_r w[t][r] * (h[p] . Wd[e][c][:]) with
+// p = slot_pos[t*k + r], plus (hs[t] . Wsd[c][:]) when Is > 0. fp64 sums.
+void oracle_down_combine(const float* h, const int32_t* offsets, const int32_t* slot_pos,
+                         const int32_t* ids, const float* w, const float* Wd, int64_t T,
+                         int64_t H, int64_t E, int64_t k, int64_t I, const float* hs,
+                         const float* Wsd, int64_t Is, float* y) {
+  (void)offsets;
+  (void)E;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < T; ++t) {
+    std::vector<double> acc(H, 0.0);
+    for (int64_t r = 0; r < k; ++r) {
+      const int64_t s = t * k + r;
+      const int64_t p = slot_pos[s];
+      const int64_t e = ids[s];
+      const float* hp = h + p * I;
+      const float* wd = Wd + e * H * I;
+      for (int64_t c = 0; c < H; ++c) {
+        double o = 0.0;
+        for (int64_t i = 0; i < I; ++i) o += (double)hp[i] * (double)wd[c * I + i];
+        acc[c] += (double)w[s] * o;
+      }
+    }
+    if (Is > 0 && hs) {
+      const float* hp = hs + t * Is;
+      for (int64_t c = 0; c < H; ++c) {
+        double o = 0.0;
+        for (int64_t i = 0; i < Is; ++i) o += (double)hp[i] * (double)Wsd[c * Is + i];
+        acc[c] += o;
+      }
+    }
+    for (int64_t c = 0; c < H; ++c) y[t * H + c] = (float)acc[c];
+  }
+}
+
+// Steps 4 + 5 with the routing given: y [T][H] from x, ids, w and the weights.
+// Each token is evaluated on its own; nothing is shared between tokens.
+void oracle_ffn_combine(const float* x, const int32_t* ids, const float* w, const float* Wg,
+                        const float* Wu, const float* Wd, int64_t T, int64_t H, int64_t E,
+                        int64_t k, int64_t I, const float* Wsg, const float* Wsu,
+                        const float* Wsd, int64_t Is, float* y) {
+  (void)E;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < T; ++t) {
+    std::vector<double> acc(H, 0.0), o(H);
+    for (int64_t r = 0; r < k; ++r) {
+      const int64_t e = ids[t * k + r];
+      expert_ffn(x + t * H, Wg + e * I * H, Wu + e * I * H, Wd + e * H * I, H, I, nullptr,
+                 o.data());
+      for (int64_t c = 0; c < H; ++c) acc[c] += (double)w[t * k + r] * o[c];
+    }
+    if (Is > 0) {
+      expert_ffn(x + t * H, Wsg, Wsu, Wsd, H, Is, nullptr, o.data());
+      for (int64_t c = 0; c < H; ++c) acc[c] += o[c];
+    }
+    for (int64_t c = 0; c < H; ++c) y[t * H + c] = (float)acc[c];
+  }
+}
+
+// The whole layer: steps 1-5. Every intermediate output pointer is nullable.
+void oracle_moe_forward(const float* x, const float* Wr, const float* bias, const float* Wg,
+                        const float* Wu, const float* Wd, const float* Wsg, const float* Wsu,
+                        const float* Wsd, int64_t T, int64_t H, int64_t E, int64_t k,
+                        int64_t I, int64_t Is, int renorm, float* y, float* logits_out,
+                        int32_t* ids_out, float* w_out) {
+  std::vector<float> logits(T * E), w(T * k);
+  std::vector<int32_t> ids(T * k);
+  oracle_router_logits(x, Wr, bias, T, H, E, logits.data());
+  oracle_route(logits.data(), T, E, k, renorm, ids.data(), w.data());
+  oracle_ffn_combine(x, ids.data(), w.data(), Wg, Wu, Wd, T, H, E, k, I, Wsg, Wsu, Wsd, Is, y);
+  if (logits_out) std::memcpy(logits_out, logits.data(), sizeof(float) * T * E);
+  if (ids_out) std::memcpy(ids_out, ids.data(), sizeof(int32_t) * T * k);
+  if (w_out) std::memcpy(w_out, w.data(), sizeof(float) * T * k);
+}
+
+}  // extern "C"
