@@ -1,0 +1,532 @@
+"""Benchmark of the MoE layer forward pass on GB300.
+
+One step = the whole layer (router logits, top-k routing, permutation, grouped
+gate/up GEMM with SwiGLU, down GEMM with the weighted combine) over one batch of
+synthetic tokens whose weights and inputs are resident in HBM.
+
+Default workload: the Qwen3-235B-shaped decode step (T=64, H=4096, E=128, k=8,
+I=1536, bf16). The prefill chunk of the same layer (T=8192) is measured too and
+reported under "prefill". Every input is larger than L2 except the token batch
+itself (the expert weights are ~4.8 GB), so no L2 flush is needed between steps.
+
+Printed: one JSON line (rank 0). value = tokens/s of the whole job; roofline =
+the dominant kernel's achieved bandwidth or FLOP rate against the measured peak;
+layer_roofline = t_roof / t_measured for the whole layer with
+t_roof = max(routed FLOPs / bf16 peak, touched bytes / HBM bandwidth);
+e2e = the same metric through MoELayer.forward with the tokens copied from
+pinned host memory and the output copied back inside the timed region;
+cpu_baseline = the CPU oracle on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): each rank runs an independent replica of the layer on its
+own batch (the layer has no exchange step on one GPU); the time is the max over
+ranks and value counts every rank's tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from moe_inputs import CONFIGS, PROFILE_CONFIGS, generate  # noqa: E402
+
+ALL_CONFIGS = {**CONFIGS, **PROFILE_CONFIGS}
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["mixture_experts_layer_route_gb300/csrc/grouped_gemm.cuh",
+                  "mixture_experts_layer_route_gb300/csrc/grouped_gemm.cu",
+                  "mixture_experts_layer_route_gb300/csrc/common.cuh"]
+STAGES = ["router_logits", "route", "permute", "swiglu_gemm", "down_gemm+combine"]
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(config: str, kernel: str):
+    """Per-launch DRAM bytes of `kernel` on `config` from the committed ncu
+    summary, or None if absent or taken on a different kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        e = t[config][kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- model
+
+def roofline_numbers(cfg, counts):
+    """Algorithmic FLOPs and bytes of the layer and of the gated GEMM, from the
+    run's own per-expert counts."""
+    es = cfg.elem_bytes
+    T, H, E, k, I, Is = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.I_shared
+    touched = int((counts > 0).sum())
+    flop_layer = 2.0 * T * k * 3 * H * I + 2.0 * T * 3 * H * Is
+    bytes_layer = (touched * 3 * H * I * es + (3 * H * Is * es if Is else 0)
+                   + 2 * T * H * es + E * H * es)
+    flop_g = 2.0 * T * k * 2 * H * I + 2.0 * T * 2 * H * Is
+    bytes_g = (touched * 2 * H * I * es + (2 * H * Is * es if Is else 0) + T * H * es
+               + (T * k * I + T * Is) * es)
+    return dict(touched=touched, flop_layer=flop_layer, bytes_layer=bytes_layer,
+                flop_gated=flop_g, bytes_gated=bytes_g)
+
+
+def build_layer(cfg, device, seed=0):
+    import mixture_experts_layer_route_gb300 as m
+    d = generate(cfg, seed=seed, device=device)
+    layer = m.MoELayer(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k,
+                       router_bias=d["router_bias"], Ws_gate=d["Ws_gate"], Ws_up=d["Ws_up"],
+                       Ws_down=d["Ws_down"], renorm=cfg.renorm)
+    return layer, d
+
+
+def stage_sequence(layer, d, T, ws, lay, stream):
+    """The kernels of one moe_forward call, issued through the sub-call entry
+    points so that CUDA events can separate them."""
+    import mixture_experts_layer_route_gb300 as m
+    pb = layer.problem(T)
+    E, k = layer.E, layer.k
+
+    def buf(name, n, dt):
+        o = lay[name]
+        return ws[o:o + n * 4].view(dt)
+
+    logits = buf("logits", T * E, torch.float32).view(T, E)
+    ids = buf("topk_ids", T * k, torch.int32).view(T, k)
+    w = buf("topk_w", T * k, torch.float32).view(T, k)
+    offs = buf("expert_offsets", E + 2, torch.int32)
+    gidx = buf("gather_idx", T * k, torch.int32)
+    spos = buf("slot_pos", T * k, torch.int32)
+    es = 2 if layer.dtype == torch.bfloat16 else 4
+    h = ws[lay["h"]:lay["h"] + T * k * layer.I * es].view(layer.dtype).view(T * k, layer.I)
+    hs = None
+    if layer.I_shared:
+        o = lay["h_shared"]
+        hs = ws[o:o + T * layer.I_shared * es].view(layer.dtype).view(T, layer.I_shared)
+    y = torch.empty(T, layer.H, dtype=layer.dtype, device=ws.device)
+    steps = [
+        lambda: m.router_logits(pb, d["x"], layer.W_router, layer.router_bias, logits, ws,
+                                stream),
+        lambda: m.route(logits, k, layer.renorm, ids, w, stream),
+        lambda: m.permute(ids, E, 1 if layer.I_shared else 0, offs, gidx, spos, ws, stream),
+        lambda: m.grouped_swiglu_gemm(pb, d["x"], offs, gidx, layer.W_gate, layer.W_up,
+                                      layer.Ws_gate, layer.Ws_up, h, hs, ws, stream),
+        lambda: m.down_combine(pb, h, hs, offs, gidx, w, layer.W_down, layer.Ws_down, y, ws,
+                               stream),
+    ]
+    return steps, offs
+
+
+def time_forward(layer, d, steps, warmup, stream):
+    x = d["x"]
+    T = x.shape[0]
+    y = torch.empty(T, layer.H, dtype=layer.dtype, device=x.device)
+    for _ in range(warmup):
+        layer.forward(x, out=y, stream=stream)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            layer.forward(x, out=y, stream=stream)
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[-1]), per
+
+
+def time_stages(layer, d, steps, warmup, stream):
+    import mixture_experts_layer_route_gb300 as m
+    T = d["x"].shape[0]
+    ws = layer.workspace(T)
+    lay = m.workspace_layout(layer.problem(T))
+    fns, offs = stage_sequence(layer, d, T, ws, lay, stream)
+    for _ in range(warmup):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    n = len(fns)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            ev[i][0].record(stream)
+            for j, f in enumerate(fns):
+                f()
+                ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    st = m.get_device_status(ws, stream)
+    if st != m.MOE_OK:
+        raise RuntimeError(f"device status {m.status_string(st)}")
+    per_stage = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+                 for j in range(n)]
+    counts = torch.diff(offs[:layer.E + 1]).cpu()
+    return per_stage, counts
+
+
+def time_e2e(layer, d, steps, warmup, stream):
+    """Public API end to end: pinned host tokens -> device, forward, -> host."""
+    x_dev = d["x"]
+    T, H = x_dev.shape
+    x_host = x_dev.cpu().pin_memory()
+    y_host = torch.empty((T, H), dtype=layer.dtype).pin_memory()
+    x_in = torch.empty_like(x_dev)
+    y = torch.empty_like(x_dev)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            x_in.copy_(x_host, non_blocking=True)
+            layer.forward(x_in, out=y, stream=stream)
+            y_host.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            x_in.copy_(x_host, non_blocking=True)
+            layer.forward(x_in, out=y, stream=stream)
+            y_host.copy_(y, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    nb = T * H * x_dev.element_size()
+    return ms, nb, nb
+
+
+def cpu_baseline(cfg, d, budget_s=10.0, max_tokens=None):
+    """The CPU oracle, as it stands, on a bounded sample of tokens of the same
+    layer: tokens/s over ~budget_s seconds of oracle work."""
+    import numpy as np
+
+    import oracle
+    o = oracle.Oracle()
+    T = cfg.T if max_tokens is None else min(cfg.T, max_tokens)
+    x = d["x"][:T]
+    # Only the experts the sampled tokens use are copied to the host.
+    lg = o.router_logits(oracle.to_np(x), oracle.to_np(d["W_router"]),
+                         oracle.to_np(d["router_bias"]))
+    ids, _ = o.route(lg, cfg.k, cfg.renorm)
+    used = np.unique(ids)
+    remap = np.full(cfg.E, -1, np.int64)
+    remap[used] = np.arange(len(used))
+    sel = torch.from_numpy(used.astype(np.int64)).to(d["W_gate"].device)
+    Wr = oracle.to_np(d["W_router"])
+    Wg = oracle.to_np(d["W_gate"][sel])
+    Wu = oracle.to_np(d["W_up"][sel])
+    Wd = oracle.to_np(d["W_down"][sel])
+    sh = [oracle.to_np(d[n]) for n in ("Ws_gate", "Ws_up", "Ws_down")]
+    xs = oracle.to_np(x)
+    bias = oracle.to_np(d["router_bias"])
+    # The oracle's own forward, restricted to the copied experts: route on the
+    # full logits, then the FFN + combine on the remapped ids.
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        lg = o.router_logits(xs, Wr, bias)
+        ids, w = o.route(lg, cfg.k, cfg.renorm)
+        o.ffn_combine(xs, np.ascontiguousarray(remap[ids].astype(np.int32)), w, Wg, Wu, Wd,
+                      *sh)
+        done += T
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": done / el, "unit": "tokens/s", "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"{done} tokens ({T} per pass, {done // T} passes) of the {cfg.name} "
+                      f"layer through the fp32 C++ oracle (router, top-k, experts, combine)",
+            "seconds": el}
+
+
+# ----------------------------------------------------------------- main
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measure_config(cfg, args, world, local, with_clocks):
+    import mixture_experts_layer_route_gb300 as m
+    stream = torch.cuda.Stream()
+    layer, d = build_layer(cfg, "cuda", seed=args.seed)
+    layer.workspace(cfg.T)
+    steps = args.steps if cfg.T <= 1024 else max(3, args.steps // 8)
+    # timed region: K steps of moe_forward
+    sampler = ClockSampler(local) if with_clocks else None
+    barrier(world)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ms_total, per = time_forward(layer, d, steps, args.warmup, stream)
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    ms_total = max_over_ranks(ms_total, world)
+    st = m.get_device_status(layer.workspace(cfg.T), stream)
+    if st != m.MOE_OK:
+        raise RuntimeError(f"device status {m.status_string(st)}")
+    # per-kernel durations (same kernels, issued stage by stage between events)
+    per_stage, counts = time_stages(layer, d, steps, args.warmup, stream)
+    e2e_ms, h2d, d2h = time_e2e(layer, d, steps, args.warmup, stream)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    rl = roofline_numbers(cfg, counts.numpy())
+    out = dict(cfg=cfg, steps=steps, ms_total=ms_total, per=per, per_stage=per_stage,
+               counts=counts, rl=rl, clocks=clocks, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+               layer=layer, d=d)
+    return out
+
+
+def summarize(r, peaks, world, prefix_src):
+    cfg = r["cfg"]
+    steps = r["steps"]
+    ms_step = r["ms_total"] / steps
+    value = world * cfg.T * steps / (r["ms_total"] / 1e3)
+    rl = r["rl"]
+    st = dict(zip(STAGES, r["per_stage"]))
+    g_ms = st["swiglu_gemm"]
+    hbm = peaks["hbm_gbs"]
+    tc = peaks["bf16_tflops_sustained"]
+    t_mem = rl["bytes_layer"] / (hbm * 1e9) * 1e3
+    t_tc = rl["flop_layer"] / (tc * 1e12) * 1e3
+    t_roof = max(t_mem, t_tc)
+    bound = "hbm" if t_mem >= t_tc else "tensor"
+    if bound == "hbm":
+        ach = rl["bytes_gated"] / (g_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "grouped_gemm_kernel<bf16,gated>", "achieved": ach,
+                "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "algorithmic_bytes_per_launch": rl["bytes_gated"]}
+    else:
+        ach = rl["flop_gated"] / (g_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": "grouped_gemm_kernel<bf16,gated>", "achieved": ach,
+                "peak": tc, "unit": "TFLOP/s", "frac": ach / tc,
+                "algorithmic_flops_per_launch": rl["flop_gated"]}
+    roof["peak_source"] = f"{prefix_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops_sustained'})"
+    roof["kernel_ms"] = g_ms
+    roof["traffic"] = traffic_for(cfg.name, "swiglu_gemm")
+    counts = r["counts"].numpy()
+    loads = counts[counts > 0]
+    return dict(
+        value=value, ms_per_step=ms_step, steps=steps,
+        median_ms=statistics.median(r["per"]), p10_ms=sorted(r["per"])[len(r["per"]) // 10],
+        p90_ms=sorted(r["per"])[(9 * len(r["per"])) // 10],
+        roofline=roof,
+        layer_roofline={"t_roof_ms": t_roof, "bound": bound, "frac": t_roof / ms_step,
+                         "flop_routed": rl["flop_layer"], "bytes_touched": rl["bytes_layer"],
+                         "experts_touched": rl["touched"]},
+        stages_ms=st,
+        expert_load={"touched": int(len(loads)), "empty": int((counts == 0).sum()),
+                     "max": int(counts.max()), "mean": float(counts.mean()),
+                     "std_over_mean": float(counts.std() / max(counts.mean(), 1e-9))},
+        e2e={"value": world * cfg.T * steps / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
+             "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+             "ms_per_step": r["e2e_ms"] / steps},
+    )
+
+
+def run_native(args):
+    world, rank, local = dist_setup(args)
+    import mixture_experts_layer_route_gb300 as m
+    from mixture_experts_layer_route_gb300 import build as b
+    if rank == 0 or not os.path.exists(m._binding.LIB_PATH):
+        b.build()
+    barrier(world)
+    peaks, src = load_peaks()
+    cfg = ALL_CONFIGS[args.config]
+    r = measure_config(cfg, args, world, local, with_clocks=True)
+    s = summarize(r, peaks, world, src)
+    clocks = r["clocks"]
+    prefill = None
+    if args.prefill and args.config != "qwen3_235b_prefill":
+        del r
+        torch.cuda.empty_cache()
+        rp = measure_config(CONFIGS["qwen3_235b_prefill"], args, world, local,
+                            with_clocks=False)
+        sp = summarize(rp, peaks, world, src)
+        prefill = {"config": {"workload": "qwen3_235b_prefill", "T": 8192, "H": 4096, "E": 128,
+                              "k": 8, "I": 1536},
+                   **{k: sp[k] for k in ("value", "ms_per_step", "roofline", "layer_roofline",
+                                         "stages_ms", "expert_load")}}
+        del rp
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        torch.cuda.empty_cache()
+        layer, d = build_layer(cfg, "cuda", seed=args.seed)
+        cpu = cpu_baseline(cfg, d, budget_s=args.cpu_seconds)
+        del layer, d
+    if rank != 0:
+        return
+    line = {
+        "metric": "MoE-layer tokens/sec at 1 GB300 (decode & prefill) + % of HBM / bf16-TC roofline",
+        "value": s["value"], "unit": "tokens/s", "n_gpus": world, "steps": s["steps"],
+        "warmup": args.warmup, "ms_per_step": s["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
+                   "I": cfg.I, "I_shared": cfg.I_shared, "renorm": cfg.renorm,
+                   "seed": args.seed, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (expert weights), no flush"},
+        "median_ms": s["median_ms"], "p10_ms": s["p10_ms"], "p90_ms": s["p90_ms"],
+        "roofline": s["roofline"], "layer_roofline": s["layer_roofline"],
+        "stages_ms": s["stages_ms"], "expert_load": s["expert_load"],
+        "e2e": s["e2e"], "gpu_launches": 6 * s["steps"],
+        "clocks": clocks,
+        "cpu_baseline": cpu, "prefill": prefill,
+    }
+    print(json.dumps(line))
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: same workload, metric and unit."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = ALL_CONFIGS[args.config]
+    torch.cuda.set_device(0)
+    layer, d = build_layer(cfg, "cuda", seed=args.seed)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, d, budget_s=0.0, max_tokens=8)
+    vals, toks, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        r = cpu_baseline(cfg, d, budget_s=per_step)
+        vals.append(r["value"])
+        secs += r["seconds"]
+        toks += int(r["value"] * r["seconds"] + 0.5)
+    value = toks / secs
+    line = {"metric": "MoE-layer tokens/sec at 1 GB300 (decode & prefill) + % of HBM / bf16-TC roofline",
+            "impl": "reference", "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
+                       "I": cfg.I, "I_shared": cfg.I_shared, "seed": args.seed},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": r["cores"],
+                             "kind": "oracle", "sample": r["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="qwen3_235b_decode", choices=sorted(ALL_CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * moe_api.h — C ABI of the GB300 Mixture-of-Experts FFN layer forward pass.
+ *
+ * The layer (per token t, with x[t] its hidden row):
+ *   logits[t][e] = x[t] . W_router[e] (+ router_bias[e])
+ *   ids[t][0..k)  = the k largest logits, descending, lowest index among equals
+ *   w[t][r]       = exp(l_{ids[t][r]} - l_max) / S, S summed over the k chosen
+ *                   experts (renorm = 1) or over all E experts (renorm = 0)
+ *   y[t]          = sum_r w[t][r] * FFN_{ids[t][r]}(x[t])  (+ FFN_shared(x[t]))
+ *   FFN_e(v)      = W_down[e] (silu(W_gate[e] v) * (W_up[e] v)),
+ *                   silu(z) = z / (1 + exp(-z))
+ * Sources: "Lower latency and higher throughput with multi-node DeepSeek
+ * deployment" (Perplexity blog; sections "Expert Parallelism", "MoE Router",
+ * "GroupGEMM"), "CuTeDSL at Perplexity" (section "Mixture-of-Experts
+ * Dispatch/Combine", "Local"), and the Qwen3.5-397B on TPU v7x write-up
+ * (section 4.2.1 ragged gather, section 4.2.2 grouped GEMM with fused SwiGLU).
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers owned by the caller, unless stated. The library
+ *    allocates no device memory; scratch comes from `workspace`, whose size is
+ *    given by moe_workspace_size(). Every pointer must be 16-byte aligned.
+ *  - Layouts are contiguous row-major: x [T][H]; W_router [E][H];
+ *    W_gate, W_up [E][I][H]; W_down [E][H][I]; shared expert Ws_gate, Ws_up
+ *    [I_shared][H], Ws_down [H][I_shared]; y [T][H]. Both expert GEMMs are thus
+ *    K-major (nn.Linear "out x in" per expert).
+ *  - x, the weights, h and y share the problem's dtype (bf16, or fp32 which the
+ *    tensor cores consume as tf32). logits and gate weights are fp32; ids,
+ *    offsets and indices are int32.
+ *  - Shapes: 1 <= k <= E <= 1024, k <= 32; H a multiple of 128; I and I_shared
+ *    multiples of 64; T*k and T*(k+1) below 2^31.
+ *  - Argument errors are detected on the host before any launch and returned
+ *    as MOE_ERR_*; outputs are then untouched. T == 0 is MOE_OK.
+ *  - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream); no call synchronises except
+ *    moe_get_device_status().
+ *  - Asynchronous device conditions (a bounded wait that ran out, a failed
+ *    device-side check) are recorded in a status word at the start of the
+ *    workspace and read with moe_get_device_status(). The word is sticky: once
+ *    set, later kernels that see it give up early. moe_forward() clears it
+ *    when it starts; the sub-calls do not (use moe_reset_device_status()).
+ *    Kernels never trap.
+ *  - Results are bitwise reproducible run to run: no floating-point atomics,
+ *    fixed reduction orders.
+ *  - Thread-compatible: calls on distinct workspaces may run concurrently; the
+ *    only global state is a per-device cache (SM count, kernel attributes)
+ *    guarded by a mutex.
+ */
+#ifndef MOE_API_H_
+#define MOE_API_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* bad pointer, shape, alignment or dtype */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but not supported by this build/device */
+  MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5,      /* (device status) a bounded wait ran out */
+  MOE_ERR_DEVICE_CHECK = 6  /* (device status) a device-side check failed */
+} moe_status;
+
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+/* Token-tile choice of the grouped GEMMs. AUTO picks DECODE when the mean
+ * number of tokens per expert (T*k/E) is at most 32, else PREFILL. */
+typedef enum { MOE_TILE_AUTO = 0, MOE_TILE_DECODE = 1, MOE_TILE_PREFILL = 2 } moe_tile;
+
+/* Test hooks (moe_problem.flags). Never set in production. */
+#define MOE_FLAG_TEST_SKIP_SIGNAL 0x1u /* the GEMM producer withholds its first load
+                                          signal, so the consumer's bounded wait runs
+                                          out and reports MOE_ERR_TIMEOUT */
+
+typedef struct {
+  int64_t T;         /* tokens */
+  int64_t H;         /* hidden size */
+  int64_t E;         /* routed experts */
+  int64_t k;         /* experts per token */
+  int64_t I;         /* routed expert intermediate size */
+  int64_t I_shared;  /* shared expert intermediate size; 0 = no shared expert */
+  int32_t renorm;    /* 1: renormalise the gate weights over the chosen k */
+  int32_t dtype;     /* moe_dtype */
+  int32_t tile;      /* moe_tile */
+  uint32_t flags;    /* MOE_FLAG_* test hooks; 0 in production */
+  uint32_t wait_limit_us; /* bound on every device-side wait; 0 = 1 s */
+  int32_t out_f32;   /* nonzero: y is written as fp32 even when dtype is bf16 (the
+                        sum of the slots before its one rounding to bf16) */
+} moe_problem;
+
+/* Bytes of workspace every call below needs for problem `pb`. */
+moe_status moe_workspace_size(const moe_problem* pb, size_t* bytes);
+
+/* Step a1, router logits: logits[t][e] = sum_h x[t][h] W_router[e][h]
+ * (+ router_bias[e]), fp32 accumulation on the CUDA cores (the "Gate" at the
+ * end of stage 2 in the DeepSeek page's five-stage layer breakdown).
+ * router_bias: fp32 [E] or NULL. logits: fp32 [T][E]. */
+moe_status moe_router_logits(const moe_problem* pb, const void* x, const void* W_router,
+                             const float* router_bias, float* logits, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Step a2, routing (DeepSeek page, "MoE Router"): per token the k largest
+ * logits in descending order, lower expert index first among equal logits,
+ * and their softmax gate weights (renorm as above). One warp per token.
+ * logits fp32 [T][E] -> topk_ids int32 [T][k], topk_w fp32 [T][k]. */
+moe_status moe_route(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
+                     int32_t* topk_ids, float* topk_w, void* stream);
+
+/* Step a3, permutation ("CuTeDSL at Perplexity", "Local" dispatch: count the
+ * tokens of each expert, give every token a unique index in its expert's
+ * list). A stable counting sort of the slots s = t*k + r by expert:
+ *   expert_offsets int32 [E+2]: [0..E] exclusive prefix of the per-expert
+ *     counts; [E+1] = [E] + (has_shared ? T : 0) closes the shared segment,
+ *     whose position T*k + t holds token t;
+ *   gather_idx int32 [T*k]: gather_idx[p] = slot at position p (ascending slot
+ *     within each expert);
+ *   slot_pos int32 [T*k]: slot_pos[s] = position of slot s.
+ * No padded buffer is produced. Needs moe_workspace_size() of a problem with
+ * these T, E, k. Out-of-range ids set MOE_ERR_DEVICE_CHECK in the status. */
+moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
+                       int has_shared, int32_t* expert_offsets, int32_t* gather_idx,
+                       int32_t* slot_pos, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Step a4, grouped gate/up GEMM with fused SwiGLU (DeepSeek page "GroupGEMM";
+ * Qwen3.5/TPU write-up 4.2.1-4.2.2). For every routed position p of expert e
+ * (token t = gather_idx[p] / k):
+ *   h[p][i] = silu(x[t] . W_gate[e][i]) * (x[t] . W_up[e][i])
+ * and, when I_shared > 0, h_shared[t][i] likewise with Ws_gate, Ws_up.
+ * Rows of x are gathered inside the GEMM's loads (no gathered copy of x).
+ * h: [T*k][I], h_shared: [T][I_shared] (NULL iff I_shared == 0), in the dtype;
+ * fp32 accumulation, one rounding to the dtype. */
+moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
+                                   const int32_t* expert_offsets, const int32_t* gather_idx,
+                                   const void* W_gate, const void* W_up, const void* Ws_gate,
+                                   const void* Ws_up, void* h, void* h_shared,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Step a5 (+a6), down projection and gate-weighted combine (DeepSeek page
+ * "Expert Parallelism": weighted sum of the routed outputs plus the shared
+ * expert; "CuTeDSL at Perplexity" "Local" combine):
+ *   y[t] = sum_r topk_w[t*k+r] * (W_down[e] h[p]) + W_sdown h_shared[t]
+ * with p = slot_pos[t*k+r] found through gather_idx. The k products per token
+ * are written in fp32 to a slot buffer in the workspace and summed in rank
+ * order (then the shared term) by one reduction kernel. y: [T][H] in the
+ * dtype, or fp32 when pb->out_f32 is set. */
+moe_status moe_down_combine(const moe_problem* pb, const void* h, const void* h_shared,
+                            const int32_t* expert_offsets, const int32_t* gather_idx,
+                            const float* topk_w, const void* W_down, const void* Ws_down,
+                            void* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The whole layer: a1 .. a5 (+a6) on `stream`, intermediates in `workspace`.
+ * Ws_* are NULL iff pb->I_shared == 0; router_bias may be NULL. */
+moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_router,
+                       const float* router_bias, const void* W_gate, const void* W_up,
+                       const void* W_down, const void* Ws_gate, const void* Ws_up,
+                       const void* Ws_down, void* y, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Byte offsets of moe_forward's intermediates inside the workspace (for
+ * inspection by tests): logits, topk_ids, topk_w, expert_offsets, gather_idx,
+ * slot_pos, h, h_shared. Each is -1 when absent. */
+typedef struct {
+  int64_t logits, topk_ids, topk_w, expert_offsets, gather_idx, slot_pos, h, h_shared;
+} moe_workspace_layout;
+moe_status moe_get_workspace_layout(const moe_problem* pb, moe_workspace_layout* out);
+
+/* Synchronises `stream`, then copies the device status word into *out. */
+moe_status moe_get_device_status(const void* workspace, void* stream, moe_status* out);
+
+/* Enqueues a clear of the device status word on `stream`. */
+moe_status moe_reset_device_status(void* workspace, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_API_H_ */

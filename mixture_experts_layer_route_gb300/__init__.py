@@ -1,0 +1,66 @@
+"""GB300 (sm_103a) Mixture-of-Experts FFN layer forward pass.
+
+The compute path is libmoe.so (CUDA kernels behind a C ABI, declared in
+include/moe_api.h); this package only marshals torch tensors into it:
+
+* ``_binding``: one Python function per C entry point, same names.
+* ``MoELayer``: holds the expert weights on the GPU and a workspace, and runs
+  ``moe_forward`` on the current torch stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from ._binding import (  # noqa: F401
+    EXPORTED, MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_FLAG_TEST_SKIP_SIGNAL, MOE_OK,
+    MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_PREFILL, STATUS_NAMES, MoEError, MoEProblem,
+    down_combine, forward, get_device_status, grouped_swiglu_gemm, load_library, make_problem,
+    permute, reset_device_status, route, router_logits, status_string, workspace_layout,
+    workspace_size)
+
+
+class MoELayer:
+    """A MoE FFN layer on one GPU.
+
+    Weights (torch CUDA tensors, contiguous, all of one dtype bf16 or fp32):
+    W_router [E,H], W_gate/W_up [E,I,H], W_down [E,H,I], optional router_bias
+    fp32 [E] and shared expert Ws_gate/Ws_up [Is,H], Ws_down [H,Is].
+    """
+
+    def __init__(self, W_router, W_gate, W_up, W_down, k, router_bias=None, Ws_gate=None,
+                 Ws_up=None, Ws_down=None, renorm=1, tile=MOE_TILE_AUTO):
+        self.W_router, self.W_gate, self.W_up, self.W_down = W_router, W_gate, W_up, W_down
+        self.router_bias = router_bias
+        self.Ws_gate, self.Ws_up, self.Ws_down = Ws_gate, Ws_up, Ws_down
+        self.E, self.I, self.H = W_gate.shape
+        self.I_shared = 0 if Ws_gate is None else Ws_gate.shape[0]
+        self.k, self.renorm, self.tile = k, renorm, tile
+        self.dtype = W_gate.dtype
+        self._ws = {}
+
+    def problem(self, T: int, flags: int = 0, wait_limit_us: int = 0,
+                out_f32: bool = False) -> MoEProblem:
+        return make_problem(T, self.H, self.E, self.k, self.I, self.I_shared, self.renorm,
+                            "bf16" if self.dtype == torch.bfloat16 else "f32", self.tile, flags,
+                            wait_limit_us, out_f32)
+
+    def workspace(self, T: int) -> torch.Tensor:
+        ws = self._ws.get(T)
+        if ws is None:
+            n = workspace_size(self.problem(T))
+            ws = torch.zeros(n, dtype=torch.uint8, device=self.W_gate.device)
+            self._ws[T] = ws
+        return ws
+
+    def forward(self, x, out=None, stream=None, out_f32=False):
+        """y = the layer applied to x [T,H]. out_f32: return y in fp32 (the value
+        before its final rounding to a bf16 layer's dtype)."""
+        T = x.shape[0]
+        odt = torch.float32 if out_f32 else self.dtype
+        y = out if out is not None else torch.empty((T, self.H), dtype=odt, device=x.device)
+        forward(self.problem(T, out_f32=out_f32), x, self.W_router, self.router_bias,
+                self.W_gate, self.W_up, self.W_down, self.Ws_gate, self.Ws_up, self.Ws_down, y,
+                self.workspace(T), stream)
+        return y
+
+    __call__ = forward

@@ -1,0 +1,210 @@
+// Host side of the grouped GEMMs: TMA tensor maps, kernel variants, launch.
+//
+// Variants (token tile BN x pipeline depth), both for bf16 (kind::f16) and
+// fp32 inputs (kind::tf32):
+//   DECODE  BN = 32,  9 stages: a few tokens per expert; the weight stream
+//           dominates, so the ring is deep (9 x 16 KB of weights in flight).
+//   PREFILL BN = 256, 4 stages: hundreds of tokens per expert; tensor-core
+//           bound, 128 x 256 tiles, epilogue overlapped via two accumulators.
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "grouped_gemm.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kMaxExperts = 1024;  // the C ABI's limit on E
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 2-D row-major matrix [rows][cols] of `es`-byte elements; box = 128 bytes of
+// columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  const uint32_t es = dtype == MOE_DTYPE_BF16 ? 2 : 4;
+  const CUtensorMapDataType dt =
+      dtype == MOE_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {128u / es, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct AttrCache {
+  std::mutex mu;
+  // (kernel pointer, device) pairs that already have the smem attribute set.
+  const void* fn[64];
+  int dev[64];
+  int n = 0;
+};
+AttrCache g_attr;
+
+cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_attr.mu);
+  for (int i = 0; i < g_attr.n; ++i)
+    if (g_attr.fn[i] == fn && g_attr.dev[i] == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && g_attr.n < 64) {
+    g_attr.fn[g_attr.n] = fn;
+    g_attr.dev[g_attr.n] = dev;
+    ++g_attr.n;
+  }
+  return e;
+}
+
+template <typename TIn, bool GATED, int BN, int STAGES>
+cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t upper_tiles,
+                           cudaStream_t st) {
+  using C = GemmCfg<TIn, GATED, BN, STAGES>;
+  const size_t smem = C::smem_bytes(E);
+  auto fn = grouped_gemm_kernel<TIn, GATED, BN, STAGES>;
+  // Opt in once to what the largest supported expert count needs, so that a
+  // later call with more experts than the first still fits.
+  cudaError_t e = ensure_smem_attr((const void*)fn, C::smem_bytes(kMaxExperts));
+  if (e != cudaSuccess) return e;
+  size_t grid = (size_t)num_sms;
+  if (upper_tiles < grid) grid = upper_tiles;
+  if (grid == 0) return cudaSuccess;
+  fn<<<(unsigned)grid, C::THREADS, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+// Upper bound of the tile count for any routing of T*k slots over E experts.
+size_t tile_upper_bound(int T, int k, int E, int BN, int routed_blocks, int shared_blocks) {
+  const size_t slots = (size_t)T * k;
+  const size_t used = slots < (size_t)E ? slots : (size_t)E;
+  return (slots / BN + used) * (size_t)routed_blocks +
+         (size_t)((T + BN - 1) / BN) * shared_blocks;
+}
+
+}  // namespace
+
+bool tensor_map_encoder_available() { return encoder() != nullptr; }
+
+cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const int32_t* offsets,
+                               const int32_t* gather_idx, const void* Wg, const void* Wu,
+                               const void* Wsg, const void* Wsu, void* h, void* hs, int* status,
+                               cudaStream_t st) {
+  GroupedGemmArgs a;
+  memset(&a, 0, sizeof(a));
+  const bool has_s = p.Is > 0;
+  bool ok = make_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
+            make_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
+            make_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
+  if (ok && has_s)
+    ok = make_map(&a.tmA[2], Wsg, p.dtype, p.Is, p.H, 64) &&
+         make_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_s) {
+    a.tmA[2] = a.tmA[0];
+    a.tmA[3] = a.tmA[1];
+  }
+  a.tmB[1] = a.tmB[0];
+  a.offsets = offsets;
+  a.gather_idx = gather_idx;
+  a.topk_w = nullptr;
+  a.out = h;
+  a.out_shared = hs;
+  a.status = status;
+  a.limit_ns = p.limit_ns;
+  a.T = p.T;
+  a.k = p.k;
+  a.E = p.E;
+  a.KP = p.k + (has_s ? 1 : 0);
+  a.n_out_routed = p.I;
+  a.n_out_shared = has_s ? p.Is : 64;
+  a.kdim_routed = p.H;
+  a.kdim_shared = p.H;
+  a.ld_out_routed = p.I;
+  a.ld_out_shared = has_s ? p.Is : 0;
+  a.flags = p.flags;
+  const int rb = p.I / 64, sb = has_s ? p.Is / 64 : 0;
+  if (p.tile == MOE_TILE_DECODE) {
+    const size_t ub = tile_upper_bound(p.T, p.k, p.E, 32, rb, sb);
+    return p.dtype == MOE_DTYPE_BF16
+               ? launch_variant<__nv_bfloat16, true, 32, 9>(a, p.num_sms, p.E, ub, st)
+               : launch_variant<float, true, 32, 9>(a, p.num_sms, p.E, ub, st);
+  }
+  const size_t ub = tile_upper_bound(p.T, p.k, p.E, 256, rb, sb);
+  return p.dtype == MOE_DTYPE_BF16
+             ? launch_variant<__nv_bfloat16, true, 256, 4>(a, p.num_sms, p.E, ub, st)
+             : launch_variant<float, true, 256, 4>(a, p.num_sms, p.E, ub, st);
+}
+
+cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
+                             const int32_t* offsets, const int32_t* gather_idx,
+                             const float* topk_w, const void* Wd, const void* Wsd, float* Y,
+                             int* status, cudaStream_t st) {
+  GroupedGemmArgs a;
+  memset(&a, 0, sizeof(a));
+  const bool has_s = p.Is > 0;
+  bool ok = make_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
+            make_map(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, 32);
+  if (ok && has_s)
+    ok = make_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128) &&
+         make_map(&a.tmB[1], hs, p.dtype, p.T, p.Is, 32);
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_s) {
+    a.tmA[2] = a.tmA[0];
+    a.tmB[1] = a.tmB[0];
+  }
+  a.tmA[1] = a.tmA[0];
+  a.tmA[3] = a.tmA[2];
+  a.offsets = offsets;
+  a.gather_idx = gather_idx;
+  a.topk_w = topk_w;
+  a.out = Y;
+  a.out_shared = nullptr;
+  a.status = status;
+  a.limit_ns = p.limit_ns;
+  a.T = p.T;
+  a.k = p.k;
+  a.E = p.E;
+  a.KP = p.k + (has_s ? 1 : 0);
+  a.n_out_routed = p.H;
+  a.n_out_shared = p.H;
+  a.kdim_routed = p.I;
+  a.kdim_shared = has_s ? p.Is : p.I;
+  a.ld_out_routed = p.H;
+  a.ld_out_shared = p.H;
+  a.flags = p.flags;
+  const int rb = p.H / 128, sb = has_s ? p.H / 128 : 0;
+  if (p.tile == MOE_TILE_DECODE) {
+    const size_t ub = tile_upper_bound(p.T, p.k, p.E, 32, rb, sb);
+    return p.dtype == MOE_DTYPE_BF16
+               ? launch_variant<__nv_bfloat16, false, 32, 9>(a, p.num_sms, p.E, ub, st)
+               : launch_variant<float, false, 32, 9>(a, p.num_sms, p.E, ub, st);
+  }
+  const size_t ub = tile_upper_bound(p.T, p.k, p.E, 256, rb, sb);
+  return p.dtype == MOE_DTYPE_BF16
+             ? launch_variant<__nv_bfloat16, false, 256, 4>(a, p.num_sms, p.E, ub, st)
+             : launch_variant<float, false, 256, 4>(a, p.num_sms, p.E, ub, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,425 @@
+// Persistent grouped GEMM over ragged expert segments on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory), fed by TMA.
+//
+// Problem ("GroupGEMM" section of "Lower latency and higher throughput with
+// multi-node DeepSeek deployment"): g groups, group i has m_i rows, each a
+// [m_i, K] x [K, N] product. Here group e < E is routed expert e with the
+// positions [offsets[e], offsets[e+1]) of the permutation; group E is the
+// shared expert with one row per token.
+//
+// Orientation: the weights are the MMA's M = 128 operand and the tokens its N
+// operand ("swap AB"). N is chosen per tile at run time as the segment's
+// remaining rows rounded up to 16, so a ragged segment wastes at most 15
+// columns, and a decode-sized segment (a handful of tokens) streams its
+// expert's weights with a narrow N. The persistent tile scheduler reads the
+// per-expert counts from device memory (no host round trip), as the same page
+// describes for MoE under CUDA Graphs.
+//
+// Two products share the engine:
+//  GATED (step a4, SwiGLU fused): A = 64 rows of W_gate[e] stacked over the
+//    same 64 rows of W_up[e]; B = token rows of x gathered by TMA
+//    (tile::gather4, indices from the permutation; no gathered copy of x
+//    exists). Accumulator lanes 0-63 hold gate, 64-127 up; the epilogue
+//    computes silu(gate) * up and stores h rows (Qwen3.5-397B on TPU v7x,
+//    4.2.1 ragged gather and 4.2.2 grouped GEMM with fused SwiGLU).
+//  DOWN (step a5): A = 128 rows of W_down[e]; B = rows of h (contiguous
+//    positions). The epilogue scales by the token's gate weight and stores the
+//    fp32 product into the token-ordered slot buffer Y[t][r][:] (the combine
+//    sums the slots afterwards in rank order).
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
+// thread) and TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each).
+// A STAGES-deep shared-memory ring (full/empty mbarriers) feeds the MMA; two
+// TMEM accumulators (tfull/tempty mbarriers) let the epilogue of one tile run
+// under the main loop of the next. Every wait is bounded (status word).
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct GroupedGemmArgs {
+  // GATED: [0] routed gate, [1] routed up, [2] shared gate, [3] shared up (64-row box).
+  // DOWN:  [0] routed down, [2] shared down (128-row box).
+  CUtensorMap tmA[4];
+  // GATED: [0] x (1-row box, gather4). DOWN: [0] h, [1] h_shared (32-row box).
+  CUtensorMap tmB[2];
+  const int32_t* offsets;     // [E+2]
+  const int32_t* gather_idx;  // [T*k]
+  const float* topk_w;        // [T*k] (DOWN)
+  void* out;                  // GATED: h [T*k][I]; DOWN: Y fp32 [T][KP][H]
+  void* out_shared;           // GATED: h_shared [T][I_shared]
+  int* status;
+  unsigned long long limit_ns;
+  int T, k, E, KP;            // KP = k + (shared expert ? 1 : 0)
+  int n_out_routed, n_out_shared;   // output features per group
+  int kdim_routed, kdim_shared;     // contraction length per group
+  int ld_out_routed, ld_out_shared; // row stride (elements) of out / out_shared
+  unsigned flags;
+};
+
+template <typename TIn, bool GATED, int BN, int STAGES>
+struct GemmCfg {
+  static constexpr int BM = 128;                     // MMA M (weight rows)
+  static constexpr int WM = GATED ? 64 : 128;        // output features per tile
+  static constexpr int BK = 128 / (int)sizeof(TIn);  // K per stage (one 128-byte row)
+  static constexpr int UMMA_K = 32 / (int)sizeof(TIn);  // K per instruction (32 bytes)
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
+  static constexpr int THREADS = 192;
+  static constexpr bool TF32 = sizeof(TIn) == 4;
+  static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
+                    TMEM_COLS == 512,
+                "TMEM allocation must be a power of two in [32, 512]");
+  static_assert(BN % 32 == 0 && BN <= 256, "token tile");
+
+  static size_t smem_bytes(int E) {
+    return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES + EPI_FLOATS * 4 +
+           (2 * STAGES + 5) * 8 + 16 + 2 * (size_t)(E + 2) * 4;
+  }
+};
+
+struct Tile {
+  int g;        // group (E = shared expert)
+  int nb;       // feature block
+  int mt;       // token tile inside the group
+  int p0;       // first position (routed) / first token (shared)
+  int n_valid;  // rows of this tile
+};
+
+template <int BN, int WM>
+__device__ __forceinline__ Tile decode_tile(int u, const int32_t* prefix, const int32_t* offs,
+                                            int G) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= u) lo = mid;
+    else hi = mid;
+  }
+  Tile t;
+  t.g = lo;
+  const int m = offs[lo + 1] - offs[lo];
+  const int mtiles = (m + BN - 1) / BN;
+  const int local = u - prefix[lo];
+  t.nb = local / mtiles;
+  t.mt = local - t.nb * mtiles;
+  t.p0 = offs[lo] + t.mt * BN;
+  t.n_valid = min(BN, m - t.mt * BN);
+  return t;
+}
+
+template <typename TIn, bool GATED, int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    grouped_gemm_kernel(const __grid_constant__ GroupedGemmArgs args) {
+  using C = GemmCfg<TIn, GATED, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  float* epi = reinterpret_cast<float*>(stages + (size_t)STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_FLOATS);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* epi_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int32_t* prefix = reinterpret_cast<int32_t*>(tmem_holder + 4);
+  int32_t* offs = prefix + (args.E + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = args.E, G = E + 1;
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 1);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmA[i]);
+    for (int i = 0; i < 2; ++i) tma_prefetch_desc(&args.tmB[i]);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+  if (warp == 2) {
+    // Tiles per group: ceil(m_g / BN) x (features_g / WM); exclusive prefix.
+    for (int i = lane; i < G + 1; i += 32) offs[i] = args.offsets[i];
+    __syncwarp();
+    const int per = (G + 31) / 32;
+    const int g0 = lane * per;
+    int local = 0;
+    for (int g = g0; g < min(G, g0 + per); ++g) {
+      const int m = offs[g + 1] - offs[g];
+      const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / C::WM;
+      local += ((m + BN - 1) / BN) * nf;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int g = g0; g < min(G, g0 + per); ++g) {
+      prefix[g] = run;
+      const int m = offs[g + 1] - offs[g];
+      const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / C::WM;
+      run += ((m + BN - 1) / BN) * nf;
+    }
+    if (lane == 31) prefix[G] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = prefix[G];
+  const uint64_t limit = args.limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Decode-sized tiles read each weight tile once: stream it past L2.
+    const uint64_t pol_w = (BN <= 64) ? l2_policy_evict_first() : l2_policy_evict_normal();
+    const uint64_t pol_t = l2_policy_evict_last();
+    uint32_t it = 0;
+    bool ok = true;
+    bool skip_once = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      const bool shared = tl.g == E;
+      const int kdim = shared ? args.kdim_shared : args.kdim_routed;
+      const int a_row0 = (shared ? 0 : tl.g * args.n_out_routed) + tl.nb * C::WM;
+      const CUtensorMap* mA0 = &args.tmA[shared ? 2 : 0];
+      const CUtensorMap* mA1 = &args.tmA[shared ? 3 : 1];
+      uint32_t tx;
+      // GATED: lane l issues gather groups q = l + 32 j (4 rows each).
+      constexpr int NQ = (BN / 4 + 31) / 32;
+      int rows[NQ][4];
+      int n4 = 0, nbox = 0;
+      if constexpr (GATED) {
+        n4 = (tl.n_valid + 3) / 4;
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          const int q = lane + 32 * j;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int jj = min(4 * q + r, tl.n_valid - 1);
+            rows[j][r] = (q < n4) ? (shared ? tl.p0 + jj - offs[E]
+                                            : args.gather_idx[tl.p0 + jj] / args.k)
+                                  : 0;
+          }
+        }
+        tx = C::A_BYTES + n4 * 4 * 128;
+      } else {
+        nbox = (tl.n_valid + 31) / 32;
+        tx = C::A_BYTES + nbox * 32 * 128;
+      }
+      const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
+      for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t round = it / STAGES;
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(empty_bar(s), (round & 1u) ^ 1u, args.status, limit);
+        wok = __shfl_sync(0xffffffffu, wok, 0);
+        if (!wok) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_dst = smem_u32(stages + (size_t)s * C::STAGE_BYTES);
+        const uint32_t b_dst = a_dst + C::A_BYTES;
+        const int kx = kb * C::BK;
+        if (skip_once) {  // test hook: withhold this stage's signal and loads
+          skip_once = false;
+          continue;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full_bar(s), tx);
+          if constexpr (GATED) {
+            tma_load_2d(a_dst, mA0, kx, a_row0, full_bar(s), pol_w);
+            tma_load_2d(a_dst + 64 * 128, mA1, kx, a_row0, full_bar(s), pol_w);
+          } else {
+            tma_load_2d(a_dst, mA0, kx, a_row0, full_bar(s), pol_w);
+            const CUtensorMap* mB = &args.tmB[shared ? 1 : 0];
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(b_dst + b * 32 * 128, mB, kx, b_row0 + 32 * b, full_bar(s), pol_t);
+          }
+        }
+        __syncwarp();
+        if constexpr (GATED) {
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) {
+            const int q = lane + 32 * j;
+            if (q < n4)
+              tma_gather4(b_dst + q * 512, &args.tmB[0], kx, rows[j][0], rows[j][1], rows[j][2],
+                          rows[j][3], full_bar(s), pol_t);
+          }
+        }
+      }
+    }
+    // Let the last loads land before the CTA can exit (bounded, status ignored).
+    if (lane == 0) {
+      const uint32_t n_last = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+      for (uint32_t i = it - n_last; i < it; ++i) {
+        const uint32_t s = i % STAGES, round = i / STAGES;
+        mbar_wait(full_bar(s), round & 1u, nullptr, 20000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, lt = 0;
+      constexpr uint32_t fmt = C::TF32 ? 2u : 1u;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++lt) {
+        const Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+        const int kdim = (tl.g == E) ? args.kdim_shared : args.kdim_routed;
+        const uint32_t acc = lt & 1u, around = lt >> 1;
+        if (!mbar_wait(tempty_bar(acc), (around & 1u) ^ 1u, args.status, limit)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        int n_mma = (tl.n_valid + 15) & ~15;
+        const uint32_t idesc = umma_idesc(fmt, 128, (uint32_t)n_mma);
+        for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t round = it / STAGES;
+          if (!mbar_wait(full_bar(s), round & 1u, args.status, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stages + (size_t)s * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+            umma_issue<C::TF32>(d_tmem, umma_desc_sw128(a_addr + kk * 32),
+                                umma_desc_sw128(b_addr + kk * 32), idesc,
+                                (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+      }
+      // All issued MMAs finished before TMEM is released (bounded, status ignored).
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, nullptr, 20000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int et = threadIdx.x - 64;        // 0..127
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t lt = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++lt) {
+      const Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      const bool shared = tl.g == E;
+      const uint32_t acc = lt & 1u, around = lt >> 1;
+      if (et == 0) *epi_flag = mbar_wait(tfull_bar(acc), around & 1u, args.status, limit) ? 1 : 0;
+      if constexpr (!GATED) {
+        // Per-token destination row in Y and gate weight of this tile.
+        int32_t* yrow = reinterpret_cast<int32_t*>(epi);
+        float* wt = epi + BN;
+        for (int j = et; j < tl.n_valid; j += 128) {
+          int row;
+          float wv;
+          if (shared) {
+            const int t = tl.p0 - offs[E] + j;
+            row = t * args.KP + args.k;
+            wv = 1.0f;
+          } else {
+            const int s = args.gather_idx[tl.p0 + j];
+            const int t = s / args.k;
+            row = t * args.KP + (s - t * args.k);
+            wv = args.topk_w[s];
+          }
+          yrow[j] = row;
+          wt[j] = wv;
+        }
+      }
+      named_barrier_sync(1, 128);
+      if (!*epi_flag) break;  // every epilogue thread sees the same flag
+      tc_fence_after();
+      const uint32_t t_acc = tmem_base + lane_base + acc * BN;
+      if constexpr (GATED) {
+        TIn* out = reinterpret_cast<TIn*>(shared ? args.out_shared : args.out);
+        const int ld = shared ? args.ld_out_shared : args.ld_out_routed;
+        const int row0 = shared ? tl.p0 - offs[E] : tl.p0;
+        const int jj = et >> 2, fg = et & 3;
+        for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+          float v[32];
+          tmem_ld32(t_acc + c0, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) epi[(q * 32 + lane) * 33 + i] = v[i];
+          named_barrier_sync(1, 128);
+          const int j = c0 + jj;
+          if (j < tl.n_valid) {
+            float hv[16];
+#pragma unroll
+            for (int f = 0; f < 16; ++f) {
+              const float g = epi[(fg * 16 + f) * 33 + jj];
+              const float up = epi[(64 + fg * 16 + f) * 33 + jj];
+              hv[f] = g / (1.0f + __expf(-g)) * up;
+            }
+            TIn* dst = out + (size_t)(row0 + j) * ld + tl.nb * 64 + fg * 16;
+            if constexpr (sizeof(TIn) == 2) {
+              uint4 pk[2];
+              uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+              for (int f = 0; f < 8; ++f) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[2 * f], hv[2 * f + 1]);
+                pw[f] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              reinterpret_cast<uint4*>(dst)[0] = pk[0];
+              reinterpret_cast<uint4*>(dst)[1] = pk[1];
+            } else {
+#pragma unroll
+              for (int f = 0; f < 4; ++f)
+                reinterpret_cast<float4*>(dst)[f] =
+                    make_float4(hv[4 * f], hv[4 * f + 1], hv[4 * f + 2], hv[4 * f + 3]);
+            }
+          }
+          tc_fence_before();
+          named_barrier_sync(1, 128);
+        }
+      } else {
+        float* Y = reinterpret_cast<float*>(args.out);
+        const int32_t* yrow = reinterpret_cast<const int32_t*>(epi);
+        const float* wt = epi + BN;
+        const int H = args.n_out_routed;  // == n_out_shared for DOWN
+        const int c = tl.nb * 128 + q * 32 + lane;
+        for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+          float v[32];
+          tmem_ld32(t_acc + c0, v);
+          const int nj = min(32, tl.n_valid - c0);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nj) Y[(size_t)yrow[c0 + i] * H + c] = wt[c0 + i] * v[i];
+        }
+        tc_fence_before();
+        named_barrier_sync(1, 128);
+      }
+      if (et == 0) mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace moe

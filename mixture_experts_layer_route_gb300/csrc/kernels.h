@@ -1,0 +1,51 @@
+// Internal launch functions of the kernels behind the C ABI (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Router (router.cu).
+int router_split_count(int64_t T, int64_t H, int64_t E, int num_sms);
+int router_split_len_ok(int H, int S);
+cudaError_t launch_router_logits(int dtype, const void* x, const void* Wr, const float* bias,
+                                 int T, int H, int E, int S, float* out_partials,
+                                 cudaStream_t st);
+cudaError_t launch_logits_reduce(const float* partials, int S, int T, int E, const float* bias,
+                                 float* logits, int num_sms, cudaStream_t st);
+cudaError_t launch_route(const float* src, int S, const float* bias, int T, int E, int k,
+                         int renorm, float* logits_out, int32_t* ids, float* w,
+                         cudaStream_t st);
+
+// Permutation (permute.cu).
+size_t permute_smem_bytes(int E);
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int has_shared,
+                           int32_t* offsets, int32_t* gather_idx, int32_t* slot_pos, int* status,
+                           cudaStream_t st);
+
+// Grouped GEMMs (grouped_gemm.cu).
+struct GemmProblem {
+  int dtype;  // MOE_DTYPE_*
+  int tile;   // MOE_TILE_DECODE or MOE_TILE_PREFILL (resolved)
+  int T, H, E, k, I, Is;
+  unsigned flags;
+  unsigned long long limit_ns;
+  int num_sms;
+};
+cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const int32_t* offsets,
+                               const int32_t* gather_idx, const void* Wg, const void* Wu,
+                               const void* Wsg, const void* Wsu, void* h, void* hs, int* status,
+                               cudaStream_t st);
+cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
+                             const int32_t* offsets, const int32_t* gather_idx,
+                             const float* topk_w, const void* Wd, const void* Wsd, float* Y,
+                             int* status, cudaStream_t st);
+bool tensor_map_encoder_available();
+
+// Combine (combine.cu): y[t] = sum_j Y[t][j] for j < KP, rank order.
+cudaError_t launch_combine(int dtype, const float* Y, int T, int H, int KP, void* y,
+                           int num_sms, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,348 @@
+// C ABI entry points: argument validation, workspace layout, kernel sequence.
+// Every launch goes to the caller's stream; nothing here synchronises except
+// moe_get_device_status().
+#include <mutex>
+
+#include "moe_api.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeader = 256;  // status word + reserved
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t logits, partials, ids, w, offsets, gather, slotpos, h, hs, Y, total;
+  int S;  // router split count
+};
+
+std::mutex g_sm_mu;
+int g_sm_count[64] = {0};
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(g_sm_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 148;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+// Number of SMs used to size the router split; a fixed value keeps the
+// workspace size independent of the device queried.
+constexpr int kRouterSplitSms = 152;
+
+size_t elem_bytes(int dtype) { return dtype == MOE_DTYPE_BF16 ? 2 : 4; }
+
+Layout layout_of(const moe_problem& p) {
+  Layout L;
+  const size_t es = elem_bytes(p.dtype);
+  const size_t T = (size_t)p.T, E = (size_t)p.E, k = (size_t)p.k;
+  const size_t KP = k + (p.I_shared > 0 ? 1 : 0);
+  L.S = router_split_count(p.T, p.H, p.E, kRouterSplitSms);
+  size_t off = kHeader;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  L.logits = take(T * E * 4);
+  L.partials = L.S > 1 ? take((size_t)L.S * T * E * 4) : L.logits;
+  L.ids = take(T * k * 4);
+  L.w = take(T * k * 4);
+  L.offsets = take((E + 2) * 4);
+  L.gather = take(T * k * 4);
+  L.slotpos = take(T * k * 4);
+  L.h = take(T * k * (size_t)p.I * es);
+  L.hs = p.I_shared > 0 ? take(T * (size_t)p.I_shared * es) : 0;
+  L.Y = take(T * KP * (size_t)p.H * 4);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_problem(const moe_problem* pb) {
+  if (!pb) return MOE_ERR_INVALID_ARG;
+  const moe_problem& p = *pb;
+  if (p.T < 0 || p.H <= 0 || p.E <= 0 || p.k <= 0 || p.I <= 0 || p.I_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (p.k > p.E || p.k > 32 || p.E > 1024) return MOE_ERR_INVALID_ARG;
+  if (p.H % 128 != 0 || p.I % 64 != 0 || p.I_shared % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+  if (p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_PREFILL) return MOE_ERR_INVALID_ARG;
+  if (p.renorm != 0 && p.renorm != 1) return MOE_ERR_INVALID_ARG;
+  if (p.out_f32 != 0 && p.out_f32 != 1) return MOE_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t)1 << 30;
+  if (p.T * (p.k + 1) >= lim || p.H >= lim || p.I >= lim || p.E * p.I >= lim ||
+      p.E * p.H >= lim)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int resolve_tile(const moe_problem& p) {
+  if (p.tile != MOE_TILE_AUTO) return p.tile;
+  return (p.T * p.k <= 32 * p.E) ? MOE_TILE_DECODE : MOE_TILE_PREFILL;
+}
+
+GemmProblem gemm_problem(const moe_problem& p) {
+  GemmProblem g;
+  g.dtype = p.dtype;
+  g.tile = resolve_tile(p);
+  g.T = (int)p.T;
+  g.H = (int)p.H;
+  g.E = (int)p.E;
+  g.k = (int)p.k;
+  g.I = (int)p.I;
+  g.Is = (int)p.I_shared;
+  g.flags = p.flags;
+  g.limit_ns = (unsigned long long)(p.wait_limit_us ? p.wait_limit_us : 1000000u) * 1000ull;
+  g.num_sms = sm_count();
+  return g;
+}
+
+int* status_ptr(void* ws) { return reinterpret_cast<int*>(ws); }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(reinterpret_cast<uint8_t*>(ws) + off);
+}
+
+moe_status check_ws(const void* ws, size_t have, size_t need) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  if (have < need) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_workspace_size(const moe_problem* pb, size_t* bytes) {
+  moe_status s = check_problem(pb);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = layout_of(*pb).total;
+  return MOE_OK;
+}
+
+moe_status moe_get_workspace_layout(const moe_problem* pb, moe_workspace_layout* out) {
+  moe_status s = check_problem(pb);
+  if (s != MOE_OK) return s;
+  if (!out) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*pb);
+  out->logits = (int64_t)L.logits;
+  out->topk_ids = (int64_t)L.ids;
+  out->topk_w = (int64_t)L.w;
+  out->expert_offsets = (int64_t)L.offsets;
+  out->gather_idx = (int64_t)L.gather;
+  out->slot_pos = (int64_t)L.slotpos;
+  out->h = (int64_t)L.h;
+  out->h_shared = pb->I_shared > 0 ? (int64_t)L.hs : -1;
+  return MOE_OK;
+}
+
+moe_status moe_router_logits(const moe_problem* pb, const void* x, const void* W_router,
+                             const float* router_bias, float* logits, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  moe_status s = check_problem(pb);
+  if (s != MOE_OK) return s;
+  const Layout L = layout_of(*pb);
+  if (pb->T == 0) return MOE_OK;
+  if (!x || !W_router || !logits) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_router) || !aligned16(logits) ||
+      (router_bias && !aligned16(router_bias)))
+    return MOE_ERR_INVALID_ARG;
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int T = (int)pb->T, H = (int)pb->H, E = (int)pb->E;
+  if (L.S == 1)
+    return cuda_status(launch_router_logits(pb->dtype, x, W_router, router_bias, T, H, E, 1,
+                                            logits, st));
+  float* part = at<float>(workspace, L.partials);
+  cudaError_t e = launch_router_logits(pb->dtype, x, W_router, router_bias, T, H, E, L.S, part, st);
+  if (e == cudaSuccess) e = launch_logits_reduce(part, L.S, T, E, router_bias, logits, sm_count(), st);
+  return cuda_status(e);
+}
+
+moe_status moe_route(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
+                     int32_t* topk_ids, float* topk_w, void* stream) {
+  if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
+  if (renorm != 0 && renorm != 1) return MOE_ERR_INVALID_ARG;
+  if (T * E >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route(logits, 1, nullptr, (int)T, (int)E, (int)k, renorm, nullptr,
+                                  topk_ids, topk_w, (cudaStream_t)stream));
+}
+
+moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
+                       int has_shared, int32_t* expert_offsets, int32_t* gather_idx,
+                       int32_t* slot_pos, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
+  if (T * (k + 1) >= ((int64_t)1 << 30)) return MOE_ERR_UNSUPPORTED;
+  if (!expert_offsets || (T > 0 && (!topk_ids || !gather_idx || !slot_pos)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(expert_offsets) || (T > 0 && (!aligned16(topk_ids) || !aligned16(gather_idx) ||
+                                               !aligned16(slot_pos))))
+    return MOE_ERR_INVALID_ARG;
+  moe_status s = check_ws(workspace, workspace_bytes, kHeader);
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_permute(topk_ids, (int)T, (int)E, (int)k, has_shared ? 1 : 0,
+                                    expert_offsets, gather_idx, slot_pos,
+                                    status_ptr(workspace), (cudaStream_t)stream));
+}
+
+moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
+                                   const int32_t* expert_offsets, const int32_t* gather_idx,
+                                   const void* W_gate, const void* W_up, const void* Ws_gate,
+                                   const void* Ws_up, void* h, void* h_shared,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status s = check_problem(pb);
+  if (s != MOE_OK) return s;
+  if (pb->T == 0) return MOE_OK;
+  const bool has_s = pb->I_shared > 0;
+  if (!x || !expert_offsets || !gather_idx || !W_gate || !W_up || !h) return MOE_ERR_INVALID_ARG;
+  if (has_s != (Ws_gate != nullptr) || has_s != (Ws_up != nullptr) ||
+      has_s != (h_shared != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, expert_offsets, gather_idx, W_gate, W_up, h};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (has_s && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(h_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if ((s = check_ws(workspace, workspace_bytes, kHeader)) != MOE_OK) return s;
+  if (!tensor_map_encoder_available()) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_swiglu_gemm(gemm_problem(*pb), x, expert_offsets, gather_idx, W_gate,
+                                        W_up, Ws_gate, Ws_up, h, h_shared,
+                                        status_ptr(workspace), (cudaStream_t)stream));
+}
+
+moe_status moe_down_combine(const moe_problem* pb, const void* h, const void* h_shared,
+                            const int32_t* expert_offsets, const int32_t* gather_idx,
+                            const float* topk_w, const void* W_down, const void* Ws_down,
+                            void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status s = check_problem(pb);
+  if (s != MOE_OK) return s;
+  if (pb->T == 0) return MOE_OK;
+  const bool has_s = pb->I_shared > 0;
+  if (!h || !expert_offsets || !gather_idx || !topk_w || !W_down || !y) return MOE_ERR_INVALID_ARG;
+  if (has_s != (Ws_down != nullptr) || has_s != (h_shared != nullptr)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {h, expert_offsets, gather_idx, topk_w, W_down, y};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (has_s && (!aligned16(Ws_down) || !aligned16(h_shared))) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*pb);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return s;
+  if (!tensor_map_encoder_available()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  const GemmProblem g = gemm_problem(*pb);
+  float* Y = at<float>(workspace, L.Y);
+  cudaError_t e = launch_down_gemm(g, h, h_shared, expert_offsets, gather_idx, topk_w, W_down,
+                                   Ws_down, Y, status_ptr(workspace), st);
+  if (e == cudaSuccess)
+    e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : pb->dtype, Y, g.T, g.H,
+                       g.k + (has_s ? 1 : 0), y, g.num_sms, st);
+  return cuda_status(e);
+}
+
+moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_router,
+                       const float* router_bias, const void* W_gate, const void* W_up,
+                       const void* W_down, const void* Ws_gate, const void* Ws_up,
+                       const void* Ws_down, void* y, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  moe_status s = check_problem(pb);
+  if (s != MOE_OK) return s;
+  if (pb->T == 0) return MOE_OK;
+  const bool has_s = pb->I_shared > 0;
+  if (!x || !W_router || !W_gate || !W_up || !W_down || !y) return MOE_ERR_INVALID_ARG;
+  if (has_s != (Ws_gate != nullptr) || has_s != (Ws_up != nullptr) ||
+      has_s != (Ws_down != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, W_router, W_gate, W_up, W_down, y};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (router_bias && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
+  if (has_s && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(Ws_down)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*pb);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return s;
+  if (!tensor_map_encoder_available()) return MOE_ERR_UNSUPPORTED;
+
+  cudaStream_t st = (cudaStream_t)stream;
+  const GemmProblem g = gemm_problem(*pb);
+  int* status = status_ptr(workspace);
+  float* logits = at<float>(workspace, L.logits);
+  float* part = at<float>(workspace, L.partials);
+  int32_t* ids = at<int32_t>(workspace, L.ids);
+  float* w = at<float>(workspace, L.w);
+  int32_t* offs = at<int32_t>(workspace, L.offsets);
+  int32_t* gidx = at<int32_t>(workspace, L.gather);
+  int32_t* spos = at<int32_t>(workspace, L.slotpos);
+  void* h = at<void>(workspace, L.h);
+  void* hs = has_s ? at<void>(workspace, L.hs) : nullptr;
+  float* Y = at<float>(workspace, L.Y);
+
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+  if (e == cudaSuccess)
+    e = launch_router_logits(pb->dtype, x, W_router, router_bias, g.T, g.H, g.E, L.S, part, st);
+  if (e == cudaSuccess)
+    e = launch_route(part, L.S, router_bias, g.T, g.E, g.k, pb->renorm,
+                     L.S > 1 ? logits : nullptr, ids, w, st);
+  if (e == cudaSuccess)
+    e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status, st);
+  if (e == cudaSuccess)
+    e = launch_swiglu_gemm(g, x, offs, gidx, W_gate, W_up, Ws_gate, Ws_up, h, hs, status, st);
+  if (e == cudaSuccess)
+    e = launch_down_gemm(g, h, hs, offs, gidx, w, W_down, Ws_down, Y, status, st);
+  if (e == cudaSuccess)
+    e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : pb->dtype, Y, g.T, g.H,
+                       g.k + (has_s ? 1 : 0), y, g.num_sms, st);
+  return cuda_status(e);
+}
+
+moe_status moe_get_device_status(const void* workspace, void* stream, moe_status* out) {
+  if (!workspace || !out) return MOE_ERR_INVALID_ARG;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  *out = (moe_status)v;
+  return MOE_OK;
+}
+
+moe_status moe_reset_device_status(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(int), (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -68,6 +68,16 @@ CONFIGS = {
     "deepseek_v3": MoEConfig("deepseek_v3", T=4096, H=7168, E=256, k=8, I=2048, I_shared=2048),
 }
 
+# Reduced shapes for ncu captures: the same per-expert token counts and matrix
+# sizes as the decode / prefill layers above, with fewer experts so that a
+# capture holds ~1.5 GB on the device (still well above the 129 MB L2).
+PROFILE_CONFIGS = {
+    "qwen3_235b_prefill_e32": MoEConfig("qwen3_235b_prefill_e32", T=2048, H=4096, E=32, k=8,
+                                        I=1536),
+    "qwen3_235b_decode_e32": MoEConfig("qwen3_235b_decode_e32", T=16, H=4096, E=32, k=8,
+                                       I=1536),
+}
+
 
 def _randn(shape, gen, device, scale, dtype, chunk_rows=None):
     """N(0, scale^2) drawn in fp32 and rounded to dtype, chunked along dim 0."""

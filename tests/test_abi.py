@@ -1,0 +1,117 @@
+"""The C-ABI library loads, exports every symbol include/moe_api.h declares,
+and rejects bad arguments on the host before touching a GPU (CPU only: no
+call here reaches the CUDA runtime)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_route_gb300 as m
+from mixture_experts_layer_route_gb300 import build as build_mod
+from moe_inputs import CONFIGS
+
+HEADER = os.path.join(os.path.dirname(__file__), "..", "include", "moe_api.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return m.load_library()
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_names():
+    assert sorted(m.EXPORTED) == declared_symbols()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_library_has_no_driver_link_dependency():
+    # The driver entry point is looked up at run time; the library must load on
+    # a host without libcuda (this one).
+    import subprocess
+    out = subprocess.run(["ldd", m._binding.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
+
+
+def test_status_strings(lib):
+    for code, name in m.STATUS_NAMES.items():
+        assert m.status_string(code) == name
+
+
+@pytest.mark.parametrize("name", sorted(CONFIGS))
+def test_workspace_size_of_each_config(lib, name):
+    c = CONFIGS[name]
+    pb = m.make_problem(c.T, c.H, c.E, c.k, c.I, c.I_shared, c.renorm, c.dtype)
+    n = m.workspace_size(pb)
+    KP = c.k + (1 if c.I_shared else 0)
+    # at least the fp32 slot buffer and h
+    assert n >= c.T * KP * c.H * 4 + c.T * c.k * c.I * c.elem_bytes
+    lay = m.workspace_layout(pb)
+    assert all(v % 256 == 0 for v in lay.values() if v >= 0)
+    assert (lay["h_shared"] >= 0) == bool(c.I_shared)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=9, E=8), 1), (dict(k=0), 1), (dict(H=200), 1), (dict(I=100), 1),
+    (dict(I_shared=96), 1), (dict(E=2000, k=2), 1), (dict(k=33, E=64), 1), (dict(T=-1), 1),
+])
+def test_invalid_problem_rejected_on_host(lib, kw, code):
+    base = dict(T=64, H=256, E=8, k=2, I=128, I_shared=0)
+    base.update(kw)
+    pb = m.make_problem(**base)
+    with pytest.raises(m.MoEError) as ei:
+        m.workspace_size(pb)
+    assert ei.value.code == code
+
+
+def test_forward_null_pointers_rejected_on_host(lib):
+    pb = m.make_problem(64, 256, 8, 2, 128)
+    rc = lib.moe_forward(ctypes.byref(pb), None, None, None, None, None, None, None, None,
+                         None, None, None, 0, None)
+    assert rc == 1  # MOE_ERR_INVALID_ARG
+
+
+def test_forward_misaligned_pointer_rejected_on_host(lib):
+    pb = m.make_problem(64, 256, 8, 2, 128)
+    rc = lib.moe_forward(ctypes.byref(pb), 0x1008, 0x2000, None, 0x3000, 0x4000, 0x5000, None,
+                         None, None, 0x6000, 0x7000, 1 << 30, None)
+    assert rc == 1
+
+
+def test_forward_small_workspace_rejected_on_host(lib):
+    pb = m.make_problem(64, 256, 8, 2, 128)
+    rc = lib.moe_forward(ctypes.byref(pb), 0x1000, 0x2000, None, 0x3000, 0x4000, 0x5000, None,
+                         None, None, 0x6000, 0x7000, 1024, None)
+    assert rc == 3  # MOE_ERR_WORKSPACE
+
+
+def test_shared_pointer_mismatch_rejected_on_host(lib):
+    pb = m.make_problem(64, 256, 8, 2, 128, I_shared=64)
+    rc = lib.moe_forward(ctypes.byref(pb), 0x1000, 0x2000, None, 0x3000, 0x4000, 0x5000, None,
+                         None, None, 0x6000, 0x7000, 1 << 30, None)
+    assert rc == 1
+
+
+def test_route_and_permute_bad_shapes_rejected_on_host(lib):
+    assert lib.moe_route(0x1000, 4, 8, 9, 1, 0x2000, 0x3000, None) == 1
+    assert lib.moe_route(0x1000, 4, 8, 2, 2, 0x2000, 0x3000, None) == 1
+    assert lib.moe_permute(0x1000, 4, 8, 0, 0, 0x2000, 0x3000, 0x4000, 0x5000, 4096, None) == 1
+    assert lib.moe_permute(0x1000, 4, 8, 2, 0, 0x2000, 0x3000, 0x4000, 0x5000, 16, None) == 3
+
+
+def test_zero_tokens_is_ok_without_launch(lib):
+    pb = m.make_problem(0, 256, 8, 2, 128)
+    rc = lib.moe_forward(ctypes.byref(pb), None, None, None, None, None, None, None, None, None,
+                         None, None, 0, None)
+    assert rc == 0
