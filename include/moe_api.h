@@ -161,6 +161,33 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
                        const void* Ws_down, void* y, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/* moe_down_combine without a workspace, for callers that cannot allocate
+ * device memory (a host that passes the layer only its inputs and outputs, a
+ * plugin not allowed to call cudaMalloc, a fixed memory budget). It computes
+ * what moe_down_combine computes, with the same arguments minus the
+ * workspace; its scratch (status word + fp32 slot buffer) is one static
+ * device array of 16 MiB + 256 bytes inside this library, which every GPU that
+ * loads the library holds until the process exits. There is no counterpart on
+ * the pages: this is a deployment convenience only.
+ *  - Size limit: T * (k + (I_shared > 0)) * H * 4 bytes must not exceed 16 MiB
+ *    (e.g. T = 128 decode tokens at H = 4096, k = 8); larger problems return
+ *    MOE_ERR_WORKSPACE before any launch.
+ *  - Allocates nothing: no cudaMalloc/cudaFree or allocating library call.
+ *    The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (different
+ *    streams or threads, same device) race on it and must be serialised by
+ *    the caller. The status word is cleared at the start of every call.
+ *  - device_status: NULL, or a HOST pointer; when given, the call waits for
+ *    `stream` and stores the device status word (MOE_OK, MOE_ERR_TIMEOUT...).
+ */
+moe_status moe_down_combine_noalloc(const moe_problem* pb, const void* h, const void* h_shared,
+                                    const int32_t* expert_offsets, const int32_t* gather_idx,
+                                    const float* topk_w, const void* W_down,
+                                    const void* Ws_down, void* y, void* stream,
+                                    moe_status* device_status);
+
 /* Byte offsets of moe_forward's intermediates inside the workspace (for
  * inspection by tests): logits, topk_ids, topk_w, expert_offsets, gather_idx,
  * slot_pos, h, h_shared. Each is -1 when absent. */

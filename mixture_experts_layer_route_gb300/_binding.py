@@ -26,7 +26,7 @@ MOE_FLAG_TEST_SKIP_SIGNAL = 0x1
 EXPORTED = ("moe_workspace_size", "moe_router_logits", "moe_route", "moe_permute",
             "moe_grouped_swiglu_gemm", "moe_down_combine", "moe_forward",
             "moe_get_workspace_layout", "moe_get_device_status", "moe_reset_device_status",
-            "moe_status_string")
+            "moe_status_string", "moe_down_combine_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -79,6 +79,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_get_workspace_layout": [pb, ctypes.POINTER(MoEWorkspaceLayout)],
             "moe_get_device_status": [_P, _P, ctypes.POINTER(ctypes.c_int)],
             "moe_reset_device_status": [_P, _P],
+            "moe_down_combine_noalloc": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                         ctypes.POINTER(ctypes.c_int)],
         }
         for name, argt in sig.items():
             f = getattr(lib, name)
@@ -168,6 +170,18 @@ def down_combine(problem, h, h_shared, expert_offsets, gather_idx, topk_w, W_dow
         ctypes.byref(problem), _ptr(h), _ptr(h_shared), _ptr(expert_offsets), _ptr(gather_idx),
         _ptr(topk_w), _ptr(W_down), _ptr(Ws_down), _ptr(y), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def down_combine_noalloc(problem, h, h_shared, expert_offsets, gather_idx, topk_w, W_down,
+                         Ws_down, y, stream=None, want_status=False):
+    """moe_down_combine without a workspace (the library's static scratch).
+    With want_status, waits for the stream and returns the device status."""
+    st = ctypes.c_int(-1)
+    _check("moe_down_combine_noalloc", load_library().moe_down_combine_noalloc(
+        ctypes.byref(problem), _ptr(h), _ptr(h_shared), _ptr(expert_offsets), _ptr(gather_idx),
+        _ptr(topk_w), _ptr(W_down), _ptr(Ws_down), _ptr(y), _stream(stream),
+        ctypes.byref(st) if want_status else None))
+    return int(st.value) if want_status else None
 
 
 def forward(problem, x, W_router, router_bias, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
