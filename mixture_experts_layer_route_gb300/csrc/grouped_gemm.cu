@@ -1,11 +1,14 @@
 // Host side of the grouped GEMMs: TMA tensor maps, kernel variants, launch.
 //
-// Variants (token tile BN x pipeline depth), both for bf16 (kind::f16) and
-// fp32 inputs (kind::tf32):
+// Variants (token tile BN x pipeline depth, token-operand mode), both for bf16
+// (kind::f16) and fp32 inputs (kind::tf32):
 //   DECODE  BN = 32,  9 stages: a few tokens per expert; the weight stream
 //           dominates, so the ring is deep (9 x 16 KB of weights in flight).
+//           Gated: tokens by TMA gather4 (8 instructions per stage).
 //   PREFILL BN = 256, 4 stages: hundreds of tokens per expert; tensor-core
 //           bound, 128 x 256 tiles, epilogue overlapped via two accumulators.
+//           Gated: tokens gathered by four cp.async warps.
+// The down projection always loads its h rows as one TMA box of BN rows.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -78,12 +81,12 @@ cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
   return e;
 }
 
-template <typename TIn, bool GATED, int BN, int STAGES>
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE>
 cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t upper_tiles,
                            cudaStream_t st) {
-  using C = GemmCfg<TIn, GATED, BN, STAGES>;
+  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE>;
   const size_t smem = C::smem_bytes(E);
-  auto fn = grouped_gemm_kernel<TIn, GATED, BN, STAGES>;
+  auto fn = grouped_gemm_kernel<TIn, GATED, BN, STAGES, BMODE>;
   // Opt in once to what the largest supported expert count needs, so that a
   // later call with more experts than the first still fits.
   cudaError_t e = ensure_smem_attr((const void*)fn, C::smem_bytes(kMaxExperts));
@@ -126,6 +129,7 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const int32_
     a.tmA[3] = a.tmA[1];
   }
   a.tmB[1] = a.tmB[0];
+  a.b_src = x;
   a.offsets = offsets;
   a.gather_idx = gather_idx;
   a.topk_w = nullptr;
@@ -148,13 +152,13 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const int32_
   if (p.tile == MOE_TILE_DECODE) {
     const size_t ub = tile_upper_bound(p.T, p.k, p.E, 32, rb, sb);
     return p.dtype == MOE_DTYPE_BF16
-               ? launch_variant<__nv_bfloat16, true, 32, 9>(a, p.num_sms, p.E, ub, st)
-               : launch_variant<float, true, 32, 9>(a, p.num_sms, p.E, ub, st);
+               ? launch_variant<__nv_bfloat16, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st)
+               : launch_variant<float, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st);
   }
   const size_t ub = tile_upper_bound(p.T, p.k, p.E, 256, rb, sb);
   return p.dtype == MOE_DTYPE_BF16
-             ? launch_variant<__nv_bfloat16, true, 256, 4>(a, p.num_sms, p.E, ub, st)
-             : launch_variant<float, true, 256, 4>(a, p.num_sms, p.E, ub, st);
+             ? launch_variant<__nv_bfloat16, true, 256, 4, kCpAsync>(a, p.num_sms, p.E, ub, st)
+             : launch_variant<float, true, 256, 4, kCpAsync>(a, p.num_sms, p.E, ub, st);
 }
 
 cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
@@ -164,11 +168,12 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
   GroupedGemmArgs a;
   memset(&a, 0, sizeof(a));
   const bool has_s = p.Is > 0;
+  const uint32_t bn = p.tile == MOE_TILE_DECODE ? 32 : 256;  // token box = token tile
   bool ok = make_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
-            make_map(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, 32);
+            make_map(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, bn);
   if (ok && has_s)
     ok = make_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128) &&
-         make_map(&a.tmB[1], hs, p.dtype, p.T, p.Is, 32);
+         make_map(&a.tmB[1], hs, p.dtype, p.T, p.Is, bn);
   if (!ok) return cudaErrorInvalidValue;
   if (!has_s) {
     a.tmA[2] = a.tmA[0];
@@ -198,13 +203,13 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
   if (p.tile == MOE_TILE_DECODE) {
     const size_t ub = tile_upper_bound(p.T, p.k, p.E, 32, rb, sb);
     return p.dtype == MOE_DTYPE_BF16
-               ? launch_variant<__nv_bfloat16, false, 32, 9>(a, p.num_sms, p.E, ub, st)
-               : launch_variant<float, false, 32, 9>(a, p.num_sms, p.E, ub, st);
+               ? launch_variant<__nv_bfloat16, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st)
+               : launch_variant<float, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st);
   }
   const size_t ub = tile_upper_bound(p.T, p.k, p.E, 256, rb, sb);
   return p.dtype == MOE_DTYPE_BF16
-             ? launch_variant<__nv_bfloat16, false, 256, 4>(a, p.num_sms, p.E, ub, st)
-             : launch_variant<float, false, 256, 4>(a, p.num_sms, p.E, ub, st);
+             ? launch_variant<__nv_bfloat16, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st)
+             : launch_variant<float, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
 }
 
 }  // namespace moe

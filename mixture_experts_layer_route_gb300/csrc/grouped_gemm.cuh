@@ -27,8 +27,21 @@
 //    fp32 product into the token-ordered slot buffer Y[t][r][:] (the combine
 //    sums the slots afterwards in rank order).
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
-// thread) and TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each).
+// Token-operand loading (B), one of three modes:
+//  kGather4 (decode-sized gated tiles): TMA tile::gather4, 4 rows per
+//    instruction straight from x by token index.
+//  kCpAsync (prefill-sized gated tiles): four extra producer warps copy the
+//    tile's token rows from x with 16-byte cp.async into the 128-byte-swizzled
+//    layout, then make them visible to the tensor core (async proxy) with
+//    fence.proxy.async before arriving on the stage barrier. An SM accepts only
+//    one TMA instruction every ~70-150 cycles, so 4-row gathers cannot fill a
+//    256-token stage in time; the load/store unit can.
+//  kTiled (down projection): the tile's h rows are contiguous, one TMA box.
+// All TMA loads of a stage are issued in one SIMT step with per-lane operands.
+//
+// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread) and
+// TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each), warps 6-9
+// (kCpAsync only) = token-row gather.
 // A STAGES-deep shared-memory ring (full/empty mbarriers) feeds the MMA; two
 // TMEM accumulators (tfull/tempty mbarriers) let the epilogue of one tile run
 // under the main loop of the next. Every wait is bounded (status word).
@@ -44,6 +57,7 @@ struct GroupedGemmArgs {
   CUtensorMap tmA[4];
   // GATED: [0] x (1-row box, gather4). DOWN: [0] h, [1] h_shared (32-row box).
   CUtensorMap tmB[2];
+  const void* b_src;          // kCpAsync: x [T][H] (token rows are gathered from it)
   const int32_t* offsets;     // [E+2]
   const int32_t* gather_idx;  // [T*k]
   const float* topk_w;        // [T*k] (DOWN)
@@ -58,7 +72,9 @@ struct GroupedGemmArgs {
   unsigned flags;
 };
 
-template <typename TIn, bool GATED, int BN, int STAGES>
+enum BMode : int { kGather4 = 0, kCpAsync = 1, kTiled = 2 };
+
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE>
 struct GemmCfg {
   static constexpr int BM = 128;                     // MMA M (weight rows)
   static constexpr int WM = GATED ? 64 : 128;        // output features per tile
@@ -69,7 +85,9 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
-  static constexpr int THREADS = 192;
+  static constexpr int GATHER_WARPS = (BMODE == kCpAsync) ? 4 : 0;
+  static constexpr int THREADS = 192 + 32 * GATHER_WARPS;
+  static constexpr int CP_LAG = STAGES - 2;  // stages of cp.async in flight per thread
   static constexpr bool TF32 = sizeof(TIn) == 4;
   static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
                     TMEM_COLS == 512,
@@ -111,10 +129,11 @@ __device__ __forceinline__ Tile decode_tile(int u, const int32_t* prefix, const 
   return t;
 }
 
-template <typename TIn, bool GATED, int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE>
+__global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GroupedGemmArgs args) {
-  using C = GemmCfg<TIn, GATED, BN, STAGES>;
+  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE>;
+  static_assert(GATED || BMODE == kTiled, "the down projection reads contiguous h rows");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -137,7 +156,7 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 1 + C::GATHER_WARPS);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -201,12 +220,12 @@ __global__ void __launch_bounds__(192, 1)
       const int a_row0 = (shared ? 0 : tl.g * args.n_out_routed) + tl.nb * C::WM;
       const CUtensorMap* mA0 = &args.tmA[shared ? 2 : 0];
       const CUtensorMap* mA1 = &args.tmA[shared ? 3 : 1];
-      uint32_t tx;
-      // GATED: lane l issues gather groups q = l + 32 j (4 rows each).
-      constexpr int NQ = (BN / 4 + 31) / 32;
+      // gather4 groups: lane l issues groups q = l + 32 j (4 rows each).
+      constexpr int NQ = (BMODE == kGather4) ? (BN / 4 + 31) / 32 : 1;
       int rows[NQ][4];
-      int n4 = 0, nbox = 0;
-      if constexpr (GATED) {
+      int n4 = 0;
+      uint32_t tx = C::A_BYTES;
+      if constexpr (BMODE == kGather4) {
         n4 = (tl.n_valid + 3) / 4;
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
@@ -219,12 +238,29 @@ __global__ void __launch_bounds__(192, 1)
                                   : 0;
           }
         }
-        tx = C::A_BYTES + n4 * 4 * 128;
-      } else {
-        nbox = (tl.n_valid + 31) / 32;
-        tx = C::A_BYTES + nbox * 32 * 128;
+        tx += n4 * 4 * 128;
+      } else if constexpr (BMODE == kTiled) {
+        tx += BN * 128;  // one box of BN rows; rows past the segment are loaded, unused
       }
       const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
+      // Per-lane operands of this tile's TMA loads (one SIMT step per stage):
+      // GATED: lanes 0, 1 = gate, up rows; DOWN: lane 0 = W_down rows, lane 1 = h rows.
+      constexpr int NA = GATED ? 2 : 1;
+      constexpr int NLOADS = NA + (BMODE == kTiled ? 1 : 0);
+      const CUtensorMap* my_map = mA0;
+      int my_row = a_row0;
+      uint32_t my_off = 0;
+      uint64_t my_pol = pol_w;
+      if (GATED && lane == 1) {
+        my_map = mA1;
+        my_off = 64 * 128;
+      }
+      if (BMODE == kTiled && lane == NA) {
+        my_map = &args.tmB[shared ? 1 : 0];
+        my_row = b_row0;
+        my_off = C::A_BYTES;
+        my_pol = pol_t;
+      }
       for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
@@ -242,20 +278,10 @@ __global__ void __launch_bounds__(192, 1)
           skip_once = false;
           continue;
         }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full_bar(s), tx);
-          if constexpr (GATED) {
-            tma_load_2d(a_dst, mA0, kx, a_row0, full_bar(s), pol_w);
-            tma_load_2d(a_dst + 64 * 128, mA1, kx, a_row0, full_bar(s), pol_w);
-          } else {
-            tma_load_2d(a_dst, mA0, kx, a_row0, full_bar(s), pol_w);
-            const CUtensorMap* mB = &args.tmB[shared ? 1 : 0];
-            for (int b = 0; b < nbox; ++b)
-              tma_load_2d(b_dst + b * 32 * 128, mB, kx, b_row0 + 32 * b, full_bar(s), pol_t);
-          }
-        }
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
         __syncwarp();
-        if constexpr (GATED) {
+        if (lane < NLOADS) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
+        if constexpr (BMODE == kGather4) {
 #pragma unroll
           for (int j = 0; j < NQ; ++j) {
             const int q = lane + 32 * j;
@@ -316,7 +342,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(drain_bar, 0, nullptr, 20000000ull);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int et = threadIdx.x - 64;        // 0..127
@@ -411,6 +437,67 @@ __global__ void __launch_bounds__(192, 1)
         named_barrier_sync(1, 128);
       }
       if (et == 0) mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  if constexpr (BMODE == kCpAsync) {
+    if (warp >= 6) {
+      // ------------------------------------------------------------ token-row gather
+      // Thread gt owns 16-byte chunk `ch` of rows r0, r0 + 16, ... of each stage;
+      // a warp covers 4 whole 128-byte rows per instruction.
+      constexpr int RPT = BN / 16;  // rows per thread
+      const int gt = threadIdx.x - 192;
+      const int ch = gt & 7, r0 = gt >> 3;
+      const TIn* xsrc = reinterpret_cast<const TIn*>(args.b_src);
+      const int ld = args.kdim_routed;  // x row length (H), also for the shared expert
+      uint32_t it = 0, arrived = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+        const bool shared = tl.g == E;
+        const int kdim = shared ? args.kdim_shared : args.kdim_routed;
+        const TIn* src[RPT];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+          const int r = r0 + 16 * i;
+          int tok = -1;
+          if (r < tl.n_valid)
+            tok = shared ? tl.p0 - offs[E] + r : args.gather_idx[tl.p0 + r] / args.k;
+          src[i] = tok >= 0 ? xsrc + (size_t)tok * ld + ch * (16 / sizeof(TIn)) : nullptr;
+        }
+        for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t round = it / STAGES;
+          int wok = 1;
+          if (lane == 0) wok = mbar_wait(empty_bar(s), (round & 1u) ^ 1u, args.status, limit);
+          wok = __shfl_sync(0xffffffffu, wok, 0);
+          if (!wok) {
+            ok = false;
+            break;
+          }
+          const uint32_t b_dst = smem_u32(stages + (size_t)s * C::STAGE_BYTES) + C::A_BYTES;
+#pragma unroll
+          for (int i = 0; i < RPT; ++i) {
+            const int r = r0 + 16 * i;
+            if (src[i])
+              cp_async_16(b_dst + r * 128 + ((ch ^ (r & 7)) << 4), src[i] + kb * C::BK);
+          }
+          cp_async_commit();
+          if (it >= (uint32_t)C::CP_LAG) {
+            // The stage issued CP_LAG steps ago has landed: publish it.
+            cp_async_wait<C::CP_LAG>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar((it - C::CP_LAG) % STAGES));
+            ++arrived;
+          }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (ok && lane == 0)
+        for (uint32_t i = arrived; i < it; ++i) mbar_arrive(full_bar(i % STAGES));
     }
   }
 
