@@ -153,6 +153,14 @@ def roofline_numbers(cfg, counts):
                 flop_gated=flop_g, bytes_gated=bytes_g)
 
 
+def kernels_per_step(cfg):
+    """Kernels one moe_forward launches: router logits, route, permute, [dispatch
+    copy of the routed rows for prefill-sized tiles], gated GEMM, down GEMM,
+    combine."""
+    prefill = cfg.T * cfg.k > 32 * cfg.E
+    return 6 + (1 if prefill else 0)
+
+
 def build_layer(cfg, device, seed=0):
     import mixture_experts_layer_route_gb300 as m
     d = generate(cfg, seed=seed, device=device)
@@ -468,7 +476,7 @@ def run_native(args):
         "median_ms": s["median_ms"], "p10_ms": s["p10_ms"], "p90_ms": s["p90_ms"],
         "roofline": s["roofline"], "layer_roofline": s["layer_roofline"],
         "stages_ms": s["stages_ms"], "expert_load": s["expert_load"],
-        "e2e": s["e2e"], "gpu_launches": 6 * s["steps"],
+        "e2e": s["e2e"], "gpu_launches": kernels_per_step(cfg) * s["steps"],
         "clocks": clocks,
         "cpu_baseline": cpu, "prefill": prefill,
     }

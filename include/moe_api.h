@@ -131,7 +131,10 @@ moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
  * (token t = gather_idx[p] / k):
  *   h[p][i] = silu(x[t] . W_gate[e][i]) * (x[t] . W_up[e][i])
  * and, when I_shared > 0, h_shared[t][i] likewise with Ws_gate, Ws_up.
- * Rows of x are gathered inside the GEMM's loads (no gathered copy of x).
+ * Decode-sized token tiles gather the rows of x inside the GEMM's own loads;
+ * prefill-sized tiles first copy the routed rows into expert order, unpadded,
+ * in the workspace (the dispatch copy of "CuTeDSL at Perplexity", "Local") and
+ * load them as whole tiles. Needs moe_workspace_size(pb) bytes of workspace.
  * h: [T*k][I], h_shared: [T][I_shared] (NULL iff I_shared == 0), in the dtype;
  * fp32 accumulation, one rounding to the dtype. */
 moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,

@@ -7,7 +7,9 @@
 //           Gated: tokens by TMA gather4 (8 instructions per stage).
 //   PREFILL BN = 256, 4 stages: hundreds of tokens per expert; tensor-core
 //           bound, 128 x 256 tiles, epilogue overlapped via two accumulators.
-//           Gated: tokens gathered by four cp.async warps.
+//           Gated: the token rows, already copied into expert order, load as
+//           one TMA box per stage (or, without that copy, through four
+//           cp.async gather warps).
 // The down projection always loads its h rows as one TMA box of BN rows.
 #include <mutex>
 
@@ -110,25 +112,32 @@ size_t tile_upper_bound(int T, int k, int E, int BN, int routed_blocks, int shar
 
 bool tensor_map_encoder_available() { return encoder() != nullptr; }
 
-cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const int32_t* offsets,
-                               const int32_t* gather_idx, const void* Wg, const void* Wu,
-                               const void* Wsg, const void* Wsu, void* h, void* hs, int* status,
-                               cudaStream_t st) {
+cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* xg,
+                               const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
+                               const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,
+                               int* status, cudaStream_t st) {
   GroupedGemmArgs a;
   memset(&a, 0, sizeof(a));
   const bool has_s = p.Is > 0;
+  const bool tiled = p.tile == MOE_TILE_PREFILL && xg != nullptr;
   bool ok = make_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
-            make_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
-            make_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
+            make_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64);
   if (ok && has_s)
     ok = make_map(&a.tmA[2], Wsg, p.dtype, p.Is, p.H, 64) &&
          make_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64);
+  if (ok) {
+    if (tiled)  // [0]: routed rows in expert order; [1]: x itself for the shared expert
+      ok = make_map(&a.tmB[0], xg, p.dtype, (uint64_t)p.T * p.k, p.H, 256) &&
+           make_map(&a.tmB[1], x, p.dtype, p.T, p.H, 256);
+    else
+      ok = make_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
+  }
   if (!ok) return cudaErrorInvalidValue;
   if (!has_s) {
     a.tmA[2] = a.tmA[0];
     a.tmA[3] = a.tmA[1];
   }
-  a.tmB[1] = a.tmB[0];
+  if (!tiled) a.tmB[1] = a.tmB[0];
   a.b_src = x;
   a.offsets = offsets;
   a.gather_idx = gather_idx;
@@ -156,6 +165,10 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const int32_
                : launch_variant<float, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st);
   }
   const size_t ub = tile_upper_bound(p.T, p.k, p.E, 256, rb, sb);
+  if (tiled)
+    return p.dtype == MOE_DTYPE_BF16
+               ? launch_variant<__nv_bfloat16, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st)
+               : launch_variant<float, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
   return p.dtype == MOE_DTYPE_BF16
              ? launch_variant<__nv_bfloat16, true, 256, 4, kCpAsync>(a, p.num_sms, p.E, ub, st)
              : launch_variant<float, true, 256, 4, kCpAsync>(a, p.num_sms, p.E, ub, st);

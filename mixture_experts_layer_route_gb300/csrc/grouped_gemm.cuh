@@ -36,7 +36,9 @@
 //    fence.proxy.async before arriving on the stage barrier. An SM accepts only
 //    one TMA instruction every ~70-150 cycles, so 4-row gathers cannot fill a
 //    256-token stage in time; the load/store unit can.
-//  kTiled (down projection): the tile's h rows are contiguous, one TMA box.
+//  kTiled (down projection, and prefill-sized gated tiles once the routed
+//    token rows were copied into expert order): the tile's rows are
+//    contiguous, one TMA box of BN rows.
 // All TMA loads of a stage are issued in one SIMT step with per-lane operands.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread) and
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
     grouped_gemm_kernel(const __grid_constant__ GroupedGemmArgs args) {
   using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE>;
   static_assert(GATED || BMODE == kTiled, "the down projection reads contiguous h rows");
+  static_assert(BMODE != kGather4 || BN <= 128, "gather4 is for decode-sized token tiles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -244,7 +247,8 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
       }
       const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
       // Per-lane operands of this tile's TMA loads (one SIMT step per stage):
-      // GATED: lanes 0, 1 = gate, up rows; DOWN: lane 0 = W_down rows, lane 1 = h rows.
+      // GATED: lanes 0, 1 = gate, up rows (+ lane 2 = token rows when tiled);
+      // DOWN: lane 0 = W_down rows, lane 1 = h rows.
       constexpr int NA = GATED ? 2 : 1;
       constexpr int NLOADS = NA + (BMODE == kTiled ? 1 : 0);
       const CUtensorMap* my_map = mA0;

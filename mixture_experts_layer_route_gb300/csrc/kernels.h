@@ -25,6 +25,10 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int has_shar
                            int32_t* offsets, int32_t* gather_idx, int32_t* slot_pos, int* status,
                            cudaStream_t st);
 
+// Dispatch copy of the routed token rows into expert order (permute.cu).
+cudaError_t launch_gather_rows(const void* x, const int32_t* gather_idx, int P, int k,
+                               size_t row_bytes, void* xg, int num_sms, cudaStream_t st);
+
 // Grouped GEMMs (grouped_gemm.cu).
 struct GemmProblem {
   int dtype;  // MOE_DTYPE_*
@@ -34,10 +38,13 @@ struct GemmProblem {
   unsigned long long limit_ns;
   int num_sms;
 };
-cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const int32_t* offsets,
-                               const int32_t* gather_idx, const void* Wg, const void* Wu,
-                               const void* Wsg, const void* Wsu, void* h, void* hs, int* status,
-                               cudaStream_t st);
+// xg: the routed token rows in expert order ([T*k][H], from launch_gather_rows);
+// required for MOE_TILE_PREFILL, ignored for MOE_TILE_DECODE (rows gathered in
+// the GEMM's own loads).
+cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* xg,
+                               const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
+                               const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,
+                               int* status, cudaStream_t st);
 cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
                              const int32_t* offsets, const int32_t* gather_idx,
                              const float* topk_w, const void* Wd, const void* Wsd, float* Y,

@@ -16,7 +16,7 @@ constexpr size_t kHeader = 256;  // status word + reserved
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t logits, partials, ids, w, offsets, gather, slotpos, h, hs, Y, total;
+  size_t logits, partials, ids, w, offsets, gather, slotpos, xg, h, hs, Y, total;
   int S;  // router split count
 };
 
@@ -40,6 +40,11 @@ int sm_count() {
 // workspace size independent of the device queried.
 constexpr int kRouterSplitSms = 152;
 
+int resolve_tile(const moe_problem& p) {
+  if (p.tile != MOE_TILE_AUTO) return p.tile;
+  return (p.T * p.k <= 32 * p.E) ? MOE_TILE_DECODE : MOE_TILE_PREFILL;
+}
+
 size_t elem_bytes(int dtype) { return dtype == MOE_DTYPE_BF16 ? 2 : 4; }
 
 Layout layout_of(const moe_problem& p) {
@@ -61,6 +66,8 @@ Layout layout_of(const moe_problem& p) {
   L.offsets = take((E + 2) * 4);
   L.gather = take(T * k * 4);
   L.slotpos = take(T * k * 4);
+  // Prefill-sized tiles read the routed token rows from an expert-ordered copy.
+  L.xg = resolve_tile(p) == MOE_TILE_PREFILL ? take(T * k * (size_t)p.H * es) : 0;
   L.h = take(T * k * (size_t)p.I * es);
   L.hs = p.I_shared > 0 ? take(T * (size_t)p.I_shared * es) : 0;
   L.Y = take(T * KP * (size_t)p.H * 4);
@@ -86,11 +93,6 @@ moe_status check_problem(const moe_problem* pb) {
       p.E * p.H >= lim)
     return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
-}
-
-int resolve_tile(const moe_problem& p) {
-  if (p.tile != MOE_TILE_AUTO) return p.tile;
-  return (p.T * p.k <= 32 * p.E) ? MOE_TILE_DECODE : MOE_TILE_PREFILL;
 }
 
 GemmProblem gemm_problem(const moe_problem& p) {
@@ -239,11 +241,22 @@ moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
   if (has_s && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(h_shared)))
     return MOE_ERR_INVALID_ARG;
-  if ((s = check_ws(workspace, workspace_bytes, kHeader)) != MOE_OK) return s;
+  const Layout L = layout_of(*pb);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return s;
   if (!tensor_map_encoder_available()) return MOE_ERR_UNSUPPORTED;
-  return cuda_status(launch_swiglu_gemm(gemm_problem(*pb), x, expert_offsets, gather_idx, W_gate,
-                                        W_up, Ws_gate, Ws_up, h, h_shared,
-                                        status_ptr(workspace), (cudaStream_t)stream));
+  const GemmProblem g = gemm_problem(*pb);
+  cudaStream_t st = (cudaStream_t)stream;
+  void* xg = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (g.tile == MOE_TILE_PREFILL) {
+    xg = at<void>(workspace, L.xg);
+    e = launch_gather_rows(x, gather_idx, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
+                           g.num_sms, st);
+  }
+  if (e == cudaSuccess)
+    e = launch_swiglu_gemm(g, x, xg, expert_offsets, gather_idx, W_gate, W_up, Ws_gate, Ws_up, h,
+                           h_shared, status_ptr(workspace), st);
+  return cuda_status(e);
 }
 
 moe_status moe_down_combine(const moe_problem* pb, const void* h, const void* h_shared,
@@ -319,8 +332,15 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
                      L.S > 1 ? logits : nullptr, ids, w, st);
   if (e == cudaSuccess)
     e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status, st);
+  void* xg = nullptr;
+  if (e == cudaSuccess && g.tile == MOE_TILE_PREFILL) {
+    xg = at<void>(workspace, L.xg);
+    e = launch_gather_rows(x, gidx, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
+                           g.num_sms, st);
+  }
   if (e == cudaSuccess)
-    e = launch_swiglu_gemm(g, x, offs, gidx, W_gate, W_up, Ws_gate, Ws_up, h, hs, status, st);
+    e = launch_swiglu_gemm(g, x, xg, offs, gidx, W_gate, W_up, Ws_gate, Ws_up, h, hs, status,
+                           st);
   if (e == cudaSuccess)
     e = launch_down_gemm(g, h, hs, offs, gidx, w, W_down, Ws_down, Y, status, st);
   if (e == cudaSuccess)

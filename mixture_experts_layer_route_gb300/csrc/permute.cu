@@ -134,7 +134,46 @@ __global__ void __launch_bounds__(PM_THREADS, 1)
   }
 }
 
+// Dispatch copy ("CuTeDSL at Perplexity", "Local": tokens are copied into
+// buffers, optionally padded, for the MoE GEMM; here unpadded): row p of xg
+// is x[gather_idx[p] / k], so every expert's rows are contiguous and the
+// grouped GEMM reads them as one TMA box per stage. One warp per row, 16-byte
+// vectors; grid sized to a multiple of the SM count.
+template <int VB>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ gather_idx,
+                                                          int P, int k, int vecs_per_row,
+                                                          uint4* __restrict__ xg) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < P; p += warps) {
+    const int t = gather_idx[p] / k;
+    const uint4* src = x + (size_t)t * vecs_per_row;
+    uint4* dst = xg + (size_t)p * vecs_per_row;
+    for (int v = lane; v < vecs_per_row; v += 32 * VB) {
+      uint4 r[VB];
+#pragma unroll
+      for (int j = 0; j < VB; ++j)
+        if (v + 32 * j < vecs_per_row) r[j] = __ldg(src + v + 32 * j);
+#pragma unroll
+      for (int j = 0; j < VB; ++j)
+        if (v + 32 * j < vecs_per_row) dst[v + 32 * j] = r[j];
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* gather_idx, int P, int k,
+                               size_t row_bytes, void* xg, int num_sms, cudaStream_t st) {
+  if (P == 0) return cudaSuccess;
+  const int vpr = (int)(row_bytes / 16);
+  int blocks = (P + 7) / 8;
+  if (blocks > 8 * num_sms) blocks = 8 * num_sms;
+  gather_rows_kernel<4><<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), gather_idx, P,
+                                                k, vpr, reinterpret_cast<uint4*>(xg));
+  return cudaGetLastError();
+}
 
 size_t permute_smem_bytes(int E) { return sizeof(int32_t) * ((size_t)PM_WARPS * E + E + PM_WARPS); }
 
