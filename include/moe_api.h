@@ -120,7 +120,9 @@ moe_status moe_route(const float* logits, int64_t T, int64_t E, int64_t k, int r
  *     within each expert);
  *   slot_pos int32 [T*k]: slot_pos[s] = position of slot s.
  * No padded buffer is produced. Needs moe_workspace_size() of a problem with
- * these T, E, k. Out-of-range ids set MOE_ERR_DEVICE_CHECK in the status. */
+ * these T, E, k (beyond 4096 slots the work is split over CTAs that exchange
+ * per-chunk counts through the workspace). Out-of-range ids set
+ * MOE_ERR_DEVICE_CHECK in the status. */
 moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
                        int has_shared, int32_t* expert_offsets, int32_t* gather_idx,
                        int32_t* slot_pos, void* workspace, size_t workspace_bytes,

@@ -21,9 +21,12 @@ cudaError_t launch_route(const float* src, int S, const float* bias, int T, int 
 
 // Permutation (permute.cu).
 size_t permute_smem_bytes(int E);
+// Workspace bytes of per-chunk counts the grid-wide variant needs (0 when one
+// CTA does the whole permutation).
+size_t permute_scratch_bytes(int64_t T, int64_t E, int64_t k);
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int has_shared,
                            int32_t* offsets, int32_t* gather_idx, int32_t* slot_pos, int* status,
-                           cudaStream_t st);
+                           int32_t* chunk_hist, cudaStream_t st);
 
 // Dispatch copy of the routed token rows into expert order (permute.cu).
 cudaError_t launch_gather_rows(const void* x, const int32_t* gather_idx, int P, int k,

@@ -16,7 +16,7 @@ constexpr size_t kHeader = 256;  // status word + reserved
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t logits, partials, ids, w, offsets, gather, slotpos, xg, h, hs, Y, total;
+  size_t pscratch, logits, partials, ids, w, offsets, gather, slotpos, xg, h, hs, Y, total;
   int S;  // router split count
 };
 
@@ -59,6 +59,9 @@ Layout layout_of(const moe_problem& p) {
     off = align_up(off + bytes);
     return o;
   };
+  // First after the header: moe_permute (which has no problem struct) finds
+  // its per-chunk counts here from T, E and k alone.
+  L.pscratch = take(permute_scratch_bytes(p.T, p.E, p.k));
   L.logits = take(T * E * 4);
   L.partials = L.S > 1 ? take((size_t)L.S * T * E * 4) : L.logits;
   L.ids = take(T * k * 4);
@@ -216,11 +219,13 @@ moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
   if (!aligned16(expert_offsets) || (T > 0 && (!aligned16(topk_ids) || !aligned16(gather_idx) ||
                                                !aligned16(slot_pos))))
     return MOE_ERR_INVALID_ARG;
-  moe_status s = check_ws(workspace, workspace_bytes, kHeader);
+  moe_status s = check_ws(workspace, workspace_bytes,
+                          align_up(kHeader + permute_scratch_bytes(T, E, k)));
   if (s != MOE_OK) return s;
   return cuda_status(launch_permute(topk_ids, (int)T, (int)E, (int)k, has_shared ? 1 : 0,
                                     expert_offsets, gather_idx, slot_pos,
-                                    status_ptr(workspace), (cudaStream_t)stream));
+                                    status_ptr(workspace), at<int32_t>(workspace, kHeader),
+                                    (cudaStream_t)stream));
 }
 
 moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
@@ -331,7 +336,8 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
     e = launch_route(part, L.S, router_bias, g.T, g.E, g.k, pb->renorm,
                      L.S > 1 ? logits : nullptr, ids, w, st);
   if (e == cudaSuccess)
-    e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status, st);
+    e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status,
+                       at<int32_t>(workspace, L.pscratch), st);
   void* xg = nullptr;
   if (e == cudaSuccess && g.tile == MOE_TILE_PREFILL) {
     xg = at<void>(workspace, L.xg);

@@ -47,7 +47,25 @@ __device__ __forceinline__ void load_vec_f32<float>(const float* p, float* out) 
   out[3] = v.w;
 }
 
+// Two fp32 lanes in one 64-bit register; fma.rn.f32x2 performs two IEEE fp32
+// FMAs (the same rounding as fmaf) with one instruction.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void fma2(unsigned long long& d, unsigned long long a,
+                                     unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 // grid (ceil(E/64), ceil(T/64), S); block 256. out: [S][T][E].
+// Each thread owns 4 tokens x 4 experts; both operands are staged in shared
+// memory as fp32, K-major, double-buffered so that the next K slice is read
+// from global memory while the current one is multiplied.
 template <typename TIn>
 __global__ void __launch_bounds__(256) router_logits_kernel(const TIn* __restrict__ x,
                                                             const TIn* __restrict__ Wr,
@@ -56,8 +74,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TIn* __restric
                                                             float* __restrict__ out) {
   constexpr int VEC = 16 / sizeof(TIn);                 // elements per 16-byte load
   constexpr int LOADS = RT_BM * RT_BK / VEC / 256;       // per thread per operand
-  __shared__ __align__(16) float As[RT_BK][RT_BM + RT_PAD];
-  __shared__ __align__(16) float Bs[RT_BK][RT_BN + RT_PAD];
+  __shared__ __align__(16) float As[2][RT_BK][RT_BM + RT_PAD];
+  __shared__ __align__(16) float Bs[2][RT_BK][RT_BN + RT_PAD];
 
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
@@ -66,51 +84,71 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TIn* __restric
   const int kbeg = ks * k_len;
   const int kend = min(H, kbeg + k_len);
 
-  float acc[4][4];
+  unsigned long long acc[4][2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0ull;
 
-  for (int kb = kbeg; kb < kend; kb += RT_BK) {
+  float ra[LOADS][VEC], rb[LOADS][VEC];
+  auto fetch = [&](int kb) {
 #pragma unroll
     for (int l = 0; l < LOADS; ++l) {
       const int idx = tid + l * 256;
-      const int row = idx % RT_BM;            // consecutive lanes -> consecutive rows
+      const int row = idx % RT_BM;  // consecutive lanes -> consecutive rows
       const int kc = (idx / RT_BM) * VEC;
-      float va[VEC], vb[VEC];
       const int t = t0 + row, e = e0 + row;
       if (t < T) {
-        load_vec_f32<TIn>(x + (size_t)t * H + kb + kc, va);
+        load_vec_f32<TIn>(x + (size_t)t * H + kb + kc, ra[l]);
       } else {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) va[i] = 0.f;
+        for (int i = 0; i < VEC; ++i) ra[l][i] = 0.f;
       }
       if (e < E) {
-        load_vec_f32<TIn>(Wr + (size_t)e * H + kb + kc, vb);
+        load_vec_f32<TIn>(Wr + (size_t)e * H + kb + kc, rb[l]);
       } else {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) vb[i] = 0.f;
+        for (int i = 0; i < VEC; ++i) rb[l][i] = 0.f;
       }
+    }
+  };
+  auto stash = [&](int buf) {
+#pragma unroll
+    for (int l = 0; l < LOADS; ++l) {
+      const int idx = tid + l * 256;
+      const int row = idx % RT_BM;
+      const int kc = (idx / RT_BM) * VEC;
 #pragma unroll
       for (int i = 0; i < VEC; ++i) {
-        As[kc + i][row] = va[i];
-        Bs[kc + i][row] = vb[i];
+        As[buf][kc + i][row] = ra[l][i];
+        Bs[buf][kc + i][row] = rb[l][i];
       }
     }
-    __syncthreads();
+  };
+
+  int buf = 0;
+  if (kbeg < kend) {
+    fetch(kbeg);
+    stash(0);
+  }
+  __syncthreads();
+  for (int kb = kbeg; kb < kend; kb += RT_BK) {
+    const bool more = kb + RT_BK < kend;
+    if (more) fetch(kb + RT_BK);
 #pragma unroll
     for (int kk = 0; kk < RT_BK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float4 a = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+      const unsigned long long b01 = pack2(b.x, b.y), b23 = pack2(b.z, b.w);
       const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      for (int i = 0; i < 4; ++i) {
+        const unsigned long long ai = pack2(av[i], av[i]);
+        fma2(acc[i][0], ai, b01);
+        fma2(acc[i][1], ai, b23);
+      }
     }
+    if (more) stash(buf ^ 1);
     __syncthreads();
+    buf ^= 1;
   }
 
   const bool add_bias = (bias != nullptr) && (gridDim.z == 1);
@@ -118,13 +156,16 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TIn* __restric
   for (int i = 0; i < 4; ++i) {
     const int t = t0 + ty * 4 + i;
     if (t >= T) continue;
+    float v[4];
+    unpack2(acc[i][0], v[0], v[1]);
+    unpack2(acc[i][1], v[2], v[3]);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + tx * 4 + j;
       if (e >= E) continue;
-      float v = acc[i][j];
-      if (add_bias) v += bias[e];
-      out[((size_t)ks * T + t) * E + e] = v;
+      float o = v[j];
+      if (add_bias) o += bias[e];
+      out[((size_t)ks * T + t) * E + e] = o;
     }
   }
 }
@@ -234,7 +275,8 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ sr
 int router_split_count(int64_t T, int64_t H, int64_t E, int num_sms) {
   const int64_t tiles = ((E + RT_BN - 1) / RT_BN) * ((T + RT_BM - 1) / RT_BM);
   if (tiles <= 0) return 1;
-  int64_t S = (2 * (int64_t)num_sms + tiles - 1) / tiles;
+  // About four CTAs per SM in total, so the last wave is a small fraction.
+  int64_t S = (4 * (int64_t)num_sms + tiles - 1) / tiles;
   const int64_t smax = H / 128;  // at least 128 of H per slice
   if (S > smax) S = smax;
   if (S < 1) S = 1;

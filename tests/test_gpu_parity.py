@@ -126,7 +126,7 @@ def _ids_with_counts(counts, seed):
 
 
 @pytest.mark.parametrize("case", ["random", "zipf", "one_expert", "t1", "big", "shared",
-                                  "e1024"])
+                                  "e1024", "chunks_shared", "chunk_edge"])
 def test_permute_bitexact(oracle, case):
     if case == "random":
         ids, _ = generate_routing(301, 16, 4, seed=1)
@@ -146,16 +146,22 @@ def test_permute_bitexact(oracle, case):
     elif case == "shared":
         ids, _ = generate_routing(97, 24, 3, seed=5)
         E, shared = 24, 1
-    else:
+    elif case == "e1024":
         ids, _ = generate_routing(700, 1024, 12, seed=6)
         E, shared = 1024, 0
+    elif case == "chunks_shared":  # several chunks of the grid-wide variant, skewed
+        ids, _ = generate_routing(3001, 64, 6, seed=7, zipf_s=1.1)
+        E, shared = 64, 1
+    else:  # exactly two chunks (4096 slots is the single-CTA limit)
+        ids, _ = generate_routing(1025, 40, 4, seed=8)
+        E, shared = 40, 0
     ids = np.ascontiguousarray(np.asarray(ids, np.int32))
     T, k = ids.shape
     dids = torch.from_numpy(ids).to(DEV)
     offs = torch.empty(E + 2, dtype=torch.int32, device=DEV)
     gidx = torch.empty(T * k, dtype=torch.int32, device=DEV)
     spos = torch.empty(T * k, dtype=torch.int32, device=DEV)
-    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    ws = ws_for(m.make_problem(T, 128, E, k, 64))
     m.permute(dids, E, shared, offs, gidx, spos, ws)
     finish(ws)
     ro, rg, rs = oracle.permute(ids, E, shared)
@@ -165,16 +171,19 @@ def test_permute_bitexact(oracle, case):
 
 
 def test_permute_out_of_range_id_sets_device_check():
-    ids = torch.tensor([[0, 1], [2, 9]], dtype=torch.int32, device=DEV)
-    offs = torch.empty(6, dtype=torch.int32, device=DEV)
-    gidx = torch.empty(4, dtype=torch.int32, device=DEV)
-    spos = torch.empty(4, dtype=torch.int32, device=DEV)
-    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
-    m.permute(ids, 4, 0, offs, gidx, spos, ws)
-    torch.cuda.synchronize()
-    assert m.get_device_status(ws) == 6  # MOE_ERR_DEVICE_CHECK
-    m.reset_device_status(ws)
-    assert m.get_device_status(ws) == m.MOE_OK
+    for T in (2, 3000):  # single-CTA and grid-wide variants
+        ids = torch.zeros(T, 2, dtype=torch.int32, device=DEV)
+        ids[:, 1] = 1
+        ids[T - 1, 1] = 9
+        offs = torch.empty(6, dtype=torch.int32, device=DEV)
+        gidx = torch.empty(2 * T, dtype=torch.int32, device=DEV)
+        spos = torch.empty(2 * T, dtype=torch.int32, device=DEV)
+        ws = ws_for(m.make_problem(T, 128, 4, 2, 64))
+        m.permute(ids, 4, 0, offs, gidx, spos, ws)
+        torch.cuda.synchronize()
+        assert m.get_device_status(ws) == 6  # MOE_ERR_DEVICE_CHECK
+        m.reset_device_status(ws)
+        assert m.get_device_status(ws) == m.MOE_OK
 
 
 # ------------------------------------------------------------------ a4 / a5 GEMMs
