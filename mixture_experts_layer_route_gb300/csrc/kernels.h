@@ -9,7 +9,6 @@ namespace moe {
 
 // Router (router.cu).
 int router_split_count(int64_t T, int64_t H, int64_t E, int num_sms);
-int router_split_len_ok(int H, int S);
 cudaError_t launch_router_logits(int dtype, const void* x, const void* Wr, const float* bias,
                                  int T, int H, int E, int S, float* out_partials,
                                  cudaStream_t st);

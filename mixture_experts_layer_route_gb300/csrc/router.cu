@@ -11,6 +11,8 @@
 // k largest one at a time (lowest expert index among equal values), then the
 // softmax gate weights over the chosen k (renorm) or over all E ("MoE Router"
 // section of the same page: top-k indices and scores per token).
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -170,6 +172,131 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TIn* __restric
   }
 }
 
+// Large-batch variant: 128 tokens x 128 experts per CTA, 8 x 8 outputs per
+// thread. Token values are stored twice in shared memory (x_t, x_t) so that a
+// 16-byte load yields two ready fma.rn.f32x2 operands; expert weights are
+// stored once and form (w_e, w_e+1) pairs. Per K step a thread issues six
+// 16-byte shared loads for 64 FMAs (32 f32x2 instructions).
+constexpr int RL_BM = 128, RL_BN = 128, RL_BK = 32;
+constexpr int RL_APITCH = 2 * RL_BM + 8;   // floats per duplicated-token row
+constexpr int RL_BPITCH = RL_BN + 4;       // floats per expert row
+constexpr size_t RL_SMEM = sizeof(float) * 2 * RL_BK * (RL_APITCH + RL_BPITCH);
+
+template <typename TIn>
+__global__ void __launch_bounds__(256, 1) router_logits_big_kernel(
+    const TIn* __restrict__ x, const TIn* __restrict__ Wr, const float* __restrict__ bias, int T,
+    int H, int E, int k_len, float* __restrict__ out) {
+  constexpr int VEC = 16 / sizeof(TIn);
+  constexpr int LOADS = RL_BM * RL_BK / VEC / 256;  // per thread per operand
+  extern __shared__ __align__(16) float rl_sm[];
+  float* As = rl_sm;                               // [2][BK][APITCH]
+  float* Bs = rl_sm + 2 * RL_BK * RL_APITCH;       // [2][BK][BPITCH]
+
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int e0 = blockIdx.x * RL_BN, t0 = blockIdx.y * RL_BM;
+  const int ks = blockIdx.z;
+  const int kbeg = ks * k_len;
+  const int kend = min(H, kbeg + k_len);
+
+  unsigned long long acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
+
+  float ra[LOADS][VEC], rb[LOADS][VEC];
+  auto fetch = [&](int kb) {
+#pragma unroll
+    for (int l = 0; l < LOADS; ++l) {
+      const int idx = tid + l * 256;
+      const int row = idx % RL_BM;
+      const int kc = (idx / RL_BM) * VEC;
+      const int t = t0 + row, e = e0 + row;
+      if (t < T) {
+        load_vec_f32<TIn>(x + (size_t)t * H + kb + kc, ra[l]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) ra[l][i] = 0.f;
+      }
+      if (e < E) {
+        load_vec_f32<TIn>(Wr + (size_t)e * H + kb + kc, rb[l]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) rb[l][i] = 0.f;
+      }
+    }
+  };
+  auto stash = [&](int buf) {
+    float* A = As + buf * RL_BK * RL_APITCH;
+    float* B = Bs + buf * RL_BK * RL_BPITCH;
+#pragma unroll
+    for (int l = 0; l < LOADS; ++l) {
+      const int idx = tid + l * 256;
+      const int row = idx % RL_BM;
+      const int kc = (idx / RL_BM) * VEC;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        *reinterpret_cast<float2*>(&A[(kc + i) * RL_APITCH + 2 * row]) =
+            make_float2(ra[l][i], ra[l][i]);
+        B[(kc + i) * RL_BPITCH + row] = rb[l][i];
+      }
+    }
+  };
+
+  int buf = 0;
+  if (kbeg < kend) {
+    fetch(kbeg);
+    stash(0);
+  }
+  __syncthreads();
+  for (int kb = kbeg; kb < kend; kb += RL_BK) {
+    const bool more = kb + RL_BK < kend;
+    if (more) fetch(kb + RL_BK);
+    const float* A = As + buf * RL_BK * RL_APITCH;
+    const float* B = Bs + buf * RL_BK * RL_BPITCH;
+#pragma unroll 4
+    for (int kk = 0; kk < RL_BK; ++kk) {
+      // tokens ty*8 .. ty*8+7 (duplicated pairs); experts tx*4..+3 and 64+tx*4..+3
+      const ulonglong2* ap = reinterpret_cast<const ulonglong2*>(&A[kk * RL_APITCH + ty * 16]);
+      const ulonglong2 a01 = ap[0], a23 = ap[1], a45 = ap[2], a67 = ap[3];
+      const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(&B[kk * RL_BPITCH + tx * 4]);
+      const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(&B[kk * RL_BPITCH + 64 + tx * 4]);
+      const unsigned long long av[8] = {a01.x, a01.y, a23.x, a23.y, a45.x, a45.y, a67.x, a67.y};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        fma2(acc[i][0], av[i], b0.x);
+        fma2(acc[i][1], av[i], b0.y);
+        fma2(acc[i][2], av[i], b1.x);
+        fma2(acc[i][3], av[i], b1.y);
+      }
+    }
+    if (more) stash(buf ^ 1);
+    __syncthreads();
+    buf ^= 1;
+  }
+
+  const bool add_bias = (bias != nullptr) && (gridDim.z == 1);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 8 + i;
+    if (t >= T) continue;
+    float v[8];
+    unpack2(acc[i][0], v[0], v[1]);
+    unpack2(acc[i][1], v[2], v[3]);
+    unpack2(acc[i][2], v[4], v[5]);
+    unpack2(acc[i][3], v[6], v[7]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = e0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+      if (e >= E) continue;
+      float o = v[j];
+      if (add_bias) o += bias[e];
+      out[((size_t)ks * T + t) * E + e] = o;
+    }
+  }
+}
+
 // Sum of S partial logits in ascending slice order, then the bias: identical
 // arithmetic in the reduction kernel and in the route kernel.
 __device__ __forceinline__ float reduce_partials(const float* __restrict__ part, int S, int T,
@@ -272,25 +399,80 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ sr
 
 }  // namespace
 
+// Batches of at least this many tokens use the 128 x 128 tile kernel.
+constexpr int64_t kRouterBigT = 1024;
+
+int64_t router_split_request(int64_t T, int64_t H, int64_t E, int num_sms);
+
+// Slice length for S slices of H: a multiple of the K step (32).
+int64_t router_slice_len(int64_t H, int64_t S) {
+  const int64_t k_len = (H + S - 1) / S;
+  return (k_len + RT_BK - 1) / RT_BK * RT_BK;
+}
+
+// Slices actually produced by S requested slices (rounding the slice length
+// up can leave fewer).
+int64_t router_effective_slices(int64_t H, int64_t S) {
+  const int64_t k_len = router_slice_len(H, S);
+  return (H + k_len - 1) / k_len;
+}
+
 int router_split_count(int64_t T, int64_t H, int64_t E, int num_sms) {
-  const int64_t tiles = ((E + RT_BN - 1) / RT_BN) * ((T + RT_BM - 1) / RT_BM);
+  return (int)router_effective_slices(H, router_split_request(T, H, E, num_sms));
+}
+
+int64_t router_split_request(int64_t T, int64_t H, int64_t E, int num_sms) {
+  const bool big = T >= kRouterBigT;
+  const int64_t bm = big ? RL_BM : RT_BM, bn = big ? RL_BN : RT_BN;
+  const int64_t resident = (big ? 1 : 4) * (int64_t)num_sms;  // CTAs per wave
+  const int64_t tiles = ((E + bn - 1) / bn) * ((T + bm - 1) / bm);
   if (tiles <= 0) return 1;
-  // About four CTAs per SM in total, so the last wave is a small fraction.
-  int64_t S = (4 * (int64_t)num_sms + tiles - 1) / tiles;
-  const int64_t smax = H / 128;  // at least 128 of H per slice
-  if (S > smax) S = smax;
-  if (S < 1) S = 1;
-  return (int)S;
+  const int64_t smax = H / 128 < 1 ? 1 : H / 128;  // at least 128 of H per slice
+  if (!big) {
+    int64_t S = (resident + tiles - 1) / tiles;
+    return (int)(S > smax ? smax : (S < 1 ? 1 : S));
+  }
+  // Smallest split whose last wave is at least 90% full (at most 8 slices),
+  // else the best-filled one.
+  int64_t best = 1;
+  double best_eff = 0.0;
+  for (int64_t S = 1; S <= 8 && S <= smax; ++S) {
+    const double waves = (double)(tiles * S) / (double)resident;
+    const double eff = waves / std::ceil(waves);
+    if (eff >= 0.9) return (int)S;
+    if (eff > best_eff) {
+      best_eff = eff;
+      best = S;
+    }
+  }
+  return (int)best;
 }
 
 cudaError_t launch_router_logits(int dtype, const void* x, const void* Wr, const float* bias,
                                  int T, int H, int E, int S, float* out_partials,
                                  cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  int k_len = (H + S - 1) / S;
-  k_len = (k_len + RT_BK - 1) / RT_BK * RT_BK;
-  const int S_eff = (H + k_len - 1) / k_len;
-  if (S_eff != S) return cudaErrorInvalidValue;
+  const int k_len = (int)router_slice_len(H, S);
+  if (router_effective_slices(H, S) != S) return cudaErrorInvalidValue;
+  if (T >= kRouterBigT) {
+    dim3 grid((E + RL_BN - 1) / RL_BN, (T + RL_BM - 1) / RL_BM, S);
+    cudaError_t e;
+    if (dtype == MOE_DTYPE_BF16) {
+      e = cudaFuncSetAttribute(router_logits_big_kernel<__nv_bfloat16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RL_SMEM);
+      if (e != cudaSuccess) return e;
+      router_logits_big_kernel<__nv_bfloat16><<<grid, 256, RL_SMEM, st>>>(
+          (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wr, bias, T, H, E, k_len,
+          out_partials);
+    } else {
+      e = cudaFuncSetAttribute(router_logits_big_kernel<float>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RL_SMEM);
+      if (e != cudaSuccess) return e;
+      router_logits_big_kernel<float><<<grid, 256, RL_SMEM, st>>>(
+          (const float*)x, (const float*)Wr, bias, T, H, E, k_len, out_partials);
+    }
+    return cudaGetLastError();
+  }
   dim3 grid((E + RT_BN - 1) / RT_BN, (T + RT_BM - 1) / RT_BM, S);
   if (dtype == MOE_DTYPE_BF16) {
     router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
@@ -301,12 +483,6 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* Wr, const
                                out_partials);
   }
   return cudaGetLastError();
-}
-
-int router_split_len_ok(int H, int S) {
-  int k_len = (H + S - 1) / S;
-  k_len = (k_len + RT_BK - 1) / RT_BK * RT_BK;
-  return ((H + k_len - 1) / k_len) == S;
 }
 
 cudaError_t launch_logits_reduce(const float* partials, int S, int T, int E, const float* bias,

@@ -76,6 +76,9 @@ PROFILE_CONFIGS = {
                                         I=1536),
     "qwen3_235b_decode_e32": MoEConfig("qwen3_235b_decode_e32", T=16, H=4096, E=32, k=8,
                                        I=1536),
+    # the prefill chunk's router shape (T=8192, H=4096, E=128) with tiny experts
+    "qwen3_235b_prefill_router": MoEConfig("qwen3_235b_prefill_router", T=8192, H=4096, E=128,
+                                           k=8, I=64),
 }
 
 

@@ -79,6 +79,10 @@ def finish(ws):
 @pytest.mark.parametrize("T,H,E,dtype,bias", [
     (64, 256, 8, "f32", False), (64, 4096, 128, "bf16", False), (333, 512, 40, "bf16", True),
     (1024, 4096, 512, "bf16", True), (5, 7168, 256, "bf16", False), (200, 1024, 64, "f32", True),
+    # 21 tiles of the small kernel: the split count must survive slice rounding
+    (448, 4096, 192, "bf16", False),
+    # the 128 x 128 kernel with token and expert tails, both dtypes
+    (1500, 1024, 200, "bf16", True), (1100, 512, 72, "f32", False), (8192, 4096, 128, "bf16", False),
 ])
 def test_router_logits(oracle, T, H, E, dtype, bias):
     cfg = MoEConfig("l", T=T, H=H, E=E, k=1, I=64, dtype=dtype, zipf_s=1.1 if bias else 0.0)
