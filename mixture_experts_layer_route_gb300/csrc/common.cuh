@@ -101,6 +101,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// 2-D tiled load multicast to the CTAs of `mask` in this cluster: the box lands
+// at the same shared-memory offset in each, and each CTA's mbarrier at `bar`'s
+// offset receives the transaction bytes written into that CTA.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* m,
+                                                      int32_t x, int32_t y, uint32_t bar,
+                                                      uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of all CTAs of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Row gather: four rows (r0..r3) of one 1-row-high box at inner index x,
 // placed at consecutive box-sized slots from `dst`.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, int32_t x,
@@ -196,6 +221,16 @@ __device__ __forceinline__ void umma_issue(uint32_t d_tmem, uint64_t adesc, uint
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   }
+}
+
+// As umma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
+// `mask` in this cluster.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.

@@ -83,20 +83,47 @@ cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
   return e;
 }
 
-template <typename TIn, bool GATED, int BN, int STAGES, int BMODE>
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1>
 cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t upper_tiles,
                            cudaStream_t st) {
-  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE>;
+  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>;
   const size_t smem = C::smem_bytes(E);
-  auto fn = grouped_gemm_kernel<TIn, GATED, BN, STAGES, BMODE>;
+  auto fn = grouped_gemm_kernel<TIn, GATED, BN, STAGES, BMODE, CL>;
   // Opt in once to what the largest supported expert count needs, so that a
   // later call with more experts than the first still fits.
   cudaError_t e = ensure_smem_attr((const void*)fn, C::smem_bytes(kMaxExperts));
   if (e != cudaSuccess) return e;
-  size_t grid = (size_t)num_sms;
-  if (upper_tiles < grid) grid = upper_tiles;
-  if (grid == 0) return cudaSuccess;
-  fn<<<(unsigned)grid, C::THREADS, smem, st>>>(a);
+  if (CL == 1) {
+    size_t grid = (size_t)num_sms;
+    if (upper_tiles < grid) grid = upper_tiles;
+    if (grid == 0) return cudaSuccess;
+    fn<<<(unsigned)grid, C::THREADS, smem, st>>>(a);
+    return cudaGetLastError();
+  }
+  // Persistent grid of as many CTA pairs as can be resident at once; upper_tiles
+  // counts pair units here.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)(num_sms / CL * CL), 1, 1);
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, (const void*)fn, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters <= 0) return cudaErrorInvalidConfiguration;
+  size_t n = (size_t)clusters;
+  if (upper_tiles < n) n = upper_tiles;
+  if (n == 0) return cudaSuccess;
+  cfg.gridDim = dim3((unsigned)(n * CL), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, fn, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -120,6 +147,9 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
   memset(&a, 0, sizeof(a));
   const bool has_s = p.Is > 0;
   const bool tiled = p.tile == MOE_TILE_PREFILL && xg != nullptr;
+  // CTA pairs share each token tile when every group has an even number of
+  // 64-row feature blocks.
+  const bool pair_g = tiled && (p.I / 64) % 2 == 0 && (!has_s || (p.Is / 64) % 2 == 0);
   bool ok = make_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
             make_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64);
   if (ok && has_s)
@@ -127,8 +157,8 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
          make_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64);
   if (ok) {
     if (tiled)  // [0]: routed rows in expert order; [1]: x itself for the shared expert
-      ok = make_map(&a.tmB[0], xg, p.dtype, (uint64_t)p.T * p.k, p.H, 256) &&
-           make_map(&a.tmB[1], x, p.dtype, p.T, p.H, 256);
+      ok = make_map(&a.tmB[0], xg, p.dtype, (uint64_t)p.T * p.k, p.H, pair_g ? 128 : 256) &&
+           make_map(&a.tmB[1], x, p.dtype, p.T, p.H, pair_g ? 128 : 256);
     else
       ok = make_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
   }
@@ -165,6 +195,12 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
                : launch_variant<float, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st);
   }
   const size_t ub = tile_upper_bound(p.T, p.k, p.E, 256, rb, sb);
+  if (pair_g)
+    return p.dtype == MOE_DTYPE_BF16
+               ? launch_variant<__nv_bfloat16, true, 256, 4, kTiled, 2>(a, p.num_sms, p.E,
+                                                                       (ub + 1) / 2, st)
+               : launch_variant<float, true, 256, 4, kTiled, 2>(a, p.num_sms, p.E,
+                                                               (ub + 1) / 2, st);
   if (tiled)
     return p.dtype == MOE_DTYPE_BF16
                ? launch_variant<__nv_bfloat16, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st)
@@ -181,7 +217,9 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
   GroupedGemmArgs a;
   memset(&a, 0, sizeof(a));
   const bool has_s = p.Is > 0;
-  const uint32_t bn = p.tile == MOE_TILE_DECODE ? 32 : 256;  // token box = token tile
+  // Token box = token tile, or half of it when CTA pairs share the tile.
+  const bool pair_d = p.tile == MOE_TILE_PREFILL && (p.H / 128) % 2 == 0;
+  const uint32_t bn = p.tile == MOE_TILE_DECODE ? 32 : (pair_d ? 128 : 256);
   bool ok = make_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
             make_map(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, bn);
   if (ok && has_s)
@@ -220,6 +258,12 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
                : launch_variant<float, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st);
   }
   const size_t ub = tile_upper_bound(p.T, p.k, p.E, 256, rb, sb);
+  if (pair_d)
+    return p.dtype == MOE_DTYPE_BF16
+               ? launch_variant<__nv_bfloat16, false, 256, 4, kTiled, 2>(a, p.num_sms, p.E,
+                                                                        (ub + 1) / 2, st)
+               : launch_variant<float, false, 256, 4, kTiled, 2>(a, p.num_sms, p.E,
+                                                                (ub + 1) / 2, st);
   return p.dtype == MOE_DTYPE_BF16
              ? launch_variant<__nv_bfloat16, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st)
              : launch_variant<float, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);

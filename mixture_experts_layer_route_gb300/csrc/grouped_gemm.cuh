@@ -41,6 +41,13 @@
 //    contiguous, one TMA box of BN rows.
 // All TMA loads of a stage are issued in one SIMT step with per-lane operands.
 //
+// Clusters (CL = 2, prefill-sized tiled variants): the two CTAs of a cluster
+// take adjacent feature blocks of the same group and token tile. Each loads its
+// own weight rows and half of the token box, multicast into both CTAs, so the
+// token tile crosses L2 once per pair; MMA completions are committed to the
+// empty barriers of both CTAs, so a stage is refilled only when both are done
+// with it.
+//
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread) and
 // TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each), warps 6-9
 // (kCpAsync only) = token-row gather.
@@ -76,7 +83,7 @@ struct GroupedGemmArgs {
 
 enum BMode : int { kGather4 = 0, kCpAsync = 1, kTiled = 2 };
 
-template <typename TIn, bool GATED, int BN, int STAGES, int BMODE>
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1>
 struct GemmCfg {
   static constexpr int BM = 128;                     // MMA M (weight rows)
   static constexpr int WM = GATED ? 64 : 128;        // output features per tile
@@ -90,6 +97,7 @@ struct GemmCfg {
   static constexpr int GATHER_WARPS = (BMODE == kCpAsync) ? 4 : 0;
   static constexpr int THREADS = 192 + 32 * GATHER_WARPS;
   static constexpr int CP_LAG = STAGES - 2;  // stages of cp.async in flight per thread
+  static_assert(CL == 1 || (CL == 2 && BMODE == kTiled), "clusters share tiled token boxes");
   static constexpr bool TF32 = sizeof(TIn) == 4;
   static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
                     TMEM_COLS == 512,
@@ -131,10 +139,10 @@ __device__ __forceinline__ Tile decode_tile(int u, const int32_t* prefix, const 
   return t;
 }
 
-template <typename TIn, bool GATED, int BN, int STAGES, int BMODE>
-__global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREADS, 1)
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL>
+__global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GroupedGemmArgs args) {
-  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE>;
+  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>;
   static_assert(GATED || BMODE == kTiled, "the down projection reads contiguous h rows");
   static_assert(BMODE != kGather4 || BN <= 128, "gather4 is for decode-sized token tiles");
   extern __shared__ uint8_t smem_raw[];
@@ -151,6 +159,10 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E, G = E + 1;
+  // Units are walked per cluster; CTA `crank` of a cluster takes feature block
+  // 2 * nb + crank of each pair unit.
+  const int crank = CL == 2 ? (int)cluster_ctarank() : 0;
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
@@ -160,7 +172,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1 + C::GATHER_WARPS);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CL);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -183,7 +195,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
     int local = 0;
     for (int g = g0; g < min(G, g0 + per); ++g) {
       const int m = offs[g + 1] - offs[g];
-      const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / C::WM;
+      const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / (C::WM * CL);
       local += ((m + BN - 1) / BN) * nf;
     }
     int incl = local;
@@ -196,13 +208,14 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
     for (int g = g0; g < min(G, g0 + per); ++g) {
       prefix[g] = run;
       const int m = offs[g + 1] - offs[g];
-      const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / C::WM;
+      const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / (C::WM * CL);
       run += ((m + BN - 1) / BN) * nf;
     }
     if (lane == 31) prefix[G] = incl;
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CL > 1) cluster_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int total = prefix[G];
@@ -216,8 +229,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
     uint32_t it = 0;
     bool ok = true;
     bool skip_once = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+    for (int u = cid; u < total && ok; u += ncl) {
+      Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      tl.nb = tl.nb * CL + crank;
       const bool shared = tl.g == E;
       const int kdim = shared ? args.kdim_shared : args.kdim_routed;
       const int a_row0 = (shared ? 0 : tl.g * args.n_out_routed) + tl.nb * C::WM;
@@ -260,9 +274,11 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
         my_off = 64 * 128;
       }
       if (BMODE == kTiled && lane == NA) {
+        // With a cluster, this CTA fetches rows [crank * BN/2, (crank + 1) * BN/2)
+        // of the token box for both CTAs.
         my_map = &args.tmB[shared ? 1 : 0];
-        my_row = b_row0;
-        my_off = C::A_BYTES;
+        my_row = b_row0 + crank * (BN / CL);
+        my_off = C::A_BYTES + crank * (BN / CL) * 128;
         my_pol = pol_t;
       }
       for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
@@ -284,7 +300,14 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
         }
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
         __syncwarp();
-        if (lane < NLOADS) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
+        if constexpr (CL == 1) {
+          if (lane < NLOADS) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
+        } else {
+          if (lane < NA) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
+          if (lane == NA)
+            tma_load_2d_multicast(a_dst + my_off, my_map, kx, my_row, full_bar(s), 0x3,
+                                  my_pol);
+        }
         if constexpr (BMODE == kGather4) {
 #pragma unroll
           for (int j = 0; j < NQ; ++j) {
@@ -311,8 +334,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
       uint32_t it = 0, lt = 0;
       constexpr uint32_t fmt = C::TF32 ? 2u : 1u;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++lt) {
-        const Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      for (int u = cid; u < total && ok; u += ncl, ++lt) {
+        Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      tl.nb = tl.nb * CL + crank;
         const int kdim = (tl.g == E) ? args.kdim_shared : args.kdim_routed;
         const uint32_t acc = lt & 1u, around = lt >> 1;
         if (!mbar_wait(tempty_bar(acc), (around & 1u) ^ 1u, args.status, limit)) break;
@@ -336,7 +360,10 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
                                 umma_desc_sw128(b_addr + kk * 32), idesc,
                                 (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(empty_bar(s));
+          if constexpr (CL == 1)
+            umma_commit(empty_bar(s));
+          else
+            umma_commit_multicast(empty_bar(s), 0x3);
         }
         if (!ok) break;
         umma_commit(tfull_bar(acc));
@@ -352,8 +379,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
     const int et = threadIdx.x - 64;        // 0..127
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t lt = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++lt) {
-      const Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+    for (int u = cid; u < total; u += ncl, ++lt) {
+      Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      tl.nb = tl.nb * CL + crank;
       const bool shared = tl.g == E;
       const uint32_t acc = lt & 1u, around = lt >> 1;
       if (et == 0) *epi_flag = mbar_wait(tfull_bar(acc), around & 1u, args.status, limit) ? 1 : 0;
@@ -456,8 +484,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
       const int ld = args.kdim_routed;  // x row length (H), also for the shared expert
       uint32_t it = 0, arrived = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      for (int u = cid; u < total && ok; u += ncl) {
+        Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      tl.nb = tl.nb * CL + crank;
         const bool shared = tl.g == E;
         const int kdim = shared ? args.kdim_shared : args.kdim_routed;
         const TIn* src[RPT];
@@ -511,6 +540,8 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE>::THREAD
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  // No CTA leaves while its peer may still multicast into it or commit to it.
+  if constexpr (CL > 1) cluster_sync();
 }
 
 }  // namespace moe
