@@ -15,6 +15,7 @@
 // written: the outputs are the offsets and two index arrays.
 #include "common.cuh"
 #include "kernels.h"
+#include "permute_block.cuh"
 
 namespace moe {
 
@@ -28,110 +29,8 @@ __global__ void __launch_bounds__(PM_THREADS, 1)
                    int32_t* __restrict__ offsets, int32_t* __restrict__ gather_idx,
                    int32_t* __restrict__ slot_pos, int* status) {
   extern __shared__ int32_t sm[];
-  int32_t* hist = sm;                        // [PM_WARPS][E]
-  int32_t* total = sm + PM_WARPS * E;        // [E]
-  int32_t* warp_sums = total + E;            // [PM_WARPS]
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = T * k;
-  const int chunk = ((n + PM_WARPS * 32 - 1) / (PM_WARPS * 32)) * 32;
-  const int beg = min(n, warp * chunk), end = min(n, beg + chunk);
-  const uint32_t lt_mask = (1u << lane) - 1u;
-
-  for (int i = tid; i < PM_WARPS * E; i += PM_THREADS) hist[i] = 0;
-  __syncthreads();
-
-  // Pass 1: per-warp counts.
-  bool bad = false;
-  for (int base = beg; base < end; base += 32) {
-    const int s = base + lane;
-    int e = -1;
-    if (s < end) {
-      e = ids[s];
-      if (e < 0 || e >= E) {
-        bad = true;
-        e = -1;
-      }
-    }
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && (peers & lt_mask) == 0) hist[warp * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  if (bad) set_status(status, MOE_ERR_DEVICE_CHECK);
-  __syncthreads();
-
-  // Column scan over warps: hist[w][e] <- count of e in warps before w.
-  for (int e = tid; e < E; e += PM_THREADS) {
-    int run = 0;
-    for (int w = 0; w < PM_WARPS; ++w) {
-      const int c = hist[w * E + e];
-      hist[w * E + e] = run;
-      run += c;
-    }
-    total[e] = run;
-  }
-  __syncthreads();
-
-  // Exclusive scan of total[] over experts (E <= 1024 = one element per thread
-  // per round); offsets written out.
-  int carry = 0;
-  for (int e0 = 0; e0 < E; e0 += PM_THREADS) {
-    const int e = e0 + tid;
-    const int v = (e < E) ? total[e] : 0;
-    int incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      int ws = warp_sums[lane];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, ws, off);
-        if (lane >= off) ws += o;
-      }
-      warp_sums[lane] = ws;  // inclusive over warps
-    }
-    __syncthreads();
-    const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
-    const int excl = before + incl - v;
-    if (e < E) {
-      total[e] = excl;  // now: first position of expert e
-      offsets[e] = excl;
-    }
-    carry += warp_sums[PM_WARPS - 1];
-    __syncthreads();
-  }
-  if (tid == 0) {
-    offsets[E] = carry;
-    offsets[E + 1] = carry + (has_shared ? T : 0);
-  }
-
-  // Pass 2: stable ranks and scatter.
-  for (int base = beg; base < end; base += 32) {
-    const int s = base + lane;
-    int e = -1;
-    if (s < end) {
-      e = ids[s];
-      if (e < 0 || e >= E) e = -1;
-    }
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    int cnt = 0;
-    if (e >= 0) cnt = hist[warp * E + e];
-    __syncwarp();
-    if (e >= 0) {
-      const int p = total[e] + cnt + __popc(peers & lt_mask);
-      gather_idx[p] = s;
-      slot_pos[s] = p;
-      if ((peers & lt_mask) == 0) hist[warp * E + e] = cnt + __popc(peers);
-    } else if (s < end) {
-      slot_pos[s] = -1;
-    }
-    __syncwarp();
-  }
+  permute_block<PM_WARPS, false>(ids, T, E, k, has_shared, offsets, gather_idx, slot_pos, status,
+                                 sm);
 }
 
 // Large T*k: the same stable order from two grid-wide kernels. Chunk c owns

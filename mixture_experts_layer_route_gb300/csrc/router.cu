@@ -299,11 +299,23 @@ __global__ void __launch_bounds__(256, 1) router_logits_big_kernel(
 
 // Sum of S partial logits in ascending slice order, then the bias: identical
 // arithmetic in the reduction kernel and in the route kernel.
+// The loads of each batch of 8 slices are issued together (they are
+// independent); the additions keep ascending slice order.
 __device__ __forceinline__ float reduce_partials(const float* __restrict__ part, int S, int T,
                                                  int E, int t, int e,
                                                  const float* __restrict__ bias) {
-  float v = part[(size_t)t * E + e];
-  for (int s = 1; s < S; ++s) v += part[((size_t)s * T + t) * E + e];
+  const size_t stride = (size_t)T * E;
+  const float* p = part + (size_t)t * E + e;
+  float v = p[0];
+  int s = 1;
+  for (; s + 8 <= S; s += 8) {
+    float q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = p[(size_t)(s + j) * stride];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v += q[j];
+  }
+  for (; s < S; ++s) v += p[(size_t)s * stride];
   if (bias) v += bias[e];
   return v;
 }
@@ -322,31 +334,14 @@ __global__ void logits_reduce_kernel(const float* __restrict__ part, int S, int 
 // S == 1: `src` holds final logits (bias already added). S > 1: `src` holds S
 // partial slices; they are reduced here and, if logits_out != nullptr, the
 // reduced logits are written out.
+// Top-k and gate weights of one token by one warp. v[i] holds the logit of
+// expert lane + 32 i (-inf past E). k rounds of warp arg-max over the not yet
+// chosen values, ties to the lower expert index; lane r keeps round r.
 template <int NV>
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ src, int S,
-                                                    const float* __restrict__ bias, int T, int E,
-                                                    int k, int renorm,
-                                                    float* __restrict__ logits_out,
-                                                    int32_t* __restrict__ ids,
-                                                    float* __restrict__ w) {
+__device__ __forceinline__ void route_warp(const float (&v)[NV], int E, int k, int renorm,
+                                           int32_t* __restrict__ ids_row,
+                                           float* __restrict__ w_row) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-
-  float v[NV];
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      v[i] = (S == 1) ? src[(size_t)t * E + e] : reduce_partials(src, S, T, E, t, e, bias);
-      if (S > 1 && logits_out) logits_out[(size_t)t * E + e] = v[i];
-    } else {
-      v[i] = -INFINITY;
-    }
-  }
-
-  // k rounds of warp arg-max over the not-yet-chosen values; ties go to the
-  // lower expert index. Lane r keeps round r's (value, index).
   uint32_t taken = 0;
   float my_val = 0.f;
   int my_idx = 0;
@@ -392,9 +387,33 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ sr
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, off);
   if (lane < k) {
-    ids[(size_t)t * k + lane] = my_idx;
-    w[(size_t)t * k + lane] = p / ssum;
+    ids_row[lane] = my_idx;
+    w_row[lane] = p / ssum;
   }
+}
+
+template <int NV>
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ src, int S,
+                                                    const float* __restrict__ bias, int T, int E,
+                                                    int k, int renorm,
+                                                    float* __restrict__ logits_out,
+                                                    int32_t* __restrict__ ids,
+                                                    float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      v[i] = (S == 1) ? src[(size_t)t * E + e] : reduce_partials(src, S, T, E, t, e, bias);
+      if (S > 1 && logits_out) logits_out[(size_t)t * E + e] = v[i];
+    } else {
+      v[i] = -INFINITY;
+    }
+  }
+  route_warp<NV>(v, E, k, renorm, ids + (size_t)t * k, w + (size_t)t * k);
 }
 
 }  // namespace
