@@ -154,11 +154,14 @@ def roofline_numbers(cfg, counts):
 
 
 def kernels_per_step(cfg):
-    """Kernels one moe_forward launches: router logits, route, permute, [dispatch
-    copy of the routed rows for prefill-sized tiles], gated GEMM, down GEMM,
-    combine."""
-    prefill = cfg.T * cfg.k > 32 * cfg.E
-    return 6 + (1 if prefill else 0)
+    """Kernels one moe_forward launches with the automatic tile choice: router
+    logits, route, permute (one kernel up to 4096 slots, else count + scatter),
+    [the expert-ordered copy of the routed rows when 128/256-token tiles can
+    run], per GEMM one launch for each token tile a group's row count can call
+    for (32: always; 128: T > 64; 256: T > 128), combine."""
+    permute = 1 if cfg.T * cfg.k <= 4096 else 2
+    variants = 1 + (cfg.T > 64) + (cfg.T > 128)
+    return 2 + permute + (1 if cfg.T > 64 else 0) + 2 * variants + 1
 
 
 def build_layer(cfg, device, seed=0):

@@ -67,9 +67,17 @@ typedef enum {
 
 typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
 
-/* Token-tile choice of the grouped GEMMs. AUTO picks DECODE when the mean
- * number of tokens per expert (T*k/E) is at most 32, else PREFILL. */
-typedef enum { MOE_TILE_AUTO = 0, MOE_TILE_DECODE = 1, MOE_TILE_PREFILL = 2 } moe_tile;
+/* Token-tile choice of the grouped GEMMs. AUTO chooses per expert, on the GPU,
+ * from that expert's row count: 32-token tiles up to 32 rows, 128-token tiles
+ * up to 128 rows, 256-token tiles beyond; a batch of T <= 64 tokens uses
+ * 32-token tiles throughout. DECODE, MEDIUM and PREFILL force the 32-, 128- or
+ * 256-token tile for every expert. */
+typedef enum {
+  MOE_TILE_AUTO = 0,
+  MOE_TILE_DECODE = 1,
+  MOE_TILE_PREFILL = 2,
+  MOE_TILE_MEDIUM = 3
+} moe_tile;
 
 /* Test hooks (moe_problem.flags). Never set in production. */
 #define MOE_FLAG_TEST_SKIP_SIGNAL 0x1u /* the GEMM producer withholds its first load

@@ -13,7 +13,7 @@ import torch
 
 from ._binding import (  # noqa: F401
     EXPORTED, MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_FLAG_TEST_SKIP_SIGNAL, MOE_OK,
-    MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_PREFILL, STATUS_NAMES, MoEError, MoEProblem,
+    MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_MEDIUM, MOE_TILE_PREFILL, STATUS_NAMES, MoEError, MoEProblem,
     down_combine, down_combine_noalloc, forward, get_device_status, grouped_swiglu_gemm, load_library, make_problem,
     permute, reset_device_status, route, router_logits, status_string, workspace_layout,
     workspace_size)

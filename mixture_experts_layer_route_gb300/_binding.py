@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
                 6: "MOE_ERR_DEVICE_CHECK"}
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
-MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_PREFILL = 0, 1, 2
+MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_PREFILL, MOE_TILE_MEDIUM = 0, 1, 2, 3
 MOE_FLAG_TEST_SKIP_SIGNAL = 0x1
 
 # Every symbol include/moe_api.h declares.

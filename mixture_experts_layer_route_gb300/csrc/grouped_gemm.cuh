@@ -27,19 +27,19 @@
 //    fp32 product into the token-ordered slot buffer Y[t][r][:] (the combine
 //    sums the slots afterwards in rank order).
 //
-// Token-operand loading (B), one of three modes:
-//  kGather4 (decode-sized gated tiles): TMA tile::gather4, 4 rows per
-//    instruction straight from x by token index.
-//  kCpAsync (prefill-sized gated tiles): four extra producer warps copy the
-//    tile's token rows from x with 16-byte cp.async into the 128-byte-swizzled
-//    layout, then make them visible to the tensor core (async proxy) with
-//    fence.proxy.async before arriving on the stage barrier. An SM accepts only
-//    one TMA instruction every ~70-150 cycles, so 4-row gathers cannot fill a
-//    256-token stage in time; the load/store unit can.
-//  kTiled (down projection, and prefill-sized gated tiles once the routed
+// Token-operand loading (B), one of two modes:
+//  kGather4 (32-token gated tiles): TMA tile::gather4, 4 rows per instruction
+//    straight from x by token index (8 instructions per stage).
+//  kTiled (down projection, and 128/256-token gated tiles once the routed
 //    token rows were copied into expert order): the tile's rows are
-//    contiguous, one TMA box of BN rows.
+//    contiguous, one TMA box per stage. An SM accepts one TMA instruction only
+//    every ~70-150 cycles, so a 256-token stage cannot be filled 4 rows at a
+//    time; one box carries it.
 // All TMA loads of a stage are issued in one SIMT step with per-lane operands.
+//
+// Row-range filter: a launch only schedules the groups whose row count lies in
+// [m_lo, m_hi]; the host launches one variant (token tile 32, 128 or 256) per
+// range, so each expert gets the tile its own load calls for.
 //
 // Clusters (CL = 2, prefill-sized tiled variants): the two CTAs of a cluster
 // take adjacent feature blocks of the same group and token tile. Each loads its
@@ -49,8 +49,7 @@
 // with it.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread) and
-// TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each), warps 6-9
-// (kCpAsync only) = token-row gather.
+// TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each).
 // A STAGES-deep shared-memory ring (full/empty mbarriers) feeds the MMA; two
 // TMEM accumulators (tfull/tempty mbarriers) let the epilogue of one tile run
 // under the main loop of the next. Every wait is bounded (status word).
@@ -66,7 +65,6 @@ struct GroupedGemmArgs {
   CUtensorMap tmA[4];
   // GATED: [0] x (1-row box, gather4). DOWN: [0] h, [1] h_shared (32-row box).
   CUtensorMap tmB[2];
-  const void* b_src;          // kCpAsync: x [T][H] (token rows are gathered from it)
   const int32_t* offsets;     // [E+2]
   const int32_t* gather_idx;  // [T*k]
   const float* topk_w;        // [T*k] (DOWN)
@@ -79,9 +77,10 @@ struct GroupedGemmArgs {
   int kdim_routed, kdim_shared;     // contraction length per group
   int ld_out_routed, ld_out_shared; // row stride (elements) of out / out_shared
   unsigned flags;
+  int m_lo, m_hi;             // groups with m_lo <= rows <= m_hi are scheduled
 };
 
-enum BMode : int { kGather4 = 0, kCpAsync = 1, kTiled = 2 };
+enum BMode : int { kGather4 = 0, kTiled = 2 };
 
 template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1>
 struct GemmCfg {
@@ -94,9 +93,7 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
-  static constexpr int GATHER_WARPS = (BMODE == kCpAsync) ? 4 : 0;
-  static constexpr int THREADS = 192 + 32 * GATHER_WARPS;
-  static constexpr int CP_LAG = STAGES - 2;  // stages of cp.async in flight per thread
+  static constexpr int THREADS = 192;
   static_assert(CL == 1 || (CL == 2 && BMODE == kTiled), "clusters share tiled token boxes");
   static constexpr bool TF32 = sizeof(TIn) == 4;
   static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
@@ -171,7 +168,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1 + C::GATHER_WARPS);
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), CL);
     }
     for (int a = 0; a < 2; ++a) {
@@ -196,7 +193,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     for (int g = g0; g < min(G, g0 + per); ++g) {
       const int m = offs[g + 1] - offs[g];
       const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / (C::WM * CL);
-      local += ((m + BN - 1) / BN) * nf;
+      if (m >= args.m_lo && m <= args.m_hi) local += ((m + BN - 1) / BN) * nf;
     }
     int incl = local;
 #pragma unroll
@@ -209,7 +206,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       prefix[g] = run;
       const int m = offs[g + 1] - offs[g];
       const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / (C::WM * CL);
-      run += ((m + BN - 1) / BN) * nf;
+      if (m >= args.m_lo && m <= args.m_hi) run += ((m + BN - 1) / BN) * nf;
     }
     if (lane == 31) prefix[G] = incl;
   }
@@ -373,7 +370,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       mbar_wait(drain_bar, 0, nullptr, 20000000ull);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int et = threadIdx.x - 64;        // 0..127
@@ -469,68 +466,6 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         named_barrier_sync(1, 128);
       }
       if (et == 0) mbar_arrive(tempty_bar(acc));
-    }
-  }
-
-  if constexpr (BMODE == kCpAsync) {
-    if (warp >= 6) {
-      // ------------------------------------------------------------ token-row gather
-      // Thread gt owns 16-byte chunk `ch` of rows r0, r0 + 16, ... of each stage;
-      // a warp covers 4 whole 128-byte rows per instruction.
-      constexpr int RPT = BN / 16;  // rows per thread
-      const int gt = threadIdx.x - 192;
-      const int ch = gt & 7, r0 = gt >> 3;
-      const TIn* xsrc = reinterpret_cast<const TIn*>(args.b_src);
-      const int ld = args.kdim_routed;  // x row length (H), also for the shared expert
-      uint32_t it = 0, arrived = 0;
-      bool ok = true;
-      for (int u = cid; u < total && ok; u += ncl) {
-        Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
-      tl.nb = tl.nb * CL + crank;
-        const bool shared = tl.g == E;
-        const int kdim = shared ? args.kdim_shared : args.kdim_routed;
-        const TIn* src[RPT];
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-          const int r = r0 + 16 * i;
-          int tok = -1;
-          if (r < tl.n_valid)
-            tok = shared ? tl.p0 - offs[E] + r : args.gather_idx[tl.p0 + r] / args.k;
-          src[i] = tok >= 0 ? xsrc + (size_t)tok * ld + ch * (16 / sizeof(TIn)) : nullptr;
-        }
-        for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t round = it / STAGES;
-          int wok = 1;
-          if (lane == 0) wok = mbar_wait(empty_bar(s), (round & 1u) ^ 1u, args.status, limit);
-          wok = __shfl_sync(0xffffffffu, wok, 0);
-          if (!wok) {
-            ok = false;
-            break;
-          }
-          const uint32_t b_dst = smem_u32(stages + (size_t)s * C::STAGE_BYTES) + C::A_BYTES;
-#pragma unroll
-          for (int i = 0; i < RPT; ++i) {
-            const int r = r0 + 16 * i;
-            if (src[i])
-              cp_async_16(b_dst + r * 128 + ((ch ^ (r & 7)) << 4), src[i] + kb * C::BK);
-          }
-          cp_async_commit();
-          if (it >= (uint32_t)C::CP_LAG) {
-            // The stage issued CP_LAG steps ago has landed: publish it.
-            cp_async_wait<C::CP_LAG>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full_bar((it - C::CP_LAG) % STAGES));
-            ++arrived;
-          }
-        }
-      }
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (ok && lane == 0)
-        for (uint32_t i = arrived; i < it; ++i) mbar_arrive(full_bar(i % STAGES));
     }
   }
 

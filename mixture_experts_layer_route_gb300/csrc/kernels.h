@@ -34,15 +34,16 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* gather_idx, int P, 
 // Grouped GEMMs (grouped_gemm.cu).
 struct GemmProblem {
   int dtype;  // MOE_DTYPE_*
-  int tile;   // MOE_TILE_DECODE or MOE_TILE_PREFILL (resolved)
+  int tile;   // moe_tile: AUTO chooses per expert from its row count
   int T, H, E, k, I, Is;
   unsigned flags;
   unsigned long long limit_ns;
   int num_sms;
 };
 // xg: the routed token rows in expert order ([T*k][H], from launch_gather_rows);
-// required for MOE_TILE_PREFILL, ignored for MOE_TILE_DECODE (rows gathered in
-// the GEMM's own loads).
+// required when gemm_needs_expert_order_copy(p) (128/256-token tiles may run),
+// ignored otherwise (32-token tiles gather rows in the GEMM's own loads).
+bool gemm_needs_expert_order_copy(const GemmProblem& p);
 cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* xg,
                                const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
                                const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,

@@ -40,9 +40,12 @@ int sm_count() {
 // workspace size independent of the device queried.
 constexpr int kRouterSplitSms = 152;
 
-int resolve_tile(const moe_problem& p) {
-  if (p.tile != MOE_TILE_AUTO) return p.tile;
-  return (p.T * p.k <= 32 * p.E) ? MOE_TILE_DECODE : MOE_TILE_PREFILL;
+// 128/256-token tiles read the routed token rows from an expert-ordered copy;
+// they can run unless every expert is forced to, or bound to, 32-token tiles.
+bool needs_copy(const moe_problem& p) {
+  if (p.tile == MOE_TILE_DECODE) return false;
+  if (p.tile == MOE_TILE_AUTO) return p.T > 64;
+  return true;
 }
 
 size_t elem_bytes(int dtype) { return dtype == MOE_DTYPE_BF16 ? 2 : 4; }
@@ -70,7 +73,7 @@ Layout layout_of(const moe_problem& p) {
   L.gather = take(T * k * 4);
   L.slotpos = take(T * k * 4);
   // Prefill-sized tiles read the routed token rows from an expert-ordered copy.
-  L.xg = resolve_tile(p) == MOE_TILE_PREFILL ? take(T * k * (size_t)p.H * es) : 0;
+  L.xg = needs_copy(p) ? take(T * k * (size_t)p.H * es) : 0;
   L.h = take(T * k * (size_t)p.I * es);
   L.hs = p.I_shared > 0 ? take(T * (size_t)p.I_shared * es) : 0;
   L.Y = take(T * KP * (size_t)p.H * 4);
@@ -88,7 +91,7 @@ moe_status check_problem(const moe_problem* pb) {
   if (p.k > p.E || p.k > 32 || p.E > 1024) return MOE_ERR_INVALID_ARG;
   if (p.H % 128 != 0 || p.I % 64 != 0 || p.I_shared % 64 != 0) return MOE_ERR_INVALID_ARG;
   if (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
-  if (p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_PREFILL) return MOE_ERR_INVALID_ARG;
+  if (p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM) return MOE_ERR_INVALID_ARG;
   if (p.renorm != 0 && p.renorm != 1) return MOE_ERR_INVALID_ARG;
   if (p.out_f32 != 0 && p.out_f32 != 1) return MOE_ERR_INVALID_ARG;
   const int64_t lim = (int64_t)1 << 30;
@@ -101,7 +104,7 @@ moe_status check_problem(const moe_problem* pb) {
 GemmProblem gemm_problem(const moe_problem& p) {
   GemmProblem g;
   g.dtype = p.dtype;
-  g.tile = resolve_tile(p);
+  g.tile = p.tile;
   g.T = (int)p.T;
   g.H = (int)p.H;
   g.E = (int)p.E;
@@ -253,7 +256,7 @@ moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
   cudaStream_t st = (cudaStream_t)stream;
   void* xg = nullptr;
   cudaError_t e = cudaSuccess;
-  if (g.tile == MOE_TILE_PREFILL) {
+  if (gemm_needs_expert_order_copy(g)) {
     xg = at<void>(workspace, L.xg);
     e = launch_gather_rows(x, gather_idx, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
                            g.num_sms, st);
@@ -339,7 +342,7 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
     e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status,
                        at<int32_t>(workspace, L.pscratch), st);
   void* xg = nullptr;
-  if (e == cudaSuccess && g.tile == MOE_TILE_PREFILL) {
+  if (e == cudaSuccess && gemm_needs_expert_order_copy(g)) {
     xg = at<void>(workspace, L.xg);
     e = launch_gather_rows(x, gidx, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
                            g.num_sms, st);

@@ -68,7 +68,7 @@ extern "C" moe_status moe_down_combine_noalloc(const moe_problem* pb, const void
   if (p.T < 0 || p.H <= 0 || p.E <= 0 || p.k <= 0 || p.I <= 0 || p.I_shared < 0 ||
       p.k > p.E || p.k > 32 || p.E > 1024 || p.H % 128 != 0 || p.I % 64 != 0 ||
       p.I_shared % 64 != 0 || (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32) ||
-      p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_PREFILL || (p.out_f32 != 0 && p.out_f32 != 1))
+      p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM || (p.out_f32 != 0 && p.out_f32 != 1))
     return MOE_ERR_INVALID_ARG;
   if (p.T == 0) return MOE_OK;
   const bool has_s = p.I_shared > 0;
@@ -95,8 +95,7 @@ extern "C" moe_status moe_down_combine_noalloc(const moe_problem* pb, const void
     return MOE_ERR_CUDA;
   GemmProblem g;
   g.dtype = p.dtype;
-  g.tile = p.tile != MOE_TILE_AUTO ? p.tile
-                                   : ((p.T * p.k <= 32 * p.E) ? MOE_TILE_DECODE : MOE_TILE_PREFILL);
+  g.tile = p.tile;
   g.T = (int)p.T;
   g.H = (int)p.H;
   g.E = (int)p.E;

@@ -192,8 +192,13 @@ def test_permute_out_of_range_id_sets_device_check():
 
 # ------------------------------------------------------------------ a4 / a5 GEMMs
 
-# Segment lengths around both token tiles (32 and 256) and the 16-row MMA step.
-RAGGED = [0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 127, 128, 129, 255, 256, 257, 300, 511, 0, 4]
+# Segment lengths around the token tiles (32, 128, 256), which are also the row
+# counts where the automatic choice changes tile (32|33, 128|129), and the
+# 16-row MMA step.
+RAGGED = [0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 192, 193, 255, 256, 257,
+          300, 511, 0, 4]
+TILES = [m.MOE_TILE_AUTO, m.MOE_TILE_DECODE, m.MOE_TILE_MEDIUM, m.MOE_TILE_PREFILL]
+TILE_IDS = ["auto", "t32", "t128", "t256"]
 
 
 def _gemm_case(case, dtype):
@@ -219,7 +224,7 @@ def _gemm_case(case, dtype):
     return cfg, d, np.ascontiguousarray(ids, dtype=np.int32), np.ascontiguousarray(w, np.float32)
 
 
-@pytest.mark.parametrize("tile", [m.MOE_TILE_DECODE, m.MOE_TILE_PREFILL])
+@pytest.mark.parametrize("tile", TILES, ids=TILE_IDS)
 @pytest.mark.parametrize("case,dtype", [("ragged", "bf16"), ("random", "bf16"),
                                         ("shared", "bf16"), ("zipf", "bf16"),
                                         ("random", "f32"), ("shared", "f32")])
@@ -245,7 +250,7 @@ def test_grouped_swiglu_gemm(oracle, case, dtype, tile):
                      tf32=dtype == "f32")
 
 
-@pytest.mark.parametrize("tile", [m.MOE_TILE_DECODE, m.MOE_TILE_PREFILL])
+@pytest.mark.parametrize("tile", TILES, ids=TILE_IDS)
 @pytest.mark.parametrize("case,dtype", [("ragged", "bf16"), ("random", "bf16"),
                                         ("shared", "bf16"), ("zipf", "bf16"),
                                         ("random", "f32"), ("shared", "f32")])
