@@ -23,20 +23,10 @@
 namespace moe {
 
 namespace {
-
-constexpr int kMaxExperts = 1024;  // the C ABI's limit on E
-// Automatic tile choice by the rows m of each group: 32-token tiles for
-// m <= kLightMax, 128-token tiles up to kMediumMax, 256-token tiles beyond
-// (thresholds measured on the Qwen3-, Zipf- and DeepSeek-shaped layers). A batch of
-// at most kSmallBatch tokens uses 32-token tiles throughout, so it runs one launch
-// per GEMM and needs no expert-ordered copy of its rows.
-constexpr int kLightMax = 32;
-constexpr int kMediumMax = 128;
-constexpr int kSmallBatch = 64;
-
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no libcuda link).
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
@@ -48,11 +38,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   });
   return g_encode;
 }
+}  // namespace
 
 // 2-D row-major matrix [rows][cols] of `es`-byte elements; box = 128 bytes of
 // columns x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
-              uint32_t box_rows) {
+bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows) {
   auto enc = encoder();
   if (!enc) return false;
   const uint32_t es = dtype == MOE_DTYPE_BF16 ? 2 : 4;
@@ -67,6 +58,18 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
+
+constexpr int kMaxExperts = 1024;  // the C ABI's limit on E
+// Automatic tile choice by the rows m of each group: 32-token tiles for
+// m <= kLightMax, 128-token tiles up to kMediumMax, 256-token tiles beyond
+// (thresholds measured on the Qwen3-, Zipf- and DeepSeek-shaped layers). A batch of
+// at most kSmallBatch tokens uses 32-token tiles throughout, so it runs one launch
+// per GEMM and needs no expert-ordered copy of its rows.
+constexpr int kLightMax = 32;
+constexpr int kMediumMax = 128;
+constexpr int kSmallBatch = 64;
 
 struct AttrCache {
   std::mutex mu;
@@ -201,20 +204,20 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
     const bool cl2 = v > 0 && pair;
     GroupedGemmArgs a;
     memset(&a, 0, sizeof(a));
-    bool ok = make_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
-              make_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64);
+    bool ok = make_tma_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
+              make_tma_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64);
     if (ok && has_s)
-      ok = make_map(&a.tmA[2], Wsg, p.dtype, p.Is, p.H, 64) &&
-           make_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64);
+      ok = make_tma_map(&a.tmA[2], Wsg, p.dtype, p.Is, p.H, 64) &&
+           make_tma_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64);
     if (ok) {
       if (v == 0) {
-        ok = make_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
+        ok = make_tma_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
         a.tmB[1] = a.tmB[0];
       } else {  // [0]: routed rows in expert order; [1]: x itself for the shared expert
         if (!xg) return cudaErrorInvalidValue;
         const uint32_t box = cl2 ? bn / 2 : bn;
-        ok = make_map(&a.tmB[0], xg, p.dtype, (uint64_t)p.T * p.k, p.H, box) &&
-             make_map(&a.tmB[1], x, p.dtype, p.T, p.H, box);
+        ok = make_tma_map(&a.tmB[0], xg, p.dtype, (uint64_t)p.T * p.k, p.H, box) &&
+             make_tma_map(&a.tmB[1], x, p.dtype, p.T, p.H, box);
       }
     }
     if (!ok) return cudaErrorInvalidValue;
@@ -285,11 +288,11 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
     const uint32_t box = cl2 ? bn / 2 : bn;  // token box = token tile, or half for CTA pairs
     GroupedGemmArgs a;
     memset(&a, 0, sizeof(a));
-    bool ok = make_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
-              make_map(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, box);
+    bool ok = make_tma_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
+              make_tma_map(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, box);
     if (ok && has_s)
-      ok = make_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128) &&
-           make_map(&a.tmB[1], hs, p.dtype, p.T, p.Is, box);
+      ok = make_tma_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128) &&
+           make_tma_map(&a.tmB[1], hs, p.dtype, p.T, p.Is, box);
     if (!ok) return cudaErrorInvalidValue;
     if (!has_s) {
       a.tmA[2] = a.tmA[0];

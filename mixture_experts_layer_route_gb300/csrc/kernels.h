@@ -1,17 +1,27 @@
 // Internal launch functions of the kernels behind the C ABI (not exported).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
 namespace moe {
 
+// TMA tensor map of a row-major [rows][cols] matrix of MOE_DTYPE_* elements:
+// boxes of 128 bytes of columns x box_rows rows, 128-byte swizzle, zero fill
+// out of bounds (grouped_gemm.cu). False if the driver entry point is missing
+// or the encoder rejects the shape.
+bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows);
+
 // Router (router.cu).
-int router_split_count(int64_t T, int64_t H, int64_t E, int num_sms);
+// Slices S of H whose partial logits the router writes (S == 1: final logits).
+int router_split_count(int dtype, int64_t T, int64_t H, int64_t E, int num_sms);
+// bf16: tensor cores (status/limit_ns bound its waits); fp32: CUDA cores.
 cudaError_t launch_router_logits(int dtype, const void* x, const void* Wr, const float* bias,
-                                 int T, int H, int E, int S, float* out_partials,
-                                 cudaStream_t st);
+                                 int T, int H, int E, int S, float* out_partials, int* status,
+                                 unsigned long long limit_ns, cudaStream_t st);
 cudaError_t launch_logits_reduce(const float* partials, int S, int T, int E, const float* bias,
                                  float* logits, int num_sms, cudaStream_t st);
 cudaError_t launch_route(const float* src, int S, const float* bias, int T, int E, int k,

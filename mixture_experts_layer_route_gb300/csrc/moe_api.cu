@@ -55,7 +55,7 @@ Layout layout_of(const moe_problem& p) {
   const size_t es = elem_bytes(p.dtype);
   const size_t T = (size_t)p.T, E = (size_t)p.E, k = (size_t)p.k;
   const size_t KP = k + (p.I_shared > 0 ? 1 : 0);
-  L.S = router_split_count(p.T, p.H, p.E, kRouterSplitSms);
+  L.S = router_split_count(p.dtype, p.T, p.H, p.E, kRouterSplitSms);
   size_t off = kHeader;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -190,11 +190,13 @@ moe_status moe_router_logits(const moe_problem* pb, const void* x, const void* W
   if ((s = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
   const int T = (int)pb->T, H = (int)pb->H, E = (int)pb->E;
+  const unsigned long long limit = gemm_problem(*pb).limit_ns;
   if (L.S == 1)
     return cuda_status(launch_router_logits(pb->dtype, x, W_router, router_bias, T, H, E, 1,
-                                            logits, st));
+                                            logits, status_ptr(workspace), limit, st));
   float* part = at<float>(workspace, L.partials);
-  cudaError_t e = launch_router_logits(pb->dtype, x, W_router, router_bias, T, H, E, L.S, part, st);
+  cudaError_t e = launch_router_logits(pb->dtype, x, W_router, router_bias, T, H, E, L.S, part,
+                                       status_ptr(workspace), limit, st);
   if (e == cudaSuccess) e = launch_logits_reduce(part, L.S, T, E, router_bias, logits, sm_count(), st);
   return cuda_status(e);
 }
@@ -334,7 +336,8 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
 
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
   if (e == cudaSuccess)
-    e = launch_router_logits(pb->dtype, x, W_router, router_bias, g.T, g.H, g.E, L.S, part, st);
+    e = launch_router_logits(pb->dtype, x, W_router, router_bias, g.T, g.H, g.E, L.S, part,
+                             status, g.limit_ns, st);
   if (e == cudaSuccess)
     e = launch_route(part, L.S, router_bias, g.T, g.E, g.k, pb->renorm,
                      L.S > 1 ? logits : nullptr, ids, w, st);

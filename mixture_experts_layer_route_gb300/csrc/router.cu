@@ -1,9 +1,11 @@
 // Router: logits (step a1) and top-k routing with gate weights (step a2).
 //
 // Logits: logits[t][e] = sum_h x[t][h] * Wr[e][h] (+ b[e]) with fp32
-// accumulation on the CUDA cores ("Gate" at the end of stage 2 of the
-// five-stage MoE layer in "Lower latency and higher throughput with multi-node
-// DeepSeek deployment"). When the tile grid alone cannot fill the GPU (decode:
+// accumulation ("Gate" at the end of stage 2 of the five-stage MoE layer in
+// "Lower latency and higher throughput with multi-node DeepSeek deployment").
+// bf16 layers compute it on the tensor cores (tcgen05, bf16 products are exact
+// in the fp32 accumulator); fp32 layers on the CUDA cores, since tf32 operands
+// would round x and Wr. When the tile grid alone cannot fill the GPU (decode:
 // T = 64), H is split into S slices whose partial sums are added later in
 // ascending slice order, so results do not depend on scheduling.
 //
@@ -12,6 +14,8 @@
 // softmax gate weights over the chosen k (renorm) or over all E ("MoE Router"
 // section of the same page: top-k indices and scores per token).
 #include <cmath>
+#include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -297,6 +301,204 @@ __global__ void __launch_bounds__(256, 1) router_logits_big_kernel(
   }
 }
 
+// ---------------------------------------------------------------- tensor cores
+// bf16 logits on tcgen05: one CTA per (128-token tile, expert tile of up to 256,
+// slice of H). A = 128 token rows of x, B = n_tile expert rows of Wr, both
+// K-major in 128-byte swizzled stages loaded by TMA; the 128 x n_tile fp32
+// accumulator lives in TMEM (lane = token, column = expert). Token and expert
+// tails read as zeros (TMA out-of-bounds fill) and are not stored.
+constexpr int RC_BM = 128;          // tokens per tile (MMA M)
+constexpr int RC_BK = 64;           // K per stage: one 128-byte row of bf16
+constexpr int RC_MAX_N = 256;       // experts per tile (MMA N limit)
+constexpr int RC_MAX_STAGES = 8;
+constexpr int RC_RING_BYTES = 200 * 1024;
+
+struct RouterTcArgs {
+  CUtensorMap tmX;  // x [T][H], box 64 x 128 rows
+  CUtensorMap tmW;  // Wr [E][H], box 64 x n_tile rows
+  const float* bias;
+  float* out;  // [S][T][E]
+  int* status;
+  unsigned long long limit_ns;
+  int T, E, H, k_len, n_tile, stages, tmem_cols;
+};
+
+int rc_n_tile(int E) { return E >= RC_MAX_N ? RC_MAX_N : (E + 15) / 16 * 16; }
+int rc_stage_bytes(int n_tile) { return RC_BM * 128 + n_tile * 128; }
+int rc_stages(int n_tile) {
+  const int s = RC_RING_BYTES / rc_stage_bytes(n_tile);
+  return s > RC_MAX_STAGES ? RC_MAX_STAGES : s;
+}
+size_t rc_smem_bytes(int n_tile) {
+  return 1024 /* alignment slack */ + (size_t)rc_stages(n_tile) * rc_stage_bytes(n_tile) +
+         (2 * RC_MAX_STAGES + 1) * 8 + 16;
+}
+
+__global__ void __launch_bounds__(128, 1)
+    router_logits_tc_kernel(const __grid_constant__ RouterTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int N = a.n_tile, ST = a.stages;
+  const uint32_t A_BYTES = RC_BM * 128, STAGE = A_BYTES + (uint32_t)N * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)ST * STAGE);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * RC_MAX_STAGES + 1);
+  auto full_bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto empty_bar = [&](int i) { return smem_u32(&bars[RC_MAX_STAGES + i]); };
+  const uint32_t done_bar = smem_u32(&bars[2 * RC_MAX_STAGES]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * RC_BM, e0 = blockIdx.y * N, slice = blockIdx.z;
+  const int kbeg = slice * a.k_len;
+  const int kend = min(a.H, kbeg + a.k_len);
+  const int nk = (kend - kbeg) / RC_BK;  // H and k_len are multiples of RC_BK
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    mbar_init(done_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&a.tmX);
+    tma_prefetch_desc(&a.tmW);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), (uint32_t)a.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    const uint64_t pol = l2_policy_evict_normal();
+    int issued = 0;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % ST;
+      const uint32_t round = (uint32_t)(kb / ST);
+      if (!mbar_wait(empty_bar(s), (round & 1u) ^ 1u, a.status, a.limit_ns)) break;
+      const uint32_t dst = smem_u32(smem + (size_t)s * STAGE);
+      mbar_arrive_expect_tx(full_bar(s), STAGE);
+      tma_load_2d(dst, &a.tmX, kbeg + kb * RC_BK, t0, full_bar(s), pol);
+      tma_load_2d(dst + A_BYTES, &a.tmW, kbeg + kb * RC_BK, e0, full_bar(s), pol);
+      ++issued;
+    }
+    // Let the last loads land before the CTA can exit (bounded, status ignored).
+    const int n_last = issued < ST ? issued : ST;
+    for (int i = issued - n_last; i < issued; ++i)
+      mbar_wait(full_bar(i % ST), (uint32_t)(i / ST) & 1u, nullptr, 20000000ull);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = umma_idesc(1u, RC_BM, (uint32_t)N);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % ST;
+      const uint32_t round = (uint32_t)(kb / ST);
+      if (!mbar_wait(full_bar(s), round & 1u, a.status, a.limit_ns)) break;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(smem + (size_t)s * STAGE);
+      const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < RC_BK / 16; ++kk)
+        umma_issue<false>(tmem, umma_desc_sw128(a_addr + kk * 32),
+                          umma_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+      umma_commit(empty_bar(s));
+    }
+    // Arrives once every MMA issued above has completed (also after a timeout).
+    umma_commit(done_bar);
+  }
+  __syncwarp();
+
+  // -------------------------------------------------------------- epilogue
+  // Warp w reads TMEM lanes 32w..32w+31 (tokens); 32 expert columns per load.
+  bool ok = mbar_wait(done_bar, 0, a.status, a.limit_ns) && read_status(a.status) == MOE_OK;
+  ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+  if (ok) {
+    tc_fence_after();
+    const int t = t0 + warp * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    float* orow = a.out + ((size_t)slice * a.T + (size_t)(t < a.T ? t : 0)) * a.E;
+    const float* bias = (a.bias != nullptr && gridDim.z == 1) ? a.bias : nullptr;
+    const bool vec = (a.E & 3) == 0;
+    for (int c0 = 0; c0 < N; c0 += 32) {
+      float v[32];
+      tmem_ld32(taddr + (uint32_t)c0, v);
+      const int eb = e0 + c0;
+      if (t < a.T) {
+        if (vec && eb + 32 <= a.E) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 o = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            if (bias) {
+              o.x += bias[eb + i];
+              o.y += bias[eb + i + 1];
+              o.z += bias[eb + i + 2];
+              o.w += bias[eb + i + 3];
+            }
+            *reinterpret_cast<float4*>(orow + eb + i) = o;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (eb + i < a.E) orow[eb + i] = bias ? v[i] + bias[eb + i] : v[i];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
+  }
+}
+
+cudaError_t launch_router_logits_tc(const void* x, const void* Wr, const float* bias, int T,
+                                    int H, int E, int S, int k_len, float* out, int* status,
+                                    unsigned long long limit_ns, cudaStream_t st) {
+  RouterTcArgs a;
+  memset(&a, 0, sizeof(a));
+  const int n_tile = rc_n_tile(E);
+  if (!make_tma_map(&a.tmX, x, MOE_DTYPE_BF16, (uint64_t)T, (uint64_t)H, RC_BM) ||
+      !make_tma_map(&a.tmW, Wr, MOE_DTYPE_BF16, (uint64_t)E, (uint64_t)H, (uint32_t)n_tile))
+    return cudaErrorInvalidValue;
+  a.bias = bias;
+  a.out = out;
+  a.status = status;
+  a.limit_ns = limit_ns;
+  a.T = T;
+  a.E = E;
+  a.H = H;
+  a.k_len = k_len;
+  a.n_tile = n_tile;
+  a.stages = rc_stages(n_tile);
+  int cols = 32;
+  while (cols < n_tile) cols *= 2;
+  a.tmem_cols = cols;
+  const size_t smem = rc_smem_bytes(n_tile);
+  // Opt in once per device for the largest ring (any n_tile fits under it).
+  static std::mutex mu;
+  static bool opted[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64 || !opted[dev]) {
+      e = cudaFuncSetAttribute(router_logits_tc_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(RC_RING_BYTES + 4096));
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) opted[dev] = true;
+    }
+  }
+  dim3 grid((unsigned)((T + RC_BM - 1) / RC_BM), (unsigned)((E + n_tile - 1) / n_tile),
+            (unsigned)S);
+  router_logits_tc_kernel<<<grid, 128, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 // Sum of S partial logits in ascending slice order, then the bias: identical
 // arithmetic in the reduction kernel and in the route kernel.
 // The loads of each batch of 8 slices are issued together (they are
@@ -423,21 +625,38 @@ constexpr int64_t kRouterBigT = 1024;
 
 int64_t router_split_request(int64_t T, int64_t H, int64_t E, int num_sms);
 
-// Slice length for S slices of H: a multiple of the K step (32).
-int64_t router_slice_len(int64_t H, int64_t S) {
+// K step of each router kernel: slices of H are multiples of it.
+int64_t router_k_step(int dtype) { return dtype == MOE_DTYPE_BF16 ? RC_BK : RT_BK; }
+
+// Slice length for S slices of H: a multiple of the K step.
+int64_t router_slice_len(int dtype, int64_t H, int64_t S) {
+  const int64_t step = router_k_step(dtype);
   const int64_t k_len = (H + S - 1) / S;
-  return (k_len + RT_BK - 1) / RT_BK * RT_BK;
+  return (k_len + step - 1) / step * step;
 }
 
 // Slices actually produced by S requested slices (rounding the slice length
 // up can leave fewer).
-int64_t router_effective_slices(int64_t H, int64_t S) {
-  const int64_t k_len = router_slice_len(H, S);
+int64_t router_effective_slices(int dtype, int64_t H, int64_t S) {
+  const int64_t k_len = router_slice_len(dtype, H, S);
   return (H + k_len - 1) / k_len;
 }
 
-int router_split_count(int64_t T, int64_t H, int64_t E, int num_sms) {
-  return (int)router_effective_slices(H, router_split_request(T, H, E, num_sms));
+// Tensor-core split: as many slices as fill one wave of one CTA per SM, each
+// at least two stages (128) of H long.
+int64_t router_tc_split_request(int64_t T, int64_t H, int64_t E, int num_sms) {
+  const int64_t n_tile = rc_n_tile((int)E);
+  const int64_t tiles = ((T + RC_BM - 1) / RC_BM) * ((E + n_tile - 1) / n_tile);
+  if (tiles <= 0) return 1;
+  const int64_t smax = H / (2 * RC_BK) < 1 ? 1 : H / (2 * RC_BK);
+  const int64_t S = num_sms / tiles;
+  return S < 1 ? 1 : (S > smax ? smax : S);
+}
+
+int router_split_count(int dtype, int64_t T, int64_t H, int64_t E, int num_sms) {
+  const int64_t req = dtype == MOE_DTYPE_BF16 ? router_tc_split_request(T, H, E, num_sms)
+                                              : router_split_request(T, H, E, num_sms);
+  return (int)router_effective_slices(dtype, H, req);
 }
 
 int64_t router_split_request(int64_t T, int64_t H, int64_t E, int num_sms) {
@@ -468,11 +687,14 @@ int64_t router_split_request(int64_t T, int64_t H, int64_t E, int num_sms) {
 }
 
 cudaError_t launch_router_logits(int dtype, const void* x, const void* Wr, const float* bias,
-                                 int T, int H, int E, int S, float* out_partials,
-                                 cudaStream_t st) {
+                                 int T, int H, int E, int S, float* out_partials, int* status,
+                                 unsigned long long limit_ns, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  const int k_len = (int)router_slice_len(H, S);
-  if (router_effective_slices(H, S) != S) return cudaErrorInvalidValue;
+  const int k_len = (int)router_slice_len(dtype, H, S);
+  if (router_effective_slices(dtype, H, S) != S) return cudaErrorInvalidValue;
+  if (dtype == MOE_DTYPE_BF16)
+    return launch_router_logits_tc(x, Wr, bias, T, H, E, S, k_len, out_partials, status,
+                                   limit_ns, st);
   if (T >= kRouterBigT) {
     dim3 grid((E + RL_BN - 1) / RL_BN, (T + RL_BM - 1) / RL_BM, S);
     cudaError_t e;

@@ -83,6 +83,8 @@ def finish(ws):
     (448, 4096, 192, "bf16", False),
     # the 128 x 128 kernel with token and expert tails, both dtypes
     (1500, 1024, 200, "bf16", True), (1100, 512, 72, "f32", False), (8192, 4096, 128, "bf16", False),
+    # tensor-core path: a 16-expert tile; four expert tiles with a tail
+    (64, 512, 8, "bf16", True), (130, 1024, 1000, "bf16", False),
 ])
 def test_router_logits(oracle, T, H, E, dtype, bias):
     cfg = MoEConfig("l", T=T, H=H, E=E, k=1, I=64, dtype=dtype, zipf_s=1.1 if bias else 0.0)
