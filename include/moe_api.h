@@ -67,11 +67,11 @@ typedef enum {
 
 typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
 
-/* Token-tile choice of the grouped GEMMs. AUTO chooses per expert, on the GPU,
- * from that expert's row count: 32-token tiles up to 32 rows, 128-token tiles
- * up to 128 rows, 256-token tiles beyond; a batch of T <= 64 tokens uses
- * 32-token tiles throughout. DECODE, MEDIUM and PREFILL force the 32-, 128- or
- * 256-token tile for every expert. */
+/* Token-tile choice of the grouped GEMMs. AUTO: a batch of T <= 64 tokens
+ * uses 32-token tiles (its rows gathered inside the GEMM's loads); larger
+ * batches use tiles of up to 256 tokens on pairs of SMs, all experts in one
+ * launch, heaviest first, each tile loading only as many token rows as it
+ * holds. DECODE, MEDIUM and PREFILL force 32-, 128- or 256-token tiles. */
 typedef enum {
   MOE_TILE_AUTO = 0,
   MOE_TILE_DECODE = 1,

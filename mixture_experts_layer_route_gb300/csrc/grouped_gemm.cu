@@ -1,18 +1,16 @@
 // Host side of the grouped GEMMs: TMA tensor maps, kernel variants, launch.
 //
-// Three variants (token tile BN x pipeline depth), for bf16 (kind::f16) and fp32
-// inputs (kind::tf32); with the automatic tile choice each expert is handled
-// by the variant its own row count calls for (all three may run in one call):
-//   32-token tiles,  9 stages, experts with <= 32 rows (every expert of a batch
-//     of <= 64 tokens): the weight stream dominates, so the ring is deep
-//     (9 x 16 KB of weights in flight); gated tokens by TMA gather4.
-//   128-token tiles, 6 stages, 33..128 rows: still weight-stream heavy, with
-//     6 x 16 KB of weights in flight and one token box per stage.
-//   256-token tiles, 4 stages, > 128 rows: tensor-core bound, 128 x 256 tiles.
-// 128- and 256-token gated tiles read the routed token rows from their
-// expert-ordered copy, one TMA box per stage; the down projection always
-// loads its h rows that way. CTA pairs share each token tile (multicast) when
-// every group has an even number of feature blocks.
+// One launch per GEMM, for bf16 (kind::f16) and fp32 inputs (kind::tf32):
+//   decode-sized batches (T <= 64, or MOE_TILE_DECODE): 32-token tiles, 9
+//     stages of 16 KB of weights; the gated GEMM gathers its token rows with
+//     TMA gather4, so no expert-ordered copy of x is made;
+//   otherwise: token tiles of up to 256 rows on CTA pairs (cta_group::2
+//     MMAs, M = 256, 6 stages of 32 KB per SM; MOE_TILE_MEDIUM: 128 rows, 8
+//     stages of 24 KB), every
+//     expert in the same launch, heaviest experts first; the gated GEMM reads
+//     the routed rows from their expert-ordered copy and each tile loads the
+//     smallest token box (128, 64 or 16 rows per CTA) that covers it. Groups
+//     with an odd number of feature blocks fall back to single-CTA tiles.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -62,13 +60,8 @@ bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, ui
 namespace {
 
 constexpr int kMaxExperts = 1024;  // the C ABI's limit on E
-// Automatic tile choice by the rows m of each group: 32-token tiles for
-// m <= kLightMax, 128-token tiles up to kMediumMax, 256-token tiles beyond
-// (thresholds measured on the Qwen3-, Zipf- and DeepSeek-shaped layers). A batch of
-// at most kSmallBatch tokens uses 32-token tiles throughout, so it runs one launch
-// per GEMM and needs no expert-ordered copy of its rows.
-constexpr int kLightMax = 32;
-constexpr int kMediumMax = 128;
+// A batch of at most kSmallBatch tokens runs the 32-token gather4 kernel: its
+// experts hold a few rows each, and its rows need no expert-ordered copy.
 constexpr int kSmallBatch = 64;
 
 struct AttrCache {
@@ -140,51 +133,58 @@ cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t 
   return cudaGetLastError();
 }
 
-// Upper bound of the tile count of one variant: groups with rows in [m_lo, m_hi].
-size_t tile_upper_bound(int T, int k, int E, int BN, int routed_blocks, int shared_blocks,
-                        int m_lo, int m_hi) {
+// Upper bound of the unit count of one launch: T*k routed rows in at most
+// min(E, T*k) groups of ceil(m / tile_n) token tiles each, plus the shared
+// expert's T rows.
+size_t unit_upper_bound(int T, int k, int E, int tile_n, int routed_blocks, int shared_blocks) {
   const size_t slots = (size_t)T * k;
-  size_t groups = slots / (size_t)(m_lo < 1 ? 1 : m_lo);
-  if (groups > (size_t)E) groups = (size_t)E;
-  const size_t shared = (shared_blocks > 0 && T >= m_lo && T <= m_hi) ? 1 : 0;
-  return (slots / BN + groups) * (size_t)routed_blocks +
-         shared * (size_t)((T + BN - 1) / BN) * shared_blocks;
+  const size_t groups = slots < (size_t)E ? slots : (size_t)E;
+  return (slots / tile_n + groups) * (size_t)routed_blocks +
+         (size_t)((T + tile_n - 1) / tile_n) * shared_blocks;
 }
 
-struct Range {
-  int lo, hi;
-};
+// One launch per GEMM: the 32-token gather4 kernel for decode-sized batches
+// (or when forced), otherwise the tiled kernel with token tiles of tile_n rows.
+bool use_decode_kernel(const GemmProblem& p) {
+  return p.tile == MOE_TILE_DECODE || (p.tile == MOE_TILE_AUTO && p.T <= kSmallBatch);
+}
 
-// Row ranges of the three variants under the automatic choice, or the whole
-// range for an explicit tile. Variants whose range cannot be met (every group
-// has at most T rows) are not launched.
-void variant_ranges(const GemmProblem& p, Range r[3]) {
-  const int big = 1 << 30;
-  r[0] = r[1] = r[2] = Range{1, 0};  // empty
-  switch (p.tile) {
-    case MOE_TILE_DECODE: r[0] = Range{1, big}; break;
-    case MOE_TILE_MEDIUM: r[1] = Range{1, big}; break;
-    case MOE_TILE_PREFILL: r[2] = Range{1, big}; break;
-    default:
-      if (p.T <= kSmallBatch) {
-        r[0] = Range{1, big};
-        break;
-      }
-      r[0] = Range{1, kLightMax};
-      r[1] = Range{kLightMax + 1, kMediumMax};
-      if (p.T > kMediumMax) r[2] = Range{kMediumMax + 1, big};
-  }
+// Token tile of the tiled kernel: 256 (6 stages of 32 KB per SM), or 128 (8
+// stages of 24 KB) when forced. 128-token tiles measured slower on every
+// layer shape: a 256 x 128 pair MMA step is fed at ~94 B/clk per SM, and an
+// expert of 129..256 rows then streams its weights to the SMs twice.
+int tiled_tile_n(const GemmProblem& p) { return p.tile == MOE_TILE_MEDIUM ? 128 : 256; }
+
+// Tensor maps of a tiled token operand [rows][cols]: boxes of b_rows, box1 and
+// 16 rows (GemmCfg::B_ROWS, BOX1).
+bool make_b_maps(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
+                 uint32_t b_rows, uint32_t box1) {
+  return make_tma_map(&m[0], base, dtype, rows, cols, b_rows) &&
+         make_tma_map(&m[1], base, dtype, rows, cols, box1) &&
+         make_tma_map(&m[2], base, dtype, rows, cols, 16);
+}
+
+void fill_common(GroupedGemmArgs& a, const GemmProblem& p, const int32_t* offsets,
+                 const int32_t* gather_idx, int* status, int tile_n) {
+  a.offsets = offsets;
+  a.gather_idx = gather_idx;
+  a.status = status;
+  a.limit_ns = p.limit_ns;
+  a.T = p.T;
+  a.k = p.k;
+  a.E = p.E;
+  a.KP = p.k + (p.Is > 0 ? 1 : 0);
+  a.flags = p.flags;
+  a.m_lo = 1;
+  a.m_hi = 1 << 30;
+  a.tile_n = tile_n;
 }
 
 }  // namespace
 
 bool tensor_map_encoder_available() { return encoder() != nullptr; }
 
-bool gemm_needs_expert_order_copy(const GemmProblem& p) {
-  Range r[3];
-  variant_ranges(p, r);
-  return r[1].lo <= r[1].hi || r[2].lo <= r[2].hi;
-}
+bool gemm_needs_expert_order_copy(const GemmProblem& p) { return !use_decode_kernel(p); }
 
 cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* xg,
                                const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
@@ -192,83 +192,59 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
                                int* status, cudaStream_t st) {
   const bool has_s = p.Is > 0;
   const bool bf16 = p.dtype == MOE_DTYPE_BF16;
-  // CTA pairs share each token tile when every group has an even number of
-  // 64-row feature blocks.
-  const bool pair = (p.I / 64) % 2 == 0 && (!has_s || (p.Is / 64) % 2 == 0);
-  Range r[3];
-  variant_ranges(p, r);
-  const int rb = p.I / 64, sb = has_s ? p.Is / 64 : 0;
-  for (int v = 0; v < 3; ++v) {
-    if (r[v].lo > r[v].hi) continue;
-    const int bn = v == 0 ? 32 : (v == 1 ? 128 : 256);
-    const bool cl2 = v > 0 && pair;
-    GroupedGemmArgs a;
-    memset(&a, 0, sizeof(a));
-    bool ok = make_tma_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
-              make_tma_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64);
-    if (ok && has_s)
-      ok = make_tma_map(&a.tmA[2], Wsg, p.dtype, p.Is, p.H, 64) &&
-           make_tma_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64);
-    if (ok) {
-      if (v == 0) {
-        ok = make_tma_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
-        a.tmB[1] = a.tmB[0];
-      } else {  // [0]: routed rows in expert order; [1]: x itself for the shared expert
-        if (!xg) return cudaErrorInvalidValue;
-        const uint32_t box = cl2 ? bn / 2 : bn;
-        ok = make_tma_map(&a.tmB[0], xg, p.dtype, (uint64_t)p.T * p.k, p.H, box) &&
-             make_tma_map(&a.tmB[1], x, p.dtype, p.T, p.H, box);
-      }
+  const bool dec = use_decode_kernel(p);
+  // CTA pairs when every group has an even number of 64-row feature blocks.
+  const bool pair = !dec && (p.I / 64) % 2 == 0 && (!has_s || (p.Is / 64) % 2 == 0);
+  const int tile_n = dec ? 32 : tiled_tile_n(p);
+  GroupedGemmArgs a;
+  memset(&a, 0, sizeof(a));
+  bool ok = make_tma_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
+            make_tma_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64);
+  if (ok && has_s)
+    ok = make_tma_map(&a.tmA[2], Wsg, p.dtype, p.Is, p.H, 64) &&
+         make_tma_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64);
+  if (ok) {
+    if (dec) {
+      ok = make_tma_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
+    } else {  // [0..2]: routed rows in expert order; [3..5]: x itself for the shared expert
+      if (!xg) return cudaErrorInvalidValue;
+      const uint32_t br = pair ? tile_n / 2 : 256, b1 = br / 2;
+      ok = make_b_maps(&a.tmB[0], xg, p.dtype, (uint64_t)p.T * p.k, p.H, br, b1) &&
+           make_b_maps(&a.tmB[3], x, p.dtype, p.T, p.H, br, b1);
     }
-    if (!ok) return cudaErrorInvalidValue;
-    if (!has_s) {
-      a.tmA[2] = a.tmA[0];
-      a.tmA[3] = a.tmA[1];
-    }
-    a.offsets = offsets;
-    a.gather_idx = gather_idx;
-    a.topk_w = nullptr;
-    a.out = h;
-    a.out_shared = hs;
-    a.status = status;
-    a.limit_ns = p.limit_ns;
-    a.T = p.T;
-    a.k = p.k;
-    a.E = p.E;
-    a.KP = p.k + (has_s ? 1 : 0);
-    a.n_out_routed = p.I;
-    a.n_out_shared = has_s ? p.Is : 64;
-    a.kdim_routed = p.H;
-    a.kdim_shared = p.H;
-    a.ld_out_routed = p.I;
-    a.ld_out_shared = has_s ? p.Is : 0;
-    a.flags = p.flags;
-    a.m_lo = r[v].lo;
-    a.m_hi = r[v].hi;
-    size_t ub = tile_upper_bound(p.T, p.k, p.E, bn, rb, sb, r[v].lo, r[v].hi);
-    cudaError_t e;
-    if (v == 0)
-      e = bf16 ? launch_variant<__nv_bfloat16, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st)
-               : launch_variant<float, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st);
-    else if (v == 1)
-      e = cl2 ? (bf16 ? launch_variant<__nv_bfloat16, true, 128, 6, kTiled, 2>(a, p.num_sms, p.E,
-                                                                              (ub + 1) / 2, st)
-                      : launch_variant<float, true, 128, 6, kTiled, 2>(a, p.num_sms, p.E,
-                                                                      (ub + 1) / 2, st))
-              : (bf16 ? launch_variant<__nv_bfloat16, true, 128, 6, kTiled>(a, p.num_sms, p.E, ub,
-                                                                           st)
-                      : launch_variant<float, true, 128, 6, kTiled>(a, p.num_sms, p.E, ub, st));
-    else
-      e = cl2 ? (bf16 ? launch_variant<__nv_bfloat16, true, 256, 4, kTiled, 2>(a, p.num_sms, p.E,
-                                                                              (ub + 1) / 2, st)
-                      : launch_variant<float, true, 256, 4, kTiled, 2>(a, p.num_sms, p.E,
-                                                                      (ub + 1) / 2, st))
-              : (bf16 ? launch_variant<__nv_bfloat16, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub,
-                                                                           st)
-                      : launch_variant<float, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st));
-    if (e != cudaSuccess) return e;
   }
-  return cudaSuccess;
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_s) {
+    a.tmA[2] = a.tmA[0];
+    a.tmA[3] = a.tmA[1];
+  }
+  fill_common(a, p, offsets, gather_idx, status, tile_n);
+  a.topk_w = nullptr;
+  a.out = h;
+  a.out_shared = hs;
+  a.n_out_routed = p.I;
+  a.n_out_shared = has_s ? p.Is : 64;
+  a.kdim_routed = p.H;
+  a.kdim_shared = p.H;
+  a.ld_out_routed = p.I;
+  a.ld_out_shared = has_s ? p.Is : 0;
+  const int rb = p.I / 64, sb = has_s ? p.Is / 64 : 0;
+  const size_t ub = unit_upper_bound(p.T, p.k, p.E, tile_n, rb, sb);
+  if (dec)
+    return bf16 ? launch_variant<__nv_bfloat16, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st)
+                : launch_variant<float, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st);
+  if (pair && tile_n == 128)
+    return bf16 ? launch_variant<__nv_bfloat16, true, 128, 8, kTiled, 2>(a, p.num_sms, p.E,
+                                                                        (ub + 1) / 2, st)
+                : launch_variant<float, true, 128, 8, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2,
+                                                                st);
+  if (pair)
+    return bf16 ? launch_variant<__nv_bfloat16, true, 256, 6, kTiled, 2>(a, p.num_sms, p.E,
+                                                                        (ub + 1) / 2, st)
+                : launch_variant<float, true, 256, 6, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2,
+                                                                st);
+  return bf16 ? launch_variant<__nv_bfloat16, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st)
+              : launch_variant<float, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
 }
 
 cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
@@ -277,73 +253,52 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
                              int* status, cudaStream_t st) {
   const bool has_s = p.Is > 0;
   const bool bf16 = p.dtype == MOE_DTYPE_BF16;
-  const bool pair = (p.H / 128) % 2 == 0;
-  Range r[3];
-  variant_ranges(p, r);
-  const int rb = p.H / 128, sb = has_s ? p.H / 128 : 0;
-  for (int v = 0; v < 3; ++v) {
-    if (r[v].lo > r[v].hi) continue;
-    const int bn = v == 0 ? 32 : (v == 1 ? 128 : 256);
-    const bool cl2 = v > 0 && pair;
-    const uint32_t box = cl2 ? bn / 2 : bn;  // token box = token tile, or half for CTA pairs
-    GroupedGemmArgs a;
-    memset(&a, 0, sizeof(a));
-    bool ok = make_tma_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
-              make_tma_map(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, box);
-    if (ok && has_s)
-      ok = make_tma_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128) &&
-           make_tma_map(&a.tmB[1], hs, p.dtype, p.T, p.Is, box);
-    if (!ok) return cudaErrorInvalidValue;
-    if (!has_s) {
-      a.tmA[2] = a.tmA[0];
-      a.tmB[1] = a.tmB[0];
-    }
-    a.tmA[1] = a.tmA[0];
-    a.tmA[3] = a.tmA[2];
-    a.offsets = offsets;
-    a.gather_idx = gather_idx;
-    a.topk_w = topk_w;
-    a.out = Y;
-    a.out_shared = nullptr;
-    a.status = status;
-    a.limit_ns = p.limit_ns;
-    a.T = p.T;
-    a.k = p.k;
-    a.E = p.E;
-    a.KP = p.k + (has_s ? 1 : 0);
-    a.n_out_routed = p.H;
-    a.n_out_shared = p.H;
-    a.kdim_routed = p.I;
-    a.kdim_shared = has_s ? p.Is : p.I;
-    a.ld_out_routed = p.H;
-    a.ld_out_shared = p.H;
-    a.flags = p.flags;
-    a.m_lo = r[v].lo;
-    a.m_hi = r[v].hi;
-    size_t ub = tile_upper_bound(p.T, p.k, p.E, bn, rb, sb, r[v].lo, r[v].hi);
-    cudaError_t e;
-    if (v == 0)
-      e = bf16 ? launch_variant<__nv_bfloat16, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st)
-               : launch_variant<float, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st);
-    else if (v == 1)
-      e = cl2 ? (bf16 ? launch_variant<__nv_bfloat16, false, 128, 6, kTiled, 2>(
-                            a, p.num_sms, p.E, (ub + 1) / 2, st)
-                      : launch_variant<float, false, 128, 6, kTiled, 2>(a, p.num_sms, p.E,
-                                                                       (ub + 1) / 2, st))
-              : (bf16 ? launch_variant<__nv_bfloat16, false, 128, 6, kTiled>(a, p.num_sms, p.E,
-                                                                            ub, st)
-                      : launch_variant<float, false, 128, 6, kTiled>(a, p.num_sms, p.E, ub, st));
-    else
-      e = cl2 ? (bf16 ? launch_variant<__nv_bfloat16, false, 256, 4, kTiled, 2>(
-                            a, p.num_sms, p.E, (ub + 1) / 2, st)
-                      : launch_variant<float, false, 256, 4, kTiled, 2>(a, p.num_sms, p.E,
-                                                                       (ub + 1) / 2, st))
-              : (bf16 ? launch_variant<__nv_bfloat16, false, 256, 4, kTiled>(a, p.num_sms, p.E,
-                                                                            ub, st)
-                      : launch_variant<float, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st));
-    if (e != cudaSuccess) return e;
+  const bool dec = use_decode_kernel(p);
+  const bool pair = !dec && (p.H / 128) % 2 == 0;
+  const int tile_n = dec ? 32 : tiled_tile_n(p);
+  // Token boxes: B_ROWS and BOX1 of the variant launched (decode: 32 and 16).
+  const uint32_t br = dec ? 32 : (pair ? tile_n / 2 : 256), b1 = br / 2 < 16 ? 16 : br / 2;
+  GroupedGemmArgs a;
+  memset(&a, 0, sizeof(a));
+  bool ok = make_tma_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
+            make_b_maps(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, br, b1);
+  if (ok && has_s)
+    ok = make_tma_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128) &&
+         make_b_maps(&a.tmB[3], hs, p.dtype, p.T, p.Is, br, b1);
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_s) {
+    a.tmA[2] = a.tmA[0];
+    for (int i = 0; i < 3; ++i) a.tmB[3 + i] = a.tmB[i];
   }
-  return cudaSuccess;
+  a.tmA[1] = a.tmA[0];
+  a.tmA[3] = a.tmA[2];
+  fill_common(a, p, offsets, gather_idx, status, tile_n);
+  a.topk_w = topk_w;
+  a.out = Y;
+  a.out_shared = nullptr;
+  a.n_out_routed = p.H;
+  a.n_out_shared = p.H;
+  a.kdim_routed = p.I;
+  a.kdim_shared = has_s ? p.Is : p.I;
+  a.ld_out_routed = p.H;
+  a.ld_out_shared = p.H;
+  const int rb = p.H / 128, sb = has_s ? p.H / 128 : 0;
+  const size_t ub = unit_upper_bound(p.T, p.k, p.E, tile_n, rb, sb);
+  if (dec)
+    return bf16 ? launch_variant<__nv_bfloat16, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st)
+                : launch_variant<float, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st);
+  if (pair && tile_n == 128)
+    return bf16 ? launch_variant<__nv_bfloat16, false, 128, 8, kTiled, 2>(a, p.num_sms, p.E,
+                                                                         (ub + 1) / 2, st)
+                : launch_variant<float, false, 128, 8, kTiled, 2>(a, p.num_sms, p.E,
+                                                                 (ub + 1) / 2, st);
+  if (pair)
+    return bf16 ? launch_variant<__nv_bfloat16, false, 256, 6, kTiled, 2>(a, p.num_sms, p.E,
+                                                                         (ub + 1) / 2, st)
+                : launch_variant<float, false, 256, 6, kTiled, 2>(a, p.num_sms, p.E,
+                                                                 (ub + 1) / 2, st);
+  return bf16 ? launch_variant<__nv_bfloat16, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st)
+              : launch_variant<float, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
 }
 
 }  // namespace moe

@@ -30,23 +30,29 @@
 // Token-operand loading (B), one of two modes:
 //  kGather4 (32-token gated tiles): TMA tile::gather4, 4 rows per instruction
 //    straight from x by token index (8 instructions per stage).
-//  kTiled (down projection, and 128/256-token gated tiles once the routed
-//    token rows were copied into expert order): the tile's rows are
-//    contiguous, one TMA box per stage. An SM accepts one TMA instruction only
+//  kTiled (down projection, and larger gated tiles once the routed token rows
+//    were copied into expert order): the tile's rows are contiguous, one TMA
+//    box per stage, the smallest of three heights that covers the tile. An SM accepts one TMA instruction only
 //    every ~70-150 cycles, so a 256-token stage cannot be filled 4 rows at a
 //    time; one box carries it.
 // All TMA loads of a stage are issued in one SIMT step with per-lane operands.
 //
-// Row-range filter: a launch only schedules the groups whose row count lies in
-// [m_lo, m_hi]; the host launches one variant (token tile 32, 128 or 256) per
-// range, so each expert gets the tile its own load calls for.
+// Schedule: every CTA derives the same list of units (group, feature block,
+// token tile) from the offsets: the groups with rows in [m_lo, m_hi], heaviest
+// first, each cut into token tiles of tile_n rows. Units are dealt round-robin
+// to the persistent CTAs (or CTA pairs).
 //
-// Clusters (CL = 2, prefill-sized tiled variants): the two CTAs of a cluster
-// take adjacent feature blocks of the same group and token tile. Each loads its
-// own weight rows and half of the token box, multicast into both CTAs, so the
-// token tile crosses L2 once per pair; MMA completions are committed to the
-// empty barriers of both CTAs, so a stage is refilled only when both are done
-// with it.
+// CTA pairs (CL = 2, the 128- and 256-token variants): one tcgen05.mma with
+// cta_group::2 spans the tensor cores of the cluster's two SMs, M = 256, N =
+// the token tile. The two CTAs take adjacent feature blocks of the same group
+// and token tile: each loads its own 128 weight rows (A) and one half of the
+// token columns (B), so every SM stores and reads half of the token tile per
+// stage instead of all of it (the shared-memory fill rate, ~90 B/clk/SM, is
+// what limits a single-SM 128 x 256 tile). The leader (rank 0) waits for both
+// CTAs' loads on its own full barriers, issues the MMAs, and commits their
+// completion to both CTAs' empty and accumulator barriers; each CTA's epilogue
+// reads its half of D from its own tensor memory and both release the
+// accumulator on the leader's barrier.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread) and
 // TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each).
@@ -63,8 +69,11 @@ struct GroupedGemmArgs {
   // GATED: [0] routed gate, [1] routed up, [2] shared gate, [3] shared up (64-row box).
   // DOWN:  [0] routed down, [2] shared down (128-row box).
   CUtensorMap tmA[4];
-  // GATED: [0] x (1-row box, gather4). DOWN: [0] h, [1] h_shared (32-row box).
-  CUtensorMap tmB[2];
+  // Token operand. gather4 (GATED, 32-token tiles): [0] x, 1-row box.
+  // Tiled: [0..2] routed rows (expert-ordered copy of x, or h), [3..5] the
+  // shared expert's rows (x, or h_shared), with boxes of B_ROWS, B_ROWS / 2
+  // and 16 rows; each tile loads the smallest box that covers its columns.
+  CUtensorMap tmB[6];
   const int32_t* offsets;     // [E+2]
   const int32_t* gather_idx;  // [T*k]
   const float* topk_w;        // [T*k] (DOWN)
@@ -78,6 +87,7 @@ struct GroupedGemmArgs {
   int ld_out_routed, ld_out_shared; // row stride (elements) of out / out_shared
   unsigned flags;
   int m_lo, m_hi;             // groups with m_lo <= rows <= m_hi are scheduled
+  int tile_n;                 // token tile (<= BN): a group of m rows has ceil(m / tile_n)
 };
 
 enum BMode : int { kGather4 = 0, kTiled = 2 };
@@ -88,22 +98,29 @@ struct GemmCfg {
   static constexpr int WM = GATED ? 64 : 128;        // output features per tile
   static constexpr int BK = 128 / (int)sizeof(TIn);  // K per stage (one 128-byte row)
   static constexpr int UMMA_K = 32 / (int)sizeof(TIn);  // K per instruction (32 bytes)
-  static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int A_BYTES = BM * 128;             // per CTA
+  static constexpr int B_ROWS = BN / CL;                 // token rows per CTA
+  static constexpr int B_BYTES = B_ROWS * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
   static constexpr int THREADS = 192;
-  static_assert(CL == 1 || (CL == 2 && BMODE == kTiled), "clusters share tiled token boxes");
+  static_assert(CL == 1 || (CL == 2 && BMODE == kTiled && BN >= 64),
+                "CTA pairs split tiled token boxes of >= 64 rows");
+  // Pair MMAs round N up to 32 (each CTA's half a multiple of 16 rows).
+  static constexpr int N_ROUND = CL == 2 ? 32 : 16;
   static constexpr bool TF32 = sizeof(TIn) == 4;
   static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
                     TMEM_COLS == 512,
                 "TMEM allocation must be a power of two in [32, 512]");
   static_assert(BN % 32 == 0 && BN <= 256, "token tile");
 
+  // Heights of the three tiled token boxes (rows per CTA).
+  static constexpr int BOX1 = B_ROWS / 2 < 16 ? 16 : B_ROWS / 2;
+
   static size_t smem_bytes(int E) {
     return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES + EPI_FLOATS * 4 +
-           (2 * STAGES + 5) * 8 + 16 + 2 * (size_t)(E + 2) * 4;
+           (2 * STAGES + 5) * 8 + 16 + 3 * (size_t)(E + 2) * 4;
   }
 };
 
@@ -115,24 +132,27 @@ struct Tile {
   int n_valid;  // rows of this tile
 };
 
-template <int BN, int WM>
-__device__ __forceinline__ Tile decode_tile(int u, const int32_t* prefix, const int32_t* offs,
-                                            int G) {
-  int lo = 0, hi = G;
+// Unit u of the schedule: the scheduled groups are listed in `order` (heaviest
+// first), `prefix[i]` = units of order[0..i); a group's units run feature block
+// by feature block, token tile fastest, so consecutive units share weights.
+__device__ __forceinline__ Tile decode_tile(int u, const int32_t* prefix, const int32_t* order,
+                                            const int32_t* offs, int ngroups, int tile_n) {
+  int lo = 0, hi = ngroups;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (prefix[mid] <= u) lo = mid;
     else hi = mid;
   }
   Tile t;
-  t.g = lo;
-  const int m = offs[lo + 1] - offs[lo];
-  const int mtiles = (m + BN - 1) / BN;
+  const int g = order[lo];
+  t.g = g;
+  const int m = offs[g + 1] - offs[g];
+  const int mtiles = (m + tile_n - 1) / tile_n;
   const int local = u - prefix[lo];
   t.nb = local / mtiles;
   t.mt = local - t.nb * mtiles;
-  t.p0 = offs[lo] + t.mt * BN;
-  t.n_valid = min(BN, m - t.mt * BN);
+  t.p0 = offs[g] + t.mt * tile_n;
+  t.n_valid = min(tile_n, m - t.mt * tile_n);
   return t;
 }
 
@@ -142,6 +162,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>;
   static_assert(GATED || BMODE == kTiled, "the down projection reads contiguous h rows");
   static_assert(BMODE != kGather4 || BN <= 128, "gather4 is for decode-sized token tiles");
+  constexpr bool PAIR = CL == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -151,14 +172,17 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* epi_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* n_sched = reinterpret_cast<int*>(tmem_holder + 2);
   int32_t* prefix = reinterpret_cast<int32_t*>(tmem_holder + 4);
   int32_t* offs = prefix + (args.E + 2);
+  int32_t* order = offs + (args.E + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E, G = E + 1;
-  // Units are walked per cluster; CTA `crank` of a cluster takes feature block
+  // Units are walked per cluster; CTA `crank` of a pair takes feature block
   // 2 * nb + crank of each pair unit.
-  const int crank = CL == 2 ? (int)cluster_ctarank() : 0;
+  const int crank = PAIR ? (int)cluster_ctarank() : 0;
+  const bool leader = crank == 0;
   const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
@@ -169,32 +193,85 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CL);
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 1);
+      mbar_init(tempty_bar(a), CL);  // a pair's leader hears both epilogues
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmA[i]);
-    for (int i = 0; i < 2; ++i) tma_prefetch_desc(&args.tmB[i]);
+    for (int i = 0; i < 6; ++i) tma_prefetch_desc(&args.tmB[i]);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+    else
+      tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+  }
   if (warp == 2) {
-    // Tiles per group: ceil(m_g / BN) x (features_g / WM); exclusive prefix.
+    // Schedule: the groups with rows in [m_lo, m_hi], heaviest class first
+    // (> 256, > 128, > 32, the rest; group order within a class), so that the
+    // long tensor-bound units start first and short weight-streaming units
+    // fill the tail. Each group has ceil(m / tile_n) x (features / (WM * CL))
+    // units. Every CTA derives the same schedule from the offsets.
+    const int tn = args.tile_n;
     for (int i = lane; i < G + 1; i += 32) offs[i] = args.offsets[i];
     __syncwarp();
-    const int per = (G + 31) / 32;
-    const int g0 = lane * per;
-    int local = 0;
-    for (int g = g0; g < min(G, g0 + per); ++g) {
+    auto klass = [&](int g) {
+      const int m = offs[g + 1] - offs[g];
+      if (m < args.m_lo || m > args.m_hi || m <= 0) return -1;
+      return m > 256 ? 0 : (m > 128 ? 1 : (m > 32 ? 2 : 3));
+    };
+    auto units = [&](int g) {
       const int m = offs[g + 1] - offs[g];
       const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / (C::WM * CL);
-      if (m >= args.m_lo && m <= args.m_hi) local += ((m + BN - 1) / BN) * nf;
+      return ((m + tn - 1) / tn) * nf;
+    };
+    const int per = (G + 31) / 32;
+    const int g0 = lane * per, g1 = min(G, g0 + per);
+    // Per-lane class counts, then a warp scan per class (registers only).
+    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+    for (int g = g0; g < g1; ++g) {
+      const int c = klass(g);
+      c0 += c == 0;
+      c1 += c == 1;
+      c2 += c == 2;
+      c3 += c == 3;
     }
+    auto excl_scan = [&](int v, int& total) {
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int w = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += w;
+      }
+      total = __shfl_sync(0xffffffffu, incl, 31);
+      return incl - v;
+    };
+    int t0, t1, t2, t3;
+    int p0 = excl_scan(c0, t0), p1 = excl_scan(c1, t1), p2 = excl_scan(c2, t2),
+        p3 = excl_scan(c3, t3);
+    p1 += t0;
+    p2 += t0 + t1;
+    p3 += t0 + t1 + t2;
+    const int base = t0 + t1 + t2 + t3;
+    for (int g = g0; g < g1; ++g) {
+      const int c = klass(g);
+      if (c == 0) order[p0++] = g;
+      else if (c == 1) order[p1++] = g;
+      else if (c == 2) order[p2++] = g;
+      else if (c == 3) order[p3++] = g;
+    }
+    const int ng = base;
+    __syncwarp();
+    const int per2 = (ng + 31) / 32;
+    const int i0 = lane * per2, i1 = min(ng, i0 + per2);
+    int local = 0;
+    for (int i = i0; i < i1; ++i) local += units(order[i]);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -202,32 +279,36 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       if (lane >= o) incl += v;
     }
     int run = incl - local;
-    for (int g = g0; g < min(G, g0 + per); ++g) {
-      prefix[g] = run;
-      const int m = offs[g + 1] - offs[g];
-      const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / (C::WM * CL);
-      if (m >= args.m_lo && m <= args.m_hi) run += ((m + BN - 1) / BN) * nf;
+    for (int i = i0; i < i1; ++i) {
+      prefix[i] = run;
+      run += units(order[i]);
     }
-    if (lane == 31) prefix[G] = incl;
+    if (lane == 31) {
+      prefix[ng] = incl;
+      *n_sched = ng;
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CL > 1) cluster_sync();  // peers' barriers exist before any multicast
+  if constexpr (PAIR) cluster_sync();  // peers' barriers and TMEM exist before any use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int total = prefix[G];
+  const int ngroups = *n_sched;
+  const int total = prefix[ngroups];
   const uint64_t limit = args.limit_ns;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Decode-sized tiles read each weight tile once: stream it past L2.
+    // Decode-sized tiles read each weight tile once: stream it past L2. (With
+    // larger tiles evict_first measured slower: the 256-byte L2 promotion
+    // fetches the next k-block's half line, which must survive until used.)
     const uint64_t pol_w = (BN <= 64) ? l2_policy_evict_first() : l2_policy_evict_normal();
     const uint64_t pol_t = l2_policy_evict_last();
     uint32_t it = 0;
     bool ok = true;
     bool skip_once = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
     for (int u = cid; u < total && ok; u += ncl) {
-      Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      Tile tl = decode_tile(u, prefix, order, offs, ngroups, args.tile_n);
       tl.nb = tl.nb * CL + crank;
       const bool shared = tl.g == E;
       const int kdim = shared ? args.kdim_shared : args.kdim_routed;
@@ -238,7 +319,16 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       constexpr int NQ = (BMODE == kGather4) ? (BN / 4 + 31) / 32 : 1;
       int rows[NQ][4];
       int n4 = 0;
-      uint32_t tx = C::A_BYTES;
+      // Tiled token box: with a pair, the MMA's N columns are split in halves;
+      // the peer's half starts at column n_mma / 2 of the tile. Each CTA loads
+      // the smallest of its three boxes that covers its n_mma / CL rows.
+      const int n_mma = (tl.n_valid + C::N_ROUND - 1) / C::N_ROUND * C::N_ROUND;
+      const int need = n_mma / CL;
+      const int bsel = need <= 16 ? 2 : (need <= C::BOX1 ? 1 : 0);
+      const int box_rows = bsel == 2 ? 16 : (bsel == 1 ? C::BOX1 : C::B_ROWS);
+      // Bytes this stage's full barrier waits for: with a pair, the leader's
+      // barrier counts both CTAs' loads.
+      uint32_t tx = CL * (C::A_BYTES + box_rows * 128);
       if constexpr (BMODE == kGather4) {
         n4 = (tl.n_valid + 3) / 4;
 #pragma unroll
@@ -252,11 +342,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
                                   : 0;
           }
         }
-        tx += n4 * 4 * 128;
-      } else if constexpr (BMODE == kTiled) {
-        tx += BN * 128;  // one box of BN rows; rows past the segment are loaded, unused
+        tx = C::A_BYTES + n4 * 4 * 128;
       }
-      const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
+      const int b_row0 = (shared ? tl.p0 - offs[E] : tl.p0) + crank * (n_mma / 2);
       // Per-lane operands of this tile's TMA loads (one SIMT step per stage):
       // GATED: lanes 0, 1 = gate, up rows (+ lane 2 = token rows when tiled);
       // DOWN: lane 0 = W_down rows, lane 1 = h rows.
@@ -271,14 +359,13 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         my_off = 64 * 128;
       }
       if (BMODE == kTiled && lane == NA) {
-        // With a cluster, this CTA fetches rows [crank * BN/2, (crank + 1) * BN/2)
-        // of the token box for both CTAs.
-        my_map = &args.tmB[shared ? 1 : 0];
-        my_row = b_row0 + crank * (BN / CL);
-        my_off = C::A_BYTES + crank * (BN / CL) * 128;
+        my_map = &args.tmB[(shared ? 3 : 0) + bsel];
+        my_row = b_row0;
+        my_off = C::A_BYTES;
         my_pol = pol_t;
       }
-      for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
+      const int nkb = kdim / C::BK;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
         int wok = 1;
@@ -295,15 +382,16 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
           skip_once = false;
           continue;
         }
-        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
-        __syncwarp();
-        if constexpr (CL == 1) {
-          if (lane < NLOADS) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
+        if constexpr (PAIR) {
+          if (leader && lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
+          __syncwarp();
+          if (lane < NLOADS)
+            tma_load_2d_pair(a_dst + my_off, my_map, kx, my_row, mapa_shared(full_bar(s), 0),
+                             my_pol);
         } else {
-          if (lane < NA) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
-          if (lane == NA)
-            tma_load_2d_multicast(a_dst + my_off, my_map, kx, my_row, full_bar(s), 0x3,
-                                  my_pol);
+          if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
+          __syncwarp();
+          if (lane < NLOADS) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
         }
         if constexpr (BMODE == kGather4) {
 #pragma unroll
@@ -317,7 +405,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       }
     }
     // Let the last loads land before the CTA can exit (bounded, status ignored).
-    if (lane == 0) {
+    // A pair's loads all complete on the leader's barriers; the leader drains
+    // them, and neither CTA leaves before the closing cluster barrier.
+    if (lane == 0 && leader) {
       const uint32_t n_last = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
       for (uint32_t i = it - n_last; i < it; ++i) {
         const uint32_t s = i % STAGES, round = i / STAGES;
@@ -327,20 +417,19 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t it = 0, lt = 0;
       constexpr uint32_t fmt = C::TF32 ? 2u : 1u;
       bool ok = true;
       for (int u = cid; u < total && ok; u += ncl, ++lt) {
-        Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
-      tl.nb = tl.nb * CL + crank;
+        Tile tl = decode_tile(u, prefix, order, offs, ngroups, args.tile_n);
         const int kdim = (tl.g == E) ? args.kdim_shared : args.kdim_routed;
         const uint32_t acc = lt & 1u, around = lt >> 1;
         if (!mbar_wait(tempty_bar(acc), (around & 1u) ^ 1u, args.status, limit)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        int n_mma = (tl.n_valid + 15) & ~15;
-        const uint32_t idesc = umma_idesc(fmt, 128, (uint32_t)n_mma);
+        const int n_mma = (tl.n_valid + C::N_ROUND - 1) / C::N_ROUND * C::N_ROUND;
+        const uint32_t idesc = umma_idesc(fmt, C::BM * CL, (uint32_t)n_mma);
         for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
@@ -353,20 +442,30 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
           const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-            umma_issue<C::TF32>(d_tmem, umma_desc_sw128(a_addr + kk * 32),
-                                umma_desc_sw128(b_addr + kk * 32), idesc,
-                                (kb | kk) != 0 ? 1u : 0u);
+            const uint64_t ad = umma_desc_sw128(a_addr + kk * 32);
+            const uint64_t bd = umma_desc_sw128(b_addr + kk * 32);
+            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            if constexpr (PAIR)
+              umma_issue_pair<C::TF32>(d_tmem, ad, bd, idesc, accum);
+            else
+              umma_issue<C::TF32>(d_tmem, ad, bd, idesc, accum);
           }
-          if constexpr (CL == 1)
-            umma_commit(empty_bar(s));
+          if constexpr (PAIR)
+            umma_commit_pair_multicast(empty_bar(s), 0x3);
           else
-            umma_commit_multicast(empty_bar(s), 0x3);
+            umma_commit(empty_bar(s));
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
+        if constexpr (PAIR)
+          umma_commit_pair_multicast(tfull_bar(acc), 0x3);
+        else
+          umma_commit(tfull_bar(acc));
       }
       // All issued MMAs finished before TMEM is released (bounded, status ignored).
-      umma_commit(drain_bar);
+      if constexpr (PAIR)
+        umma_commit_pair(drain_bar);
+      else
+        umma_commit(drain_bar);
       mbar_wait(drain_bar, 0, nullptr, 20000000ull);
     }
     __syncwarp();
@@ -377,7 +476,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t lt = 0;
     for (int u = cid; u < total; u += ncl, ++lt) {
-      Tile tl = decode_tile<BN, C::WM>(u, prefix, offs, G);
+      Tile tl = decode_tile(u, prefix, order, offs, ngroups, args.tile_n);
       tl.nb = tl.nb * CL + crank;
       const bool shared = tl.g == E;
       const uint32_t acc = lt & 1u, around = lt >> 1;
@@ -465,18 +564,29 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         tc_fence_before();
         named_barrier_sync(1, 128);
       }
-      if (et == 0) mbar_arrive(tempty_bar(acc));
+      if (et == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+        else
+          mbar_arrive(tempty_bar(acc));
+      }
     }
   }
 
+  // Teardown: every MMA has completed (the leader drained them) and every
+  // epilogue read of TMEM is done before either CTA of a pair frees its half.
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  // No CTA leaves while its peer may still multicast into it or commit to it.
-  if constexpr (CL > 1) cluster_sync();
 }
 
 }  // namespace moe
