@@ -103,6 +103,8 @@ struct GemmCfg {
   static constexpr int B_BYTES = B_ROWS * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  // Epilogue staging: GATED, the 128 x 32 accumulator chunk (gate and up rows
+  // meet in one thread); DOWN, per-token row index and gate weight.
   static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
   static constexpr int THREADS = 192;
   static_assert(CL == 1 || (CL == 2 && BMODE == kTiled && BN >= 64),
@@ -548,18 +550,36 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
           named_barrier_sync(1, 128);
         }
       } else {
+        // Thread = output feature c (its TMEM lane); for each token column a
+        // warp stores 32 consecutive floats of that token's slot row. The
+        // epilogue warps share their schedulers with the producer and MMA
+        // warps, so the per-column work is kept to one multiply and one store:
+        // row indices and weights come four columns per shared-memory load.
         float* Y = reinterpret_cast<float*>(args.out);
-        const int32_t* yrow = reinterpret_cast<const int32_t*>(epi);
-        const float* wt = epi + BN;
-        const int H = args.n_out_routed;  // == n_out_shared for DOWN
-        const int c = tl.nb * 128 + q * 32 + lane;
+        const int4* yrow4 = reinterpret_cast<const int4*>(epi);
+        const float4* wt4 = reinterpret_cast<const float4*>(epi + BN);
+        const size_t H = (size_t)args.n_out_routed;  // == n_out_shared for DOWN
+        float* Yc = Y + tl.nb * 128 + q * 32 + lane;
         for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
           float v[32];
           tmem_ld32(t_acc + c0, v);
           const int nj = min(32, tl.n_valid - c0);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nj) Y[(size_t)yrow[c0 + i] * H + c] = wt[c0 + i] * v[i];
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const int4 r = yrow4[(c0 >> 2) + i4];
+            const float4 wv = wt4[(c0 >> 2) + i4];
+            const int i = 4 * i4;
+            if (i + 3 < nj) {
+              Yc[(size_t)r.x * H] = wv.x * v[i];
+              Yc[(size_t)r.y * H] = wv.y * v[i + 1];
+              Yc[(size_t)r.z * H] = wv.z * v[i + 2];
+              Yc[(size_t)r.w * H] = wv.w * v[i + 3];
+            } else {
+              if (i < nj) Yc[(size_t)r.x * H] = wv.x * v[i];
+              if (i + 1 < nj) Yc[(size_t)r.y * H] = wv.y * v[i + 1];
+              if (i + 2 < nj) Yc[(size_t)r.z * H] = wv.z * v[i + 2];
+            }
+          }
         }
         tc_fence_before();
         named_barrier_sync(1, 128);

@@ -595,7 +595,7 @@ __device__ __forceinline__ void route_warp(const float (&v)[NV], int E, int k, i
 }
 
 template <int NV>
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ src, int S,
+__global__ void __launch_bounds__(256, 2) route_kernel(const float* __restrict__ src, int S,
                                                     const float* __restrict__ bias, int T, int E,
                                                     int k, int renorm,
                                                     float* __restrict__ logits_out,
@@ -605,14 +605,48 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ sr
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   float v[NV];
+  const float* row = src + (size_t)t * E;
+  if (S == 1) {
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      v[i] = (S == 1) ? src[(size_t)t * E + e] : reduce_partials(src, S, T, E, t, e, bias);
-      if (S > 1 && logits_out) logits_out[(size_t)t * E + e] = v[i];
-    } else {
-      v[i] = -INFINITY;
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? row[e] : -INFINITY;
+    }
+  } else {
+    // Sum of the S partial slices in ascending slice order, then the bias (the
+    // arithmetic of reduce_partials). All loads of a batch of B slices, for
+    // all of the lane's experts, are issued before any of them is added.
+    constexpr int B = NV >= 32 ? 1 : 32 / NV;
+    const size_t stride = (size_t)T * E;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? row[e] : 0.f;
+    }
+    for (int s0 = 1; s0 < S; s0 += B) {
+      float q[NV][B];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+          q[i][j] = (e < E && s0 + j < S) ? row[(size_t)(s0 + j) * stride + e] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+#pragma unroll
+        for (int j = 0; j < B; ++j)
+          if (s0 + j < S) v[i] += q[i][j];
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        if (bias) v[i] += bias[e];
+        if (logits_out) logits_out[(size_t)t * E + e] = v[i];
+      } else {
+        v[i] = -INFINITY;
+      }
     }
   }
   route_warp<NV>(v, E, k, renorm, ids + (size_t)t * k, w + (size_t)t * k);
@@ -643,12 +677,16 @@ int64_t router_effective_slices(int dtype, int64_t H, int64_t S) {
 }
 
 // Tensor-core split: as many slices as fill one wave of one CTA per SM, each
-// at least two stages (128) of H long.
+// at least two stages (128) of H long, and at most kRouterMaxSlices: the route
+// kernel adds the slices, and more than a few of them cost it more latency
+// than they save here.
+constexpr int64_t kRouterMaxSlices = 8;
 int64_t router_tc_split_request(int64_t T, int64_t H, int64_t E, int num_sms) {
   const int64_t n_tile = rc_n_tile((int)E);
   const int64_t tiles = ((T + RC_BM - 1) / RC_BM) * ((E + n_tile - 1) / n_tile);
   if (tiles <= 0) return 1;
-  const int64_t smax = H / (2 * RC_BK) < 1 ? 1 : H / (2 * RC_BK);
+  int64_t smax = H / (2 * RC_BK) < 1 ? 1 : H / (2 * RC_BK);
+  if (smax > kRouterMaxSlices) smax = kRouterMaxSlices;
   const int64_t S = num_sms / tiles;
   return S < 1 ? 1 : (S > smax ? smax : S);
 }
