@@ -526,7 +526,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
             for (int f = 0; f < 16; ++f) {
               const float g = epi[(fg * 16 + f) * 33 + jj];
               const float up = epi[(64 + fg * 16 + f) * 33 + jj];
-              hv[f] = g / (1.0f + __expf(-g)) * up;
+              // silu(g) * up; approximate exp and divide (a few ulp of fp32,
+              // far below the bf16 rounding of h that follows).
+              hv[f] = __fdividef(g, 1.0f + __expf(-g)) * up;
             }
             TIn* dst = out + (size_t)(row0 + j) * ld + tl.nb * 64 + fg * 16;
             if constexpr (sizeof(TIn) == 2) {
