@@ -156,12 +156,10 @@ def roofline_numbers(cfg, counts):
 def kernels_per_step(cfg):
     """Kernels one moe_forward launches with the automatic tile choice: router
     logits, route, permute (one kernel up to 4096 slots, else count + scatter),
-    [the expert-ordered copy of the routed rows when 128/256-token tiles can
-    run], per GEMM one launch for each token tile a group's row count can call
-    for (32: always; 128: T > 64; 256: T > 128), combine."""
+    [the expert-ordered copy of the routed rows for batches of more than 64
+    tokens], one launch per GEMM, combine."""
     permute = 1 if cfg.T * cfg.k <= 4096 else 2
-    variants = 1 + (cfg.T > 64) + (cfg.T > 128)
-    return 2 + permute + (1 if cfg.T > 64 else 0) + 2 * variants + 1
+    return 2 + permute + (1 if cfg.T > 64 else 0) + 2 + 1
 
 
 def build_layer(cfg, device, seed=0):
@@ -283,6 +281,32 @@ def time_e2e(layer, d, steps, warmup, stream):
     return ms, nb, nb
 
 
+def time_graph(layer, d, steps, warmup, stream):
+    """The same forward pass captured once in a CUDA graph and replayed K times:
+    identical kernels and work, without the host launch path between them."""
+    x = d["x"]
+    T = x.shape[0]
+    y = torch.empty(T, layer.H, dtype=layer.dtype, device=x.device)
+    with torch.cuda.stream(stream):
+        layer.forward(x, out=y, stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        layer.forward(x, out=y)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1)
+
+
 def cpu_baseline(cfg, d, budget_s=10.0, max_tokens=None):
     """The CPU oracle, as it stands, on a bounded sample of tokens of the same
     layer: tokens/s over ~budget_s seconds of oracle work."""
@@ -380,9 +404,11 @@ def measure_config(cfg, args, world, local, with_clocks):
     per_stage, counts = time_stages(layer, d, steps, args.warmup, stream)
     e2e_ms, h2d, d2h = time_e2e(layer, d, steps, args.warmup, stream)
     e2e_ms = max_over_ranks(e2e_ms, world)
+    graph_ms = max_over_ranks(time_graph(layer, d, steps, args.warmup, stream), world)
     rl = roofline_numbers(cfg, counts.numpy())
     out = dict(cfg=cfg, steps=steps, ms_total=ms_total, per=per, per_stage=per_stage,
                counts=counts, rl=rl, clocks=clocks, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+               graph_ms=graph_ms,
                layer=layer, d=d)
     return out
 
@@ -431,6 +457,10 @@ def summarize(r, peaks, world, prefix_src):
         e2e={"value": world * cfg.T * steps / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
              "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
              "ms_per_step": r["e2e_ms"] / steps},
+        graph={"value": world * cfg.T * steps / (r["graph_ms"] / 1e3), "unit": "tokens/s",
+               "ms_per_step": r["graph_ms"] / steps,
+               "layer_roofline_frac": t_roof / (r["graph_ms"] / steps),
+               "how": "the same moe_forward captured once in a CUDA graph, replayed"},
     )
 
 
@@ -456,7 +486,7 @@ def run_native(args):
         prefill = {"config": {"workload": "qwen3_235b_prefill", "T": 8192, "H": 4096, "E": 128,
                               "k": 8, "I": 1536},
                    **{k: sp[k] for k in ("value", "ms_per_step", "roofline", "layer_roofline",
-                                         "stages_ms", "expert_load")}}
+                                         "stages_ms", "expert_load", "graph")}}
         del rp
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -479,7 +509,7 @@ def run_native(args):
         "median_ms": s["median_ms"], "p10_ms": s["p10_ms"], "p90_ms": s["p90_ms"],
         "roofline": s["roofline"], "layer_roofline": s["layer_roofline"],
         "stages_ms": s["stages_ms"], "expert_load": s["expert_load"],
-        "e2e": s["e2e"], "gpu_launches": kernels_per_step(cfg) * s["steps"],
+        "e2e": s["e2e"], "graph": s["graph"], "gpu_launches": kernels_per_step(cfg) * s["steps"],
         "clocks": clocks,
         "cpu_baseline": cpu, "prefill": prefill,
     }

@@ -98,6 +98,10 @@ typedef struct {
   uint32_t wait_limit_us; /* bound on every device-side wait; 0 = 1 s */
   int32_t out_f32;   /* nonzero: y is written as fp32 even when dtype is bf16 (the
                         sum of the slots before its one rounding to bf16) */
+  int32_t n_group;   /* <= 1: plain top-k routing. > 1: group-limited routing (see
+                        moe_route_grouped); E % n_group == 0, n_group <= 32 */
+  int32_t topk_group; /* groups kept per token when n_group > 1: 1 <= topk_group <=
+                         n_group and k <= topk_group * (E / n_group) */
 } moe_problem;
 
 /* Bytes of workspace every call below needs for problem `pb`. */
@@ -117,6 +121,19 @@ moe_status moe_router_logits(const moe_problem* pb, const void* x, const void* W
  * logits fp32 [T][E] -> topk_ids int32 [T][k], topk_w fp32 [T][k]. */
 moe_status moe_route(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
                      int32_t* topk_ids, float* topk_w, void* stream);
+
+/* Step a2, group-limited form (DeepSeek page, "MoE Router": the Mixtral router
+ * is the DeepSeek router whose top-K group is the group of all experts). The E
+ * experts form n_group contiguous groups of E / n_group. Per token: a group's
+ * score is its largest logit; the topk_group groups with the largest scores
+ * are kept (lower group index first among equals); then the k largest logits
+ * of the kept experts, as moe_route. Gate weights as moe_route, from the
+ * unmasked logits (renorm = 0: the softmax over all E). n_group <= 1 is
+ * moe_route. Requires E % n_group == 0, n_group <= 32, 1 <= topk_group <=
+ * n_group and k <= topk_group * (E / n_group); otherwise MOE_ERR_INVALID_ARG. */
+moe_status moe_route_grouped(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
+                             int64_t n_group, int64_t topk_group, int32_t* topk_ids,
+                             float* topk_w, void* stream);
 
 /* Step a3, permutation ("CuTeDSL at Perplexity", "Local" dispatch: count the
  * tokens of each expert, give every token a unique index in its expert's

@@ -15,7 +15,8 @@ from ._binding import (  # noqa: F401
     EXPORTED, MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_FLAG_TEST_SKIP_SIGNAL, MOE_OK,
     MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_MEDIUM, MOE_TILE_PREFILL, STATUS_NAMES, MoEError, MoEProblem,
     down_combine, down_combine_noalloc, forward, get_device_status, grouped_swiglu_gemm, load_library, make_problem,
-    permute, reset_device_status, route, router_logits, status_string, workspace_layout,
+    permute, reset_device_status, route, route_grouped, router_logits, status_string,
+    workspace_layout,
     workspace_size)
 
 
@@ -25,16 +26,20 @@ class MoELayer:
     Weights (torch CUDA tensors, contiguous, all of one dtype bf16 or fp32):
     W_router [E,H], W_gate/W_up [E,I,H], W_down [E,H,I], optional router_bias
     fp32 [E] and shared expert Ws_gate/Ws_up [Is,H], Ws_down [H,Is].
+    n_group > 1 limits each token's experts to its topk_group best groups of
+    E / n_group consecutive experts (moe_route_grouped).
     """
 
     def __init__(self, W_router, W_gate, W_up, W_down, k, router_bias=None, Ws_gate=None,
-                 Ws_up=None, Ws_down=None, renorm=1, tile=MOE_TILE_AUTO):
+                 Ws_up=None, Ws_down=None, renorm=1, tile=MOE_TILE_AUTO, n_group=1,
+                 topk_group=1):
         self.W_router, self.W_gate, self.W_up, self.W_down = W_router, W_gate, W_up, W_down
         self.router_bias = router_bias
         self.Ws_gate, self.Ws_up, self.Ws_down = Ws_gate, Ws_up, Ws_down
         self.E, self.I, self.H = W_gate.shape
         self.I_shared = 0 if Ws_gate is None else Ws_gate.shape[0]
         self.k, self.renorm, self.tile = k, renorm, tile
+        self.n_group, self.topk_group = n_group, topk_group
         self.dtype = W_gate.dtype
         self._ws = {}
 
@@ -42,7 +47,7 @@ class MoELayer:
                 out_f32: bool = False) -> MoEProblem:
         return make_problem(T, self.H, self.E, self.k, self.I, self.I_shared, self.renorm,
                             "bf16" if self.dtype == torch.bfloat16 else "f32", self.tile, flags,
-                            wait_limit_us, out_f32)
+                            wait_limit_us, out_f32, self.n_group, self.topk_group)
 
     def workspace(self, T: int) -> torch.Tensor:
         ws = self._ws.get(T)

@@ -23,7 +23,8 @@ MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_PREFILL, MOE_TILE_MEDIUM = 0, 1, 2, 3
 MOE_FLAG_TEST_SKIP_SIGNAL = 0x1
 
 # Every symbol include/moe_api.h declares.
-EXPORTED = ("moe_workspace_size", "moe_router_logits", "moe_route", "moe_permute",
+EXPORTED = ("moe_workspace_size", "moe_router_logits", "moe_route", "moe_route_grouped",
+            "moe_permute",
             "moe_grouped_swiglu_gemm", "moe_down_combine", "moe_forward",
             "moe_get_workspace_layout", "moe_get_device_status", "moe_reset_device_status",
             "moe_status_string", "moe_down_combine_noalloc")
@@ -40,7 +41,8 @@ class MoEProblem(ctypes.Structure):
                 ("k", ctypes.c_int64), ("I", ctypes.c_int64), ("I_shared", ctypes.c_int64),
                 ("renorm", ctypes.c_int32), ("dtype", ctypes.c_int32), ("tile", ctypes.c_int32),
                 ("flags", ctypes.c_uint32), ("wait_limit_us", ctypes.c_uint32),
-                ("out_f32", ctypes.c_int32)]
+                ("out_f32", ctypes.c_int32), ("n_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32)]
 
 
 class MoEWorkspaceLayout(ctypes.Structure):
@@ -70,6 +72,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_workspace_size": [pb, ctypes.POINTER(ctypes.c_size_t)],
             "moe_router_logits": [pb, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_route": [_P, _I64, _I64, _I64, ctypes.c_int, _P, _P, _P],
+            "moe_route_grouped": [_P, _I64, _I64, _I64, ctypes.c_int, _I64, _I64, _P, _P, _P],
             "moe_permute": [_P, _I64, _I64, _I64, ctypes.c_int, _P, _P, _P, _P, ctypes.c_size_t,
                             _P],
             "moe_grouped_swiglu_gemm": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -115,10 +118,11 @@ def _check(name: str, code: int):
 
 
 def make_problem(T, H, E, k, I, I_shared=0, renorm=1, dtype="bf16", tile=MOE_TILE_AUTO,
-                 flags=0, wait_limit_us=0, out_f32=False) -> MoEProblem:
+                 flags=0, wait_limit_us=0, out_f32=False, n_group=1,
+                 topk_group=1) -> MoEProblem:
     dt = MOE_DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else MOE_DTYPE_F32
     return MoEProblem(T, H, E, k, I, I_shared, renorm, dt, tile, flags, wait_limit_us,
-                      1 if out_f32 else 0)
+                      1 if out_f32 else 0, n_group, topk_group)
 
 
 def workspace_size(problem: MoEProblem) -> int:
@@ -145,6 +149,13 @@ def route(logits, k, renorm, topk_ids, topk_w, stream=None):
     T, E = logits.shape
     _check("moe_route", load_library().moe_route(_ptr(logits), T, E, k, int(renorm),
                                                  _ptr(topk_ids), _ptr(topk_w), _stream(stream)))
+
+
+def route_grouped(logits, k, renorm, n_group, topk_group, topk_ids, topk_w, stream=None):
+    T, E = logits.shape
+    _check("moe_route_grouped", load_library().moe_route_grouped(
+        _ptr(logits), T, E, k, int(renorm), int(n_group), int(topk_group), _ptr(topk_ids),
+        _ptr(topk_w), _stream(stream)))
 
 
 def permute(topk_ids, E, has_shared, expert_offsets, gather_idx, slot_pos, workspace,

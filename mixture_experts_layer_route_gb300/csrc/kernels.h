@@ -24,9 +24,11 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* Wr, const
                                  unsigned long long limit_ns, cudaStream_t st);
 cudaError_t launch_logits_reduce(const float* partials, int S, int T, int E, const float* bias,
                                  float* logits, int num_sms, cudaStream_t st);
+// n_group <= 1: plain top-k; else the top-k limited to the best topk_group of
+// n_group contiguous expert groups.
 cudaError_t launch_route(const float* src, int S, const float* bias, int T, int E, int k,
-                         int renorm, float* logits_out, int32_t* ids, float* w,
-                         cudaStream_t st);
+                         int renorm, int n_group, int topk_group, float* logits_out,
+                         int32_t* ids, float* w, cudaStream_t st);
 
 // Permutation (permute.cu).
 size_t permute_smem_bytes(int E);

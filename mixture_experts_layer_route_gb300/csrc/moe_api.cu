@@ -83,6 +83,14 @@ Layout layout_of(const moe_problem& p) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Group-limited routing parameters (n_group <= 1: plain top-k, always valid).
+bool groups_valid(int64_t E, int64_t k, int64_t n_group, int64_t topk_group) {
+  if (n_group <= 1) return true;
+  if (n_group > 32 || E % n_group != 0) return false;
+  if (topk_group < 1 || topk_group > n_group) return false;
+  return k <= topk_group * (E / n_group);
+}
+
 moe_status check_problem(const moe_problem* pb) {
   if (!pb) return MOE_ERR_INVALID_ARG;
   const moe_problem& p = *pb;
@@ -94,6 +102,7 @@ moe_status check_problem(const moe_problem* pb) {
   if (p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM) return MOE_ERR_INVALID_ARG;
   if (p.renorm != 0 && p.renorm != 1) return MOE_ERR_INVALID_ARG;
   if (p.out_f32 != 0 && p.out_f32 != 1) return MOE_ERR_INVALID_ARG;
+  if (!groups_valid(p.E, p.k, p.n_group, p.topk_group)) return MOE_ERR_INVALID_ARG;
   const int64_t lim = (int64_t)1 << 30;
   if (p.T * (p.k + 1) >= lim || p.H >= lim || p.I >= lim || p.E * p.I >= lim ||
       p.E * p.H >= lim)
@@ -209,7 +218,22 @@ moe_status moe_route(const float* logits, int64_t T, int64_t E, int64_t k, int r
   if (T == 0) return MOE_OK;
   if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_route(logits, 1, nullptr, (int)T, (int)E, (int)k, renorm, nullptr,
+  return cuda_status(launch_route(logits, 1, nullptr, (int)T, (int)E, (int)k, renorm, 1, 1,
+                                  nullptr, topk_ids, topk_w, (cudaStream_t)stream));
+}
+
+moe_status moe_route_grouped(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
+                             int64_t n_group, int64_t topk_group, int32_t* topk_ids,
+                             float* topk_w, void* stream) {
+  if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
+  if (renorm != 0 && renorm != 1) return MOE_ERR_INVALID_ARG;
+  if (!groups_valid(E, k, n_group, topk_group)) return MOE_ERR_INVALID_ARG;
+  if (T * E >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route(logits, 1, nullptr, (int)T, (int)E, (int)k, renorm,
+                                  n_group > 1 ? (int)n_group : 1, (int)topk_group, nullptr,
                                   topk_ids, topk_w, (cudaStream_t)stream));
 }
 
@@ -340,6 +364,7 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
                              status, g.limit_ns, st);
   if (e == cudaSuccess)
     e = launch_route(part, L.S, router_bias, g.T, g.E, g.k, pb->renorm,
+                     pb->n_group > 1 ? pb->n_group : 1, pb->topk_group,
                      L.S > 1 ? logits : nullptr, ids, w, st);
   if (e == cudaSuccess)
     e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status,

@@ -539,11 +539,55 @@ __global__ void logits_reduce_kernel(const float* __restrict__ part, int S, int 
 // Top-k and gate weights of one token by one warp. v[i] holds the logit of
 // expert lane + 32 i (-inf past E). k rounds of warp arg-max over the not yet
 // chosen values, ties to the lower expert index; lane r keeps round r.
+// Group-limited form (n_group > 1, the DeepSeek router of the same section, of
+// which plain top-k is the one-group case): the experts form n_group
+// contiguous groups of E / n_group; a group's score is its largest logit; only
+// the topk_group best groups (lower group index among equals) take part in the
+// k rounds. Gate weights use the unmasked logits.
 template <int NV>
 __device__ __forceinline__ void route_warp(const float (&v)[NV], int E, int k, int renorm,
+                                           int n_group, int topk_group,
                                            int32_t* __restrict__ ids_row,
                                            float* __restrict__ w_row) {
   const int lane = threadIdx.x & 31;
+  float vs[NV];  // selection values: v, or -inf outside the kept groups
+#pragma unroll
+  for (int i = 0; i < NV; ++i) vs[i] = v[i];
+  if (n_group > 1) {
+    const int G = E / n_group;
+    int grp[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) grp[i] = (lane + 32 * i) / G;  // >= n_group past E
+    float gscore = -INFINITY;  // lane j: score of group j
+    for (int j = 0; j < n_group; ++j) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (grp[i] == j) mx = fmaxf(mx, v[i]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (lane == j) gscore = mx;
+    }
+    uint32_t kept = 0;
+    for (int r = 0; r < topk_group; ++r) {
+      const bool cand = lane < n_group && !((kept >> lane) & 1u);
+      float bv = cand ? gscore : -INFINITY;
+      int bi = cand ? lane : 0x7fffffff;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      kept |= 1u << bi;
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (grp[i] >= n_group || !((kept >> grp[i]) & 1u)) vs[i] = -INFINITY;
+  }
   uint32_t taken = 0;
   float my_val = 0.f;
   int my_idx = 0;
@@ -554,8 +598,8 @@ __device__ __forceinline__ void route_warp(const float (&v)[NV], int E, int k, i
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       const bool free_ = !((taken >> i) & 1u) && e < E;
-      if (free_ && (v[i] > bv || bi == 0x7fffffff)) {  // ascending e: first max wins
-        bv = v[i];
+      if (free_ && (vs[i] > bv || bi == 0x7fffffff)) {  // ascending e: first max wins
+        bv = vs[i];
         bi = e;
       }
     }
@@ -597,7 +641,8 @@ __device__ __forceinline__ void route_warp(const float (&v)[NV], int E, int k, i
 template <int NV>
 __global__ void __launch_bounds__(256, 2) route_kernel(const float* __restrict__ src, int S,
                                                     const float* __restrict__ bias, int T, int E,
-                                                    int k, int renorm,
+                                                    int k, int renorm, int n_group,
+                                                    int topk_group,
                                                     float* __restrict__ logits_out,
                                                     int32_t* __restrict__ ids,
                                                     float* __restrict__ w) {
@@ -649,7 +694,7 @@ __global__ void __launch_bounds__(256, 2) route_kernel(const float* __restrict__
       }
     }
   }
-  route_warp<NV>(v, E, k, renorm, ids + (size_t)t * k, w + (size_t)t * k);
+  route_warp<NV>(v, E, k, renorm, n_group, topk_group, ids + (size_t)t * k, w + (size_t)t * k);
 }
 
 }  // namespace
@@ -775,15 +820,15 @@ cudaError_t launch_logits_reduce(const float* partials, int S, int T, int E, con
 }
 
 cudaError_t launch_route(const float* src, int S, const float* bias, int T, int E, int k,
-                         int renorm, float* logits_out, int32_t* ids, float* w,
-                         cudaStream_t st) {
+                         int renorm, int n_group, int topk_group, float* logits_out,
+                         int32_t* ids, float* w, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int warps = 8;
   const int blocks = (T + warps - 1) / warps;
   const int nv = (E + 31) / 32;
 #define MOE_ROUTE_CASE(NV)                                                                  \
-  route_kernel<NV><<<blocks, warps * 32, 0, st>>>(src, S, bias, T, E, k, renorm, logits_out, \
-                                                   ids, w)
+  route_kernel<NV><<<blocks, warps * 32, 0, st>>>(src, S, bias, T, E, k, renorm, n_group,   \
+                                                   topk_group, logits_out, ids, w)
   if (nv <= 1) MOE_ROUTE_CASE(1);
   else if (nv <= 2) MOE_ROUTE_CASE(2);
   else if (nv <= 4) MOE_ROUTE_CASE(4);

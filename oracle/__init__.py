@@ -40,6 +40,7 @@ def _declare(lib):
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_router_logits.argtypes = [_f, _f, _f, _L, _L, _L, _f]
     lib.oracle_route.argtypes = [_f, _L, _L, _L, ctypes.c_int, _i, _f]
+    lib.oracle_route_grouped.argtypes = [_f, _L, _L, _L, ctypes.c_int, _L, _L, _i, _f]
     lib.oracle_permute.argtypes = [_i, _L, _L, _L, ctypes.c_int, _i, _i, _i]
     lib.oracle_expert_h.argtypes = [_f, _i, _i, _f, _f, _L, _L, _L, _L, _L, _f, _f, _f, _L, _f]
     lib.oracle_down_combine.argtypes = [_f, _i, _i, _i, _f, _f, _L, _L, _L, _L, _L, _f, _f,
@@ -48,7 +49,8 @@ def _declare(lib):
                                        _f, _L, _f]
     lib.oracle_moe_forward.argtypes = [_f, _f, _f, _f, _f, _f, _f, _f, _f, _L, _L, _L, _L, _L,
                                        _L, ctypes.c_int, _f, _f, _i, _f]
-    for n in ("oracle_router_logits", "oracle_route", "oracle_permute", "oracle_expert_h",
+    for n in ("oracle_router_logits", "oracle_route", "oracle_route_grouped", "oracle_permute",
+              "oracle_expert_h",
               "oracle_down_combine", "oracle_ffn_combine", "oracle_moe_forward"):
         getattr(lib, n).restype = None
     return lib
@@ -100,6 +102,16 @@ class Oracle:
         w = np.empty((T, k), np.float32)
         self.lib.oracle_route(self._pf(logits), T, E, k, int(renorm), self._pi(ids),
                               self._pf(w))
+        return ids, w
+
+    def route_grouped(self, logits, k, renorm=1, n_group=1, topk_group=1):
+        """Top-k limited to the best topk_group of n_group contiguous expert
+        groups (group score: the group's largest logit)."""
+        T, E = logits.shape
+        ids = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float32)
+        self.lib.oracle_route_grouped(self._pf(logits), T, E, k, int(renorm), int(n_group),
+                                      int(topk_group), self._pi(ids), self._pf(w))
         return ids, w
 
     def permute(self, ids, E, has_shared=0):

@@ -11,7 +11,9 @@
 //      deployment", five-stage layer breakdown: the "Gate" ends stage 2).
 //   2. top-k on the logits, lowest expert index first among equals, then the
 //      softmax gate weights, renormalised over the k chosen experts
-//      (same page, section "MoE Router": top-K indices and scores).
+//      (same page, section "MoE Router": top-K indices and scores); optionally
+//      limited to the best topk_group of n_group expert groups (the same
+//      section's DeepSeek form of the router).
 //   3. a stable counting sort of the (token, rank) slots by expert: per-expert
 //      counts, offsets and a unique position for every slot ("CuTeDSL at
 //      Perplexity", section "Mixture-of-Experts Dispatch/Combine", "Local").
@@ -113,6 +115,62 @@ void oracle_route(const float* logits, int64_t T, int64_t E, int64_t k, int reno
       for (int64_t e = 0; e < E; ++e) {
         if (taken[e]) continue;
         if (best < 0 || l[e] > l[best]) best = e;  // strict '>' keeps the lower index
+      }
+      taken[best] = 1;
+      ids[t * k + r] = (int32_t)best;
+    }
+    const double m = (double)l[ids[t * k]];
+    double S = 0.0;
+    if (renorm) {
+      for (int64_t r = 0; r < k; ++r) S += std::exp((double)l[ids[t * k + r]] - m);
+    } else {
+      for (int64_t e = 0; e < E; ++e) S += std::exp((double)l[e] - m);
+    }
+    for (int64_t r = 0; r < k; ++r)
+      w[t * k + r] = (float)(std::exp((double)l[ids[t * k + r]] - m) / S);
+  }
+}
+
+// Step 2, group-limited form ("MoE Router" section of the DeepSeek page: the
+// Mixtral router is the DeepSeek router whose top-K group is the group of all
+// experts). The E experts form n_group contiguous groups of E / n_group. For
+// each token: a group's score is the largest logit in it; the topk_group
+// groups with the largest scores are kept (lower group index among equals);
+// then k rounds of "largest not yet chosen logit among the kept groups, lowest
+// index among equals". Weights as in oracle_route, from the unmasked logits
+// (renorm == 0: the softmax over all E). n_group <= 1 is oracle_route.
+void oracle_route_grouped(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
+                          int64_t n_group, int64_t topk_group, int32_t* ids, float* w) {
+  if (n_group <= 1) {
+    oracle_route(logits, T, E, k, renorm, ids, w);
+    return;
+  }
+  const int64_t G = E / n_group;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    const float* l = logits + t * E;
+    std::vector<float> score(n_group);
+    for (int64_t j = 0; j < n_group; ++j) {
+      float best = l[j * G];
+      for (int64_t e = j * G + 1; e < (j + 1) * G; ++e)
+        if (l[e] > best) best = l[e];
+      score[j] = best;
+    }
+    std::vector<char> kept(n_group, 0);
+    for (int64_t r = 0; r < topk_group; ++r) {
+      int64_t bj = -1;
+      for (int64_t j = 0; j < n_group; ++j) {
+        if (kept[j]) continue;
+        if (bj < 0 || score[j] > score[bj]) bj = j;  // strict '>' keeps the lower index
+      }
+      kept[bj] = 1;
+    }
+    std::vector<char> taken(E, 0);
+    for (int64_t r = 0; r < k; ++r) {
+      int64_t best = -1;
+      for (int64_t e = 0; e < E; ++e) {
+        if (taken[e] || !kept[e / G]) continue;
+        if (best < 0 || l[e] > l[best]) best = e;
       }
       taken[best] = 1;
       ids[t * k + r] = (int32_t)best;

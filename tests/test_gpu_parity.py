@@ -122,6 +122,38 @@ def test_route_bitexact(oracle, T, E, k, renorm, ties):
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=1e-6)
 
 
+@pytest.mark.parametrize("T,E,k,n_group,topk_group,renorm,ties", [
+    (64, 256, 8, 8, 4, 1, False), (100, 64, 6, 8, 3, 1, True), (50, 128, 8, 4, 2, 0, False),
+    (33, 512, 10, 16, 5, 1, True), (40, 32, 6, 32, 6, 1, False), (77, 12, 5, 3, 2, 1, True),
+    (20, 1024, 32, 32, 8, 1, False), (64, 16, 4, 2, 2, 1, True),
+])
+def test_route_grouped_bitexact(oracle, T, E, k, n_group, topk_group, renorm, ties):
+    """Group-limited top-k: ids bit-exact and weights within 1e-6 of the oracle
+    on the same fp32 logits (ties inside and across groups when `ties`)."""
+    g = np.random.default_rng(T * 11 + E + n_group)
+    if ties:
+        logits = g.integers(-2, 3, size=(T, E)).astype(np.float32)
+    else:
+        logits = (2.0 * g.standard_normal((T, E))).astype(np.float32)
+    lt = torch.from_numpy(logits).to(DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    m.route_grouped(lt, k, renorm, n_group, topk_group, ids, w)
+    torch.cuda.synchronize()
+    rid, rw = oracle.route_grouped(logits, k, renorm, n_group, topk_group)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=1e-6)
+
+
+def test_route_grouped_rejects_bad_groups():
+    lt = torch.zeros(4, 64, dtype=torch.float32, device=DEV)
+    ids = torch.empty(4, 8, dtype=torch.int32, device=DEV)
+    w = torch.empty(4, 8, dtype=torch.float32, device=DEV)
+    for n_group, topk_group in ((6, 2), (8, 0), (8, 9), (64, 7), (16, 1)):
+        with pytest.raises(m.MoEError):
+            m.route_grouped(lt, 8, 1, n_group, topk_group, ids, w)
+
+
 # ------------------------------------------------------------------ a3 permute
 
 def _ids_with_counts(counts, seed):
@@ -321,6 +353,35 @@ def test_forward_vs_oracle(oracle, cfg):
         assert_bf16_is_rounded(y, y32)
     else:
         assert torch.equal(y, y32)
+
+
+@pytest.mark.parametrize("T,dtype", [(300, "bf16"), (64, "bf16"), (130, "f32")])
+def test_forward_grouped_routing_vs_oracle(oracle, T, dtype):
+    """moe_forward with group-limited routing (8 groups, 3 kept) and a shared
+    expert: the ids and weights the forward pass stored equal the oracle's
+    group-limited route of the logits it stored, and y matches the oracle's
+    experts and combine on those ids and weights."""
+    cfg = MoEConfig("grouped", T=T, H=256, E=64, k=6, I=128, I_shared=128, dtype=dtype)
+    d = generate(cfg, seed=9, device=DEV)
+    layer = m.MoELayer(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k,
+                       Ws_gate=d["Ws_gate"], Ws_up=d["Ws_up"], Ws_down=d["Ws_down"],
+                       n_group=8, topk_group=3)
+    y32 = layer(d["x"], out_f32=True)
+    ws = layer.workspace(T)
+    finish(ws)
+    lay = m.workspace_layout(layer.problem(T))
+    E, k = cfg.E, cfg.k
+    logits = ws[lay["logits"]:lay["logits"] + T * E * 4].view(torch.float32).view(T, E)
+    gids = ws[lay["topk_ids"]:lay["topk_ids"] + T * k * 4].view(torch.int32).view(T, k)
+    gw = ws[lay["topk_w"]:lay["topk_w"] + T * k * 4].view(torch.float32).view(T, k)
+    rid, rw = oracle.route_grouped(logits.cpu().numpy(), k, 1, 8, 3)
+    np.testing.assert_array_equal(gids.cpu().numpy(), rid)
+    np.testing.assert_allclose(gw.cpu().numpy(), rw, rtol=0, atol=1e-6)
+    assert max(len(set(r.tolist())) for r in rid // 8) <= 3  # at most topk_group groups
+    n = {kk: to_np(v) for kk, v in d.items()}
+    ref = oracle.ffn_combine(n["x"], rid, rw, n["W_gate"], n["W_up"], n["W_down"], n["Ws_gate"],
+                             n["Ws_up"], n["Ws_down"])
+    assert_close(y32.cpu().numpy(), ref, "y")
 
 
 def test_forward_is_bitwise_reproducible():

@@ -113,6 +113,58 @@ def test_weights_k1_is_exactly_one(oracle):
     np.testing.assert_array_equal(ids[:, 0], np.argmax(logits, axis=1))
 
 
+# ------------------------------------------- group-limited top-k (a2, DeepSeek form)
+
+def _np_grouped_topk(logits, k, n_group, topk_group):
+    """Brute force in numpy: a group's score is its largest logit; the
+    topk_group best groups are kept (lower group index among equals); then a
+    stable sort of the negated logits of the kept experts."""
+    T, E = logits.shape
+    G = E // n_group
+    score = logits.reshape(T, n_group, G).max(axis=2)
+    order = np.argsort(-score, axis=1, kind="stable")[:, :topk_group]
+    keep = np.zeros((T, n_group), bool)
+    np.put_along_axis(keep, order, True, axis=1)
+    masked = np.where(np.repeat(keep, G, axis=1), logits, -np.inf)
+    return np.argsort(-masked, axis=1, kind="stable")[:, :k]
+
+
+@pytest.mark.parametrize("E,k,n_group,topk_group", [(16, 3, 4, 2), (64, 8, 8, 3), (256, 8, 8, 4),
+                                                    (12, 5, 3, 2), (32, 6, 16, 5)])
+def test_grouped_topk_matches_bruteforce(oracle, E, k, n_group, topk_group):
+    """Small integer logits give ties inside groups, between group scores and
+    across groups; ids and renormalised weights against the definition."""
+    from scipy.special import softmax
+    r = _rng(E + 7 * k + n_group)
+    logits = r.integers(-3, 4, size=(64, E)).astype(np.float32)
+    ids, w = oracle.route_grouped(logits, k, 1, n_group, topk_group)
+    np.testing.assert_array_equal(ids, _np_grouped_topk(logits, k, n_group, topk_group))
+    sel = np.take_along_axis(logits.astype(np.float64), ids, axis=1)
+    np.testing.assert_allclose(w, softmax(sel, axis=1), atol=1e-7, rtol=0)
+
+
+def test_grouped_topk_reduces_to_plain_topk(oracle):
+    """Keeping every group, or groups of one expert with topk_group = k, is the
+    plain top-k (the Mixtral case of the same router); renorm = 0 keeps the
+    full softmax."""
+    from scipy.special import softmax
+    logits = _rng(8).standard_normal((40, 32)).astype(np.float32)
+    plain = np.argsort(-logits, axis=1, kind="stable")[:, :6]
+    full = softmax(logits.astype(np.float64), axis=1)
+    for n_group, topk_group in ((2, 2), (8, 8), (32, 6)):
+        ids, w = oracle.route_grouped(logits, 6, 0, n_group, topk_group)
+        np.testing.assert_array_equal(ids, plain)
+        np.testing.assert_allclose(w, np.take_along_axis(full, ids, axis=1), atol=1e-7, rtol=0)
+
+
+def test_grouped_topk_stays_in_kept_groups(oracle):
+    logits = (3.0 * _rng(9).standard_normal((50, 64))).astype(np.float32)
+    ids, _ = oracle.route_grouped(logits, 8, 1, 8, 2)
+    groups = ids // 8
+    assert all(len(set(row.tolist())) <= 2 for row in groups)
+    np.testing.assert_array_equal(ids[:, 0], np.argmax(logits, axis=1))
+
+
 # ---------------------------------------------------------------- permute (a3)
 
 @pytest.mark.parametrize("T,E,k,shared", [(37, 8, 2, 0), (100, 16, 4, 1), (1, 4, 4, 0),

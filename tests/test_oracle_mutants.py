@@ -28,6 +28,9 @@ MUTANTS = {
     "permute_unstable": ("  for (int64_t s = 0; s < T * k; ++s) {\n    const int64_t e = ids[s];",
                          "  for (int64_t s = T * k - 1; s >= 0; --s) {\n    const int64_t e = ids[s];"),
     "logit_index_transposed": ("(double)Wr[e * H + c]", "(double)Wr[c * E + e]"),
+    "group_score_is_sum": ("if (l[e] > best) best = l[e];", "best += l[e];"),
+    "group_tie_break_to_higher_index": ("score[j] > score[bj]", "score[j] >= score[bj]"),
+    "group_mask_ignored": ("if (taken[e] || !kept[e / G]) continue;", "if (taken[e]) continue;"),
 }
 
 PIN_CALLS = [
@@ -46,6 +49,10 @@ PIN_CALLS = [
     lambda o: pins.test_token_permutation_equivariance(o),
     lambda o: pins.test_stages_compose_to_forward(o),
     lambda o: pins.test_closed_form_golden(o),
+    lambda o: pins.test_grouped_topk_matches_bruteforce(o, 16, 3, 4, 2),
+    lambda o: pins.test_grouped_topk_matches_bruteforce(o, 64, 8, 8, 3),
+    lambda o: pins.test_grouped_topk_reduces_to_plain_topk(o),
+    lambda o: pins.test_grouped_topk_stays_in_kept_groups(o),
 ]
 
 
