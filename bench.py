@@ -413,6 +413,53 @@ def measure_config(cfg, args, world, local, with_clocks):
     return out
 
 
+def measure_fp8(cfg, args, world, peaks):
+    """The same workload with E4M3 expert weights (moe_forward_fp8): weights
+    quantized once, K timed steps of the layer. Roofline: weight bytes are one
+    per element plus a 4-byte scale per row; the FP8 tensor peak is the
+    measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25 = 2)."""
+    import mixture_experts_layer_route_gb300 as m
+    stream = torch.cuda.Stream()
+    d = generate(cfg, seed=args.seed, device="cuda")
+    layer = m.MoELayerFP8(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k,
+                          router_bias=d["router_bias"], Ws_gate=d["Ws_gate"], Ws_up=d["Ws_up"],
+                          Ws_down=d["Ws_down"], renorm=cfg.renorm)
+    for n in ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down"):
+        d[n] = None  # only the E4M3 copies stay resident
+    torch.cuda.empty_cache()
+    ws = layer.workspace(cfg.T)
+    steps = args.steps if cfg.T <= 1024 else max(3, args.steps // 8)
+    barrier(world)
+    ms_total, per = time_forward(layer, d, steps, args.warmup, stream)
+    barrier(world)
+    ms_total = max_over_ranks(ms_total, world)
+    st = m.get_device_status(ws, stream)
+    if st != m.MOE_OK:
+        raise RuntimeError(f"device status {m.status_string(st)}")
+    lay = m.workspace_layout(layer.problem(cfg.T))
+    offs = ws[lay["expert_offsets"]:lay["expert_offsets"] + (cfg.E + 2) * 4].view(torch.int32)
+    counts = torch.diff(offs[:cfg.E + 1]).cpu().numpy()
+    T, H, E, k, I, Is = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.I_shared
+    touched = int((counts > 0).sum())
+    wbytes = touched * (3 * H * I + 4 * (2 * I + H)) + ((3 * H * Is + 4 * (2 * Is + H)) if Is else 0)
+    bytes_layer = wbytes + 2 * T * H * 2 + E * H * 2
+    flop_layer = 2.0 * T * k * 3 * H * I + 2.0 * T * 3 * H * Is
+    ms_step = ms_total / steps
+    t_mem = bytes_layer / (peaks["hbm_gbs"] * 1e9) * 1e3
+    p8 = 2.0 * peaks["bf16_tflops_sustained"]
+    t_tc = flop_layer / (p8 * 1e12) * 1e3
+    t_roof = max(t_mem, t_tc)
+    return {"value": world * T * steps / (ms_total / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms_step, "median_ms": statistics.median(per),
+            "weights": "E4M3, one power-of-two scale per row (moe_forward_fp8)",
+            "layer_roofline": {"t_roof_ms": t_roof, "bound": "hbm" if t_mem >= t_tc else "tensor",
+                               "frac": t_roof / ms_step, "bytes_touched": bytes_layer,
+                               "flop_routed": flop_layer, "fp8_peak_tflops": p8,
+                               "fp8_peak_source": "2 x measured bf16_tflops_sustained (nominal "
+                                                  "fp8/bf16 ratio)"},
+            "experts_touched": touched}
+
+
 def summarize(r, peaks, world, prefix_src):
     cfg = r["cfg"]
     steps = r["steps"]
@@ -488,6 +535,13 @@ def run_native(args):
                    **{k: sp[k] for k in ("value", "ms_per_step", "roofline", "layer_roofline",
                                          "stages_ms", "expert_load", "graph")}}
         del rp
+        if args.fp8:
+            torch.cuda.empty_cache()
+            prefill["fp8"] = measure_fp8(CONFIGS["qwen3_235b_prefill"], args, world, peaks)
+    fp8 = None
+    if args.fp8 and cfg.dtype == "bf16" and cfg.I % 128 == 0 and cfg.I_shared % 128 == 0:
+        torch.cuda.empty_cache()
+        fp8 = measure_fp8(cfg, args, world, peaks)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         torch.cuda.empty_cache()
@@ -509,7 +563,8 @@ def run_native(args):
         "median_ms": s["median_ms"], "p10_ms": s["p10_ms"], "p90_ms": s["p90_ms"],
         "roofline": s["roofline"], "layer_roofline": s["layer_roofline"],
         "stages_ms": s["stages_ms"], "expert_load": s["expert_load"],
-        "e2e": s["e2e"], "graph": s["graph"], "gpu_launches": kernels_per_step(cfg) * s["steps"],
+        "e2e": s["e2e"], "graph": s["graph"], "fp8": fp8,
+        "gpu_launches": kernels_per_step(cfg) * s["steps"],
         "clocks": clocks,
         "cpu_baseline": cpu, "prefill": prefill,
     }
@@ -559,6 +614,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", dest="fp8", action="store_false",
+                    help="skip the E4M3-weight measurement of the same workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

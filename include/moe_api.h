@@ -65,7 +65,9 @@ typedef enum {
   MOE_ERR_DEVICE_CHECK = 6  /* (device status) a device-side check failed */
 } moe_status;
 
-typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+/* MOE_DTYPE_E4M3: bf16 activations with E4M3 expert weights, one power-of-two
+ * scale per weight row (moe_quantize_rows_e4m3); only moe_forward_fp8 takes it. */
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1, MOE_DTYPE_E4M3 = 2 } moe_dtype;
 
 /* Token-tile choice of the grouped GEMMs. AUTO: a batch of T <= 64 tokens
  * uses 32-token tiles (its rows gathered inside the GEMM's loads); larger
@@ -225,6 +227,38 @@ typedef struct {
   int64_t logits, topk_ids, topk_w, expert_offsets, gather_idx, slot_pos, h, h_shared;
 } moe_workspace_layout;
 moe_status moe_get_workspace_layout(const moe_problem* pb, moe_workspace_layout* out);
+
+/* FP8 expert weights ("Hosting Qwen on Blackwell": Qwen3-235B served with FP8
+ * microscaled weights converted statically). A matrix is stored as E4M3 codes
+ * (OCP 8-bit floating point: 4 exponent bits, bias 7, 3 mantissa bits, largest
+ * finite 448, no infinities) with one power-of-two scale per row:
+ *   e = the smallest integer with max_i |v_i| <= 448 * 2^e, e >= -126 (e = 0
+ *       for a row of zeros); scale = 2^e; q_i = E4M3(v_i / 2^e), nearest even.
+ * Scaling by powers of two never rounds, so a value is q * scale and a dot
+ * product of two rows is scale_a * scale_b * sum(q_a * q_b).
+ * src [rows][cols] bf16 or fp32 (src_dtype), cols a multiple of 16 -> q uint8
+ * [rows][cols], scale fp32 [rows]. Device pointers, 16-byte aligned. */
+moe_status moe_quantize_rows_e4m3(const void* src, int32_t src_dtype, int64_t rows,
+                                  int64_t cols, uint8_t* q, float* scale, void* stream);
+
+/* The layer with E4M3 expert weights: pb->dtype = MOE_DTYPE_E4M3; x, W_router
+ * and y are bf16 (y fp32 with out_f32); routing and permutation as moe_forward.
+ * Weights are the outputs of moe_quantize_rows_e4m3 over the bf16/fp32 matrices
+ * viewed as rows: Wq_gate, Wq_up [E*I][H] with s_gate, s_up [E*I]; Wq_down
+ * [E*H][I] with s_down [E*H]; shared Wsq_gate, Wsq_up [I_s][H] with ss_gate,
+ * ss_up [I_s]; Wsq_down [H][I_s] with ss_down [H] (all NULL iff I_shared == 0).
+ * Per forward pass each token row of x is quantized the same way; the gated
+ * GEMM accumulates code products in fp32 and applies both scales, then
+ * h = bf16(silu(g) * u); each h row is quantized; the down GEMM applies its
+ * scales and the gate weight; the combine is moe_forward's. Requires I and
+ * I_shared multiples of 128. Workspace: moe_workspace_size(pb). */
+moe_status moe_forward_fp8(const moe_problem* pb, const void* x, const void* W_router,
+                           const float* router_bias, const uint8_t* Wq_gate, const float* s_gate,
+                           const uint8_t* Wq_up, const float* s_up, const uint8_t* Wq_down,
+                           const float* s_down, const uint8_t* Wsq_gate, const float* ss_gate,
+                           const uint8_t* Wsq_up, const float* ss_up, const uint8_t* Wsq_down,
+                           const float* ss_down, void* y, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, then copies the device status word into *out. */
 moe_status moe_get_device_status(const void* workspace, void* stream, moe_status* out);

@@ -12,11 +12,11 @@ from __future__ import annotations
 import torch
 
 from ._binding import (  # noqa: F401
-    EXPORTED, MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_FLAG_TEST_SKIP_SIGNAL, MOE_OK,
+    EXPORTED, MOE_DTYPE_BF16, MOE_DTYPE_E4M3, MOE_DTYPE_F32, MOE_FLAG_TEST_SKIP_SIGNAL, MOE_OK,
     MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_MEDIUM, MOE_TILE_PREFILL, STATUS_NAMES, MoEError, MoEProblem,
-    down_combine, down_combine_noalloc, forward, get_device_status, grouped_swiglu_gemm, load_library, make_problem,
-    permute, reset_device_status, route, route_grouped, router_logits, status_string,
-    workspace_layout,
+    down_combine, down_combine_noalloc, forward, forward_fp8, get_device_status, grouped_swiglu_gemm, load_library, make_problem,
+    permute, quantize_rows_e4m3, reset_device_status, route, route_grouped, router_logits,
+    status_string, workspace_layout,
     workspace_size)
 
 
@@ -66,6 +66,64 @@ class MoELayer:
         forward(self.problem(T, out_f32=out_f32), x, self.W_router, self.router_bias,
                 self.W_gate, self.W_up, self.W_down, self.Ws_gate, self.Ws_up, self.Ws_down, y,
                 self.workspace(T), stream)
+        return y
+
+    __call__ = forward
+
+
+def quantize_e4m3(W: torch.Tensor):
+    """(codes uint8, row scales fp32) of W viewed as rows of its last dimension,
+    by moe_quantize_rows_e4m3 (E4M3 with one power-of-two scale per row)."""
+    rows = W.numel() // W.shape[-1]
+    q = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+    s = torch.empty(W.shape[:-1], dtype=torch.float32, device=W.device)
+    quantize_rows_e4m3(W.reshape(rows, W.shape[-1]), q.view(rows, W.shape[-1]), s.view(rows))
+    return q, s
+
+
+class MoELayerFP8:
+    """The layer with E4M3 expert weights (moe_forward_fp8). Takes the same bf16
+    weights as MoELayer and quantizes the expert matrices once, row by row, on
+    the GPU; x, W_router and y stay bf16."""
+
+    def __init__(self, W_router, W_gate, W_up, W_down, k, router_bias=None, Ws_gate=None,
+                 Ws_up=None, Ws_down=None, renorm=1, tile=MOE_TILE_AUTO, n_group=1,
+                 topk_group=1):
+        self.W_router, self.router_bias = W_router, router_bias
+        self.E, self.I, self.H = W_gate.shape
+        self.I_shared = 0 if Ws_gate is None else Ws_gate.shape[0]
+        self.k, self.renorm, self.tile = k, renorm, tile
+        self.n_group, self.topk_group = n_group, topk_group
+        self.dtype = torch.bfloat16  # activations (x, y)
+        self.gate, self.up, self.down = (quantize_e4m3(W) for W in (W_gate, W_up, W_down))
+        if self.I_shared:
+            self.s_gate, self.s_up, self.s_down = (quantize_e4m3(W) for W in (Ws_gate, Ws_up,
+                                                                             Ws_down))
+        else:
+            self.s_gate = self.s_up = self.s_down = (None, None)
+        self._ws = {}
+
+    def problem(self, T: int, flags: int = 0, wait_limit_us: int = 0,
+                out_f32: bool = False) -> MoEProblem:
+        return make_problem(T, self.H, self.E, self.k, self.I, self.I_shared, self.renorm,
+                            "e4m3", self.tile, flags, wait_limit_us, out_f32, self.n_group,
+                            self.topk_group)
+
+    def workspace(self, T: int) -> torch.Tensor:
+        ws = self._ws.get(T)
+        if ws is None:
+            n = workspace_size(self.problem(T))
+            ws = torch.zeros(n, dtype=torch.uint8, device=self.W_router.device)
+            self._ws[T] = ws
+        return ws
+
+    def forward(self, x, out=None, stream=None, out_f32=False):
+        T = x.shape[0]
+        odt = torch.float32 if out_f32 else torch.bfloat16
+        y = out if out is not None else torch.empty((T, self.H), dtype=odt, device=x.device)
+        forward_fp8(self.problem(T, out_f32=out_f32), x, self.W_router, self.router_bias,
+                    *self.gate, *self.up, *self.down, *self.s_gate, *self.s_up, *self.s_down, y,
+                    self.workspace(T), stream)
         return y
 
     __call__ = forward

@@ -18,7 +18,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
                 6: "MOE_ERR_DEVICE_CHECK"}
-MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
+MOE_DTYPE_F32, MOE_DTYPE_BF16, MOE_DTYPE_E4M3 = 0, 1, 2
 MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_PREFILL, MOE_TILE_MEDIUM = 0, 1, 2, 3
 MOE_FLAG_TEST_SKIP_SIGNAL = 0x1
 
@@ -27,7 +27,8 @@ EXPORTED = ("moe_workspace_size", "moe_router_logits", "moe_route", "moe_route_g
             "moe_permute",
             "moe_grouped_swiglu_gemm", "moe_down_combine", "moe_forward",
             "moe_get_workspace_layout", "moe_get_device_status", "moe_reset_device_status",
-            "moe_status_string", "moe_down_combine_noalloc")
+            "moe_status_string", "moe_down_combine_noalloc", "moe_quantize_rows_e4m3",
+            "moe_forward_fp8")
 
 
 class MoEError(RuntimeError):
@@ -82,6 +83,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_get_workspace_layout": [pb, ctypes.POINTER(MoEWorkspaceLayout)],
             "moe_get_device_status": [_P, _P, ctypes.POINTER(ctypes.c_int)],
             "moe_reset_device_status": [_P, _P],
+            "moe_quantize_rows_e4m3": [_P, ctypes.c_int32, _I64, _I64, _P, _P, _P],
+            "moe_forward_fp8": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                _P, _P, ctypes.c_size_t, _P],
             "moe_down_combine_noalloc": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.POINTER(ctypes.c_int)],
         }
@@ -120,7 +124,8 @@ def _check(name: str, code: int):
 def make_problem(T, H, E, k, I, I_shared=0, renorm=1, dtype="bf16", tile=MOE_TILE_AUTO,
                  flags=0, wait_limit_us=0, out_f32=False, n_group=1,
                  topk_group=1) -> MoEProblem:
-    dt = MOE_DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else MOE_DTYPE_F32
+    dt = (MOE_DTYPE_BF16 if dtype in ("bf16", torch.bfloat16)
+          else MOE_DTYPE_E4M3 if dtype == "e4m3" else MOE_DTYPE_F32)
     return MoEProblem(T, H, E, k, I, I_shared, renorm, dt, tile, flags, wait_limit_us,
                       1 if out_f32 else 0, n_group, topk_group)
 
@@ -193,6 +198,24 @@ def down_combine_noalloc(problem, h, h_shared, expert_offsets, gather_idx, topk_
         _ptr(topk_w), _ptr(W_down), _ptr(Ws_down), _ptr(y), _stream(stream),
         ctypes.byref(st) if want_status else None))
     return int(st.value) if want_status else None
+
+
+def quantize_rows_e4m3(src, q, scale, stream=None):
+    """E4M3 codes q [rows, cols] (uint8) and power-of-two row scales (fp32) of
+    src [rows, cols] (bf16 or fp32), as moe_quantize_rows_e4m3 defines them."""
+    rows, cols = src.shape
+    dt = MOE_DTYPE_BF16 if src.dtype == torch.bfloat16 else MOE_DTYPE_F32
+    _check("moe_quantize_rows_e4m3", load_library().moe_quantize_rows_e4m3(
+        _ptr(src), dt, rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def forward_fp8(problem, x, W_router, router_bias, Wq_gate, s_gate, Wq_up, s_up, Wq_down, s_down,
+                Wsq_gate, ss_gate, Wsq_up, ss_up, Wsq_down, ss_down, y, workspace, stream=None):
+    _check("moe_forward_fp8", load_library().moe_forward_fp8(
+        ctypes.byref(problem), _ptr(x), _ptr(W_router), _ptr(router_bias), _ptr(Wq_gate),
+        _ptr(s_gate), _ptr(Wq_up), _ptr(s_up), _ptr(Wq_down), _ptr(s_down), _ptr(Wsq_gate),
+        _ptr(ss_gate), _ptr(Wsq_up), _ptr(ss_up), _ptr(Wsq_down), _ptr(ss_down), _ptr(y),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def forward(problem, x, W_router, router_bias, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,

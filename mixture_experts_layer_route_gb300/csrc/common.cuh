@@ -191,8 +191,9 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor for kind::f16 (fmt 1 = bf16) or kind::tf32 (fmt 2):
-// fp32 accumulator, both operands K-major, shape M x N.
+// Instruction descriptor for kind::f16 (fmt 1 = bf16), kind::tf32 (fmt 2) or
+// kind::f8f6f4 (fmt 0 = E4M3): fp32 accumulator, both operands K-major, shape
+// M x N.
 __host__ __device__ constexpr uint32_t umma_idesc(uint32_t fmt, uint32_t M, uint32_t N) {
   return (1u << 4)                 // D format: f32
          | (fmt << 7)              // A format
@@ -201,14 +202,44 @@ __host__ __device__ constexpr uint32_t umma_idesc(uint32_t fmt, uint32_t M, uint
          | ((M >> 4) << 24);       // M / 16
 }
 
-template <bool TF32>
+// Operand kinds of tcgen05.mma: bf16 x bf16 (kind::f16), fp32 read as tf32
+// (kind::tf32), E4M3 x E4M3 (kind::f8f6f4). The instruction descriptor's A/B
+// format codes: bf16 1, tf32 2, E4M3 0.
+enum UmmaKind : int { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
+
+template <typename TIn>
+struct UmmaOf;
+template <>
+struct UmmaOf<__nv_bfloat16> {
+  static constexpr int kind = kKindF16;
+  static constexpr uint32_t fmt = 1;
+};
+template <>
+struct UmmaOf<float> {
+  static constexpr int kind = kKindTF32;
+  static constexpr uint32_t fmt = 2;
+};
+template <>
+struct UmmaOf<uint8_t> {  // E4M3 codes
+  static constexpr int kind = kKindF8;
+  static constexpr uint32_t fmt = 0;
+};
+
+template <int KIND>
 __device__ __forceinline__ void umma_issue(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                            uint32_t idesc, uint32_t accumulate) {
-  if constexpr (TF32) {
+  if constexpr (KIND == kKindTF32) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else if constexpr (KIND == kKindF8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   } else {
@@ -228,14 +259,21 @@ __device__ __forceinline__ void umma_issue(uint32_t d_tmem, uint64_t adesc, uint
 // peer); D rows 0..M/2-1 land in the leader's tensor memory and the rest in the
 // peer's, at the same column address. A kernel uses one cta_group throughout.
 
-template <bool TF32>
+template <int KIND>
 __device__ __forceinline__ void umma_issue_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                 uint32_t idesc, uint32_t accumulate) {
-  if constexpr (TF32) {
+  if constexpr (KIND == kKindTF32) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else if constexpr (KIND == kKindF8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   } else {

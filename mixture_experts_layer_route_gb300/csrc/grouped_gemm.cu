@@ -44,9 +44,10 @@ bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, ui
                   uint32_t box_rows) {
   auto enc = encoder();
   if (!enc) return false;
-  const uint32_t es = dtype == MOE_DTYPE_BF16 ? 2 : 4;
-  const CUtensorMapDataType dt =
-      dtype == MOE_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const uint32_t es = dtype == MOE_DTYPE_BF16 ? 2 : (dtype == MOE_DTYPE_E4M3 ? 1 : 4);
+  const CUtensorMapDataType dt = dtype == MOE_DTYPE_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == MOE_DTYPE_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * es};
   cuuint32_t box[2] = {128u / es, box_rows};
@@ -180,6 +181,27 @@ void fill_common(GroupedGemmArgs& a, const GemmProblem& p, const int32_t* offset
   a.tile_n = tile_n;
 }
 
+template <typename TIn>
+cudaError_t launch_gated(const GroupedGemmArgs& a, const GemmProblem& p, bool dec, bool pair,
+                         int tile_n, size_t ub, cudaStream_t st) {
+  if (dec) return launch_variant<TIn, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st);
+  if (pair && tile_n == 128)
+    return launch_variant<TIn, true, 128, 8, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2, st);
+  if (pair) return launch_variant<TIn, true, 256, 6, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2, st);
+  return launch_variant<TIn, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
+}
+
+template <typename TIn>
+cudaError_t launch_down(const GroupedGemmArgs& a, const GemmProblem& p, bool dec, bool pair,
+                        int tile_n, size_t ub, cudaStream_t st) {
+  if (dec) return launch_variant<TIn, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st);
+  if (pair && tile_n == 128)
+    return launch_variant<TIn, false, 128, 8, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2, st);
+  if (pair)
+    return launch_variant<TIn, false, 256, 6, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2, st);
+  return launch_variant<TIn, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
+}
+
 }  // namespace
 
 bool tensor_map_encoder_available() { return encoder() != nullptr; }
@@ -189,9 +211,8 @@ bool gemm_needs_expert_order_copy(const GemmProblem& p) { return !use_decode_ker
 cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* xg,
                                const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
                                const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,
-                               int* status, cudaStream_t st) {
+                               int* status, cudaStream_t st, const GemmScales* sc) {
   const bool has_s = p.Is > 0;
-  const bool bf16 = p.dtype == MOE_DTYPE_BF16;
   const bool dec = use_decode_kernel(p);
   // CTA pairs when every group has an even number of 64-row feature blocks.
   const bool pair = !dec && (p.I / 64) % 2 == 0 && (!has_s || (p.Is / 64) % 2 == 0);
@@ -220,6 +241,10 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
   }
   fill_common(a, p, offsets, gather_idx, status, tile_n);
   a.topk_w = nullptr;
+  if (sc) {
+    for (int i = 0; i < 4; ++i) a.sA[i] = sc->a[i];
+    for (int i = 0; i < 2; ++i) a.sB[i] = sc->b[i];
+  }
   a.out = h;
   a.out_shared = hs;
   a.n_out_routed = p.I;
@@ -230,29 +255,21 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
   a.ld_out_shared = has_s ? p.Is : 0;
   const int rb = p.I / 64, sb = has_s ? p.Is / 64 : 0;
   const size_t ub = unit_upper_bound(p.T, p.k, p.E, tile_n, rb, sb);
-  if (dec)
-    return bf16 ? launch_variant<__nv_bfloat16, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st)
-                : launch_variant<float, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st);
-  if (pair && tile_n == 128)
-    return bf16 ? launch_variant<__nv_bfloat16, true, 128, 8, kTiled, 2>(a, p.num_sms, p.E,
-                                                                        (ub + 1) / 2, st)
-                : launch_variant<float, true, 128, 8, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2,
-                                                                st);
-  if (pair)
-    return bf16 ? launch_variant<__nv_bfloat16, true, 256, 6, kTiled, 2>(a, p.num_sms, p.E,
-                                                                        (ub + 1) / 2, st)
-                : launch_variant<float, true, 256, 6, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2,
-                                                                st);
-  return bf16 ? launch_variant<__nv_bfloat16, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st)
-              : launch_variant<float, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
+  switch (p.dtype) {
+    case MOE_DTYPE_BF16:
+      return launch_gated<__nv_bfloat16>(a, p, dec, pair, tile_n, ub, st);
+    case MOE_DTYPE_E4M3:
+      return launch_gated<uint8_t>(a, p, dec, pair, tile_n, ub, st);
+    default:
+      return launch_gated<float>(a, p, dec, pair, tile_n, ub, st);
+  }
 }
 
 cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
                              const int32_t* offsets, const int32_t* gather_idx,
                              const float* topk_w, const void* Wd, const void* Wsd, float* Y,
-                             int* status, cudaStream_t st) {
+                             int* status, cudaStream_t st, const GemmScales* sc) {
   const bool has_s = p.Is > 0;
-  const bool bf16 = p.dtype == MOE_DTYPE_BF16;
   const bool dec = use_decode_kernel(p);
   const bool pair = !dec && (p.H / 128) % 2 == 0;
   const int tile_n = dec ? 32 : tiled_tile_n(p);
@@ -274,6 +291,10 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
   a.tmA[3] = a.tmA[2];
   fill_common(a, p, offsets, gather_idx, status, tile_n);
   a.topk_w = topk_w;
+  if (sc) {
+    for (int i = 0; i < 4; ++i) a.sA[i] = sc->a[i];
+    for (int i = 0; i < 2; ++i) a.sB[i] = sc->b[i];
+  }
   a.out = Y;
   a.out_shared = nullptr;
   a.n_out_routed = p.H;
@@ -284,21 +305,14 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
   a.ld_out_shared = p.H;
   const int rb = p.H / 128, sb = has_s ? p.H / 128 : 0;
   const size_t ub = unit_upper_bound(p.T, p.k, p.E, tile_n, rb, sb);
-  if (dec)
-    return bf16 ? launch_variant<__nv_bfloat16, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st)
-                : launch_variant<float, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st);
-  if (pair && tile_n == 128)
-    return bf16 ? launch_variant<__nv_bfloat16, false, 128, 8, kTiled, 2>(a, p.num_sms, p.E,
-                                                                         (ub + 1) / 2, st)
-                : launch_variant<float, false, 128, 8, kTiled, 2>(a, p.num_sms, p.E,
-                                                                 (ub + 1) / 2, st);
-  if (pair)
-    return bf16 ? launch_variant<__nv_bfloat16, false, 256, 6, kTiled, 2>(a, p.num_sms, p.E,
-                                                                         (ub + 1) / 2, st)
-                : launch_variant<float, false, 256, 6, kTiled, 2>(a, p.num_sms, p.E,
-                                                                 (ub + 1) / 2, st);
-  return bf16 ? launch_variant<__nv_bfloat16, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st)
-              : launch_variant<float, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
+  switch (p.dtype) {
+    case MOE_DTYPE_BF16:
+      return launch_down<__nv_bfloat16>(a, p, dec, pair, tile_n, ub, st);
+    case MOE_DTYPE_E4M3:
+      return launch_down<uint8_t>(a, p, dec, pair, tile_n, ub, st);
+    default:
+      return launch_down<float>(a, p, dec, pair, tile_n, ub, st);
+  }
 }
 
 }  // namespace moe

@@ -61,6 +61,8 @@
 // under the main loop of the next. Every wait is bounded (status word).
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace moe {
@@ -77,7 +79,14 @@ struct GroupedGemmArgs {
   const int32_t* offsets;     // [E+2]
   const int32_t* gather_idx;  // [T*k]
   const float* topk_w;        // [T*k] (DOWN)
-  void* out;                  // GATED: h [T*k][I]; DOWN: Y fp32 [T][KP][H]
+  // E4M3 inputs only (TIn = uint8_t): power-of-two scale of every A row
+  // (indexed like tmA, by the row's global index) and of every B row (GATED: x
+  // rows by token, for routed and shared tiles; DOWN: [0] h rows by position,
+  // [1] h_shared rows by token). Products are exact in fp32, so the epilogue
+  // applies them to the accumulator without rounding.
+  const float* sA[4];
+  const float* sB[2];
+  void* out;                  // GATED: h [T*k][I] (bf16 for E4M3 inputs); DOWN: Y fp32 [T][KP][H]
   void* out_shared;           // GATED: h_shared [T][I_shared]
   int* status;
   unsigned long long limit_ns;
@@ -94,6 +103,9 @@ enum BMode : int { kGather4 = 0, kTiled = 2 };
 
 template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1>
 struct GemmCfg {
+  // E4M3 inputs (uint8_t codes) write bf16 h; other inputs write their own type.
+  static constexpr bool F8 = sizeof(TIn) == 1;
+  using TOut = std::conditional_t<F8, __nv_bfloat16, TIn>;
   static constexpr int BM = 128;                     // MMA M (weight rows)
   static constexpr int WM = GATED ? 64 : 128;        // output features per tile
   static constexpr int BK = 128 / (int)sizeof(TIn);  // K per stage (one 128-byte row)
@@ -105,13 +117,13 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   // Epilogue staging: GATED, the 128 x 32 accumulator chunk (gate and up rows
   // meet in one thread); DOWN, per-token row index and gate weight.
-  static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
+  static constexpr int EPI_FLOATS = GATED ? 128 * 33 + (F8 ? BN : 0) : 2 * BN;
   static constexpr int THREADS = 192;
   static_assert(CL == 1 || (CL == 2 && BMODE == kTiled && BN >= 64),
                 "CTA pairs split tiled token boxes of >= 64 rows");
   // Pair MMAs round N up to 32 (each CTA's half a multiple of 16 rows).
   static constexpr int N_ROUND = CL == 2 ? 32 : 16;
-  static constexpr bool TF32 = sizeof(TIn) == 4;
+  static constexpr int KIND = UmmaOf<TIn>::kind;
   static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
                     TMEM_COLS == 512,
                 "TMEM allocation must be a power of two in [32, 512]");
@@ -421,7 +433,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       uint32_t it = 0, lt = 0;
-      constexpr uint32_t fmt = C::TF32 ? 2u : 1u;
+      constexpr uint32_t fmt = UmmaOf<TIn>::fmt;
       bool ok = true;
       for (int u = cid; u < total && ok; u += ncl, ++lt) {
         Tile tl = decode_tile(u, prefix, order, offs, ngroups, args.tile_n);
@@ -448,9 +460,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
             const uint64_t bd = umma_desc_sw128(b_addr + kk * 32);
             const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
             if constexpr (PAIR)
-              umma_issue_pair<C::TF32>(d_tmem, ad, bd, idesc, accum);
+              umma_issue_pair<C::KIND>(d_tmem, ad, bd, idesc, accum);
             else
-              umma_issue<C::TF32>(d_tmem, ad, bd, idesc, accum);
+              umma_issue<C::KIND>(d_tmem, ad, bd, idesc, accum);
           }
           if constexpr (PAIR)
             umma_commit_pair_multicast(empty_bar(s), 0x3);
@@ -500,8 +512,17 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
             row = t * args.KP + (s - t * args.k);
             wv = args.topk_w[s];
           }
+          // E4M3: the h row's power-of-two scale joins the gate weight (exact).
+          if constexpr (C::F8) wv *= shared ? args.sB[1][tl.p0 - offs[E] + j] : args.sB[0][tl.p0 + j];
           yrow[j] = row;
           wt[j] = wv;
+        }
+      } else if constexpr (C::F8) {
+        // Scale of each column's token row (x quantized per token).
+        float* cs = epi + 128 * 33;
+        for (int j = et; j < tl.n_valid; j += 128) {
+          const int t = shared ? tl.p0 - offs[E] + j : args.gather_idx[tl.p0 + j] / args.k;
+          cs[j] = args.sB[0][t];
         }
       }
       named_barrier_sync(1, 128);
@@ -509,15 +530,31 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       tc_fence_after();
       const uint32_t t_acc = tmem_base + lane_base + acc * BN;
       if constexpr (GATED) {
-        TIn* out = reinterpret_cast<TIn*>(shared ? args.out_shared : args.out);
+        using TOut = typename C::TOut;
+        TOut* out = reinterpret_cast<TOut*>(shared ? args.out_shared : args.out);
         const int ld = shared ? args.ld_out_shared : args.ld_out_routed;
         const int row0 = shared ? tl.p0 - offs[E] : tl.p0;
         const int jj = et >> 2, fg = et & 3;
+        // E4M3: this thread's accumulator row (lane r < 64 gate, else up row)
+        // has a power-of-two scale; each column adds its token's.
+        float rs = 1.0f;
+        if constexpr (C::F8) {
+          const int r = q * 32 + lane;
+          const int f = tl.nb * 64 + (r & 63);
+          const float* sa = args.sA[(shared ? 2 : 0) + (r >> 6)];
+          rs = sa[(shared ? 0 : tl.g * args.n_out_routed) + f];
+        }
+        const float* cs = epi + 128 * 33;
         for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
           float v[32];
           tmem_ld32(t_acc + c0, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) epi[(q * 32 + lane) * 33 + i] = v[i];
+          for (int i = 0; i < 32; ++i) {
+            if constexpr (C::F8)
+              epi[(q * 32 + lane) * 33 + i] = v[i] * (rs * cs[c0 + i]);
+            else
+              epi[(q * 32 + lane) * 33 + i] = v[i];
+          }
           named_barrier_sync(1, 128);
           const int j = c0 + jj;
           if (j < tl.n_valid) {
@@ -530,8 +567,8 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
               // far below the bf16 rounding of h that follows).
               hv[f] = __fdividef(g, 1.0f + __expf(-g)) * up;
             }
-            TIn* dst = out + (size_t)(row0 + j) * ld + tl.nb * 64 + fg * 16;
-            if constexpr (sizeof(TIn) == 2) {
+            TOut* dst = out + (size_t)(row0 + j) * ld + tl.nb * 64 + fg * 16;
+            if constexpr (sizeof(TOut) == 2) {
               uint4 pk[2];
               uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
@@ -562,9 +599,18 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         const float4* wt4 = reinterpret_cast<const float4*>(epi + BN);
         const size_t H = (size_t)args.n_out_routed;  // == n_out_shared for DOWN
         float* Yc = Y + tl.nb * 128 + q * 32 + lane;
+        // E4M3: power-of-two scale of this thread's W_down row (exact).
+        float rs = 1.0f;
+        if constexpr (C::F8)
+          rs = args.sA[shared ? 2 : 0][(shared ? 0 : (size_t)tl.g * H) + tl.nb * 128 + q * 32 +
+                                       lane];
         for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
           float v[32];
           tmem_ld32(t_acc + c0, v);
+          if constexpr (C::F8) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= rs;
+          }
           const int nj = min(32, tl.n_valid - c0);
 #pragma unroll
           for (int i4 = 0; i4 < 8; ++i4) {

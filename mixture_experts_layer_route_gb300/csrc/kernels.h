@@ -56,15 +56,28 @@ struct GemmProblem {
 // required when gemm_needs_expert_order_copy(p) (128/256-token tiles may run),
 // ignored otherwise (32-token tiles gather rows in the GEMM's own loads).
 bool gemm_needs_expert_order_copy(const GemmProblem& p);
+// Per-row power-of-two scales of E4M3 operands (dtype MOE_DTYPE_E4M3 only):
+// a[0..3] = gate, up, shared gate, shared up rows (gated GEMM) or a[0] = W_down,
+// a[2] = shared W_down rows (down GEMM); b[0] = x rows by token (gated) or h
+// rows by position (down), b[1] = h_shared rows by token (down).
+struct GemmScales {
+  const float* a[4];
+  const float* b[2];
+};
 cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* xg,
                                const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
                                const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,
-                               int* status, cudaStream_t st);
+                               int* status, cudaStream_t st, const GemmScales* sc = nullptr);
 cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
                              const int32_t* offsets, const int32_t* gather_idx,
                              const float* topk_w, const void* Wd, const void* Wsd, float* Y,
-                             int* status, cudaStream_t st);
+                             int* status, cudaStream_t st, const GemmScales* sc = nullptr);
 bool tensor_map_encoder_available();
+
+// Row quantization to E4M3 with a power-of-two scale per row (quantize.cu):
+// src [rows][cols] of MOE_DTYPE_BF16 or MOE_DTYPE_F32, cols a multiple of 16.
+cudaError_t launch_quantize_rows(int dtype, const void* src, int64_t rows, int64_t cols,
+                                 uint8_t* q, float* scale, int num_sms, cudaStream_t st);
 
 // Combine (combine.cu): y[t] = sum_j Y[t][j] for j < KP, rank order.
 cudaError_t launch_combine(int dtype, const float* Y, int T, int H, int KP, void* y,

@@ -17,6 +17,9 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
   size_t pscratch, logits, partials, ids, w, offsets, gather, slotpos, xg, h, hs, Y, total;
+  // E4M3 layers only: quantized token rows and scales, quantized h rows and
+  // scales (routed and shared); 0 otherwise.
+  size_t xq, sx, hq, sh, hsq, shs;
   int S;  // router split count
 };
 
@@ -48,14 +51,21 @@ bool needs_copy(const moe_problem& p) {
   return true;
 }
 
-size_t elem_bytes(int dtype) { return dtype == MOE_DTYPE_BF16 ? 2 : 4; }
+// Bytes of one element of the expert GEMM operands (E4M3 codes: 1).
+size_t elem_bytes(int dtype) {
+  return dtype == MOE_DTYPE_BF16 ? 2 : (dtype == MOE_DTYPE_E4M3 ? 1 : 4);
+}
+// Dtype of the activations (x, W_router, h, y): bf16 for E4M3 layers.
+int act_dtype(int dtype) { return dtype == MOE_DTYPE_E4M3 ? MOE_DTYPE_BF16 : dtype; }
 
 Layout layout_of(const moe_problem& p) {
   Layout L;
   const size_t es = elem_bytes(p.dtype);
   const size_t T = (size_t)p.T, E = (size_t)p.E, k = (size_t)p.k;
   const size_t KP = k + (p.I_shared > 0 ? 1 : 0);
-  L.S = router_split_count(p.dtype, p.T, p.H, p.E, kRouterSplitSms);
+  const bool f8 = p.dtype == MOE_DTYPE_E4M3;
+  const size_t as = elem_bytes(act_dtype(p.dtype));
+  L.S = router_split_count(act_dtype(p.dtype), p.T, p.H, p.E, kRouterSplitSms);
   size_t off = kHeader;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -73,9 +83,15 @@ Layout layout_of(const moe_problem& p) {
   L.gather = take(T * k * 4);
   L.slotpos = take(T * k * 4);
   // Prefill-sized tiles read the routed token rows from an expert-ordered copy.
+  L.xq = f8 ? take(T * (size_t)p.H) : 0;
+  L.sx = f8 ? take(T * 4) : 0;
   L.xg = needs_copy(p) ? take(T * k * (size_t)p.H * es) : 0;
-  L.h = take(T * k * (size_t)p.I * es);
-  L.hs = p.I_shared > 0 ? take(T * (size_t)p.I_shared * es) : 0;
+  L.h = take(T * k * (size_t)p.I * as);
+  L.hs = p.I_shared > 0 ? take(T * (size_t)p.I_shared * as) : 0;
+  L.hq = f8 ? take(T * k * (size_t)p.I) : 0;
+  L.sh = f8 ? take(T * k * 4) : 0;
+  L.hsq = f8 && p.I_shared > 0 ? take(T * (size_t)p.I_shared) : 0;
+  L.shs = f8 && p.I_shared > 0 ? take(T * 4) : 0;
   L.Y = take(T * KP * (size_t)p.H * 4);
   L.total = off;
   return L;
@@ -91,14 +107,21 @@ bool groups_valid(int64_t E, int64_t k, int64_t n_group, int64_t topk_group) {
   return k <= topk_group * (E / n_group);
 }
 
-moe_status check_problem(const moe_problem* pb) {
+// allow_e4m3: the entry points that take E4M3 weights (workspace queries and
+// moe_forward_fp8); the bf16/fp32 sub-calls reject that dtype.
+moe_status check_problem(const moe_problem* pb, bool allow_e4m3 = false) {
   if (!pb) return MOE_ERR_INVALID_ARG;
   const moe_problem& p = *pb;
   if (p.T < 0 || p.H <= 0 || p.E <= 0 || p.k <= 0 || p.I <= 0 || p.I_shared < 0)
     return MOE_ERR_INVALID_ARG;
   if (p.k > p.E || p.k > 32 || p.E > 1024) return MOE_ERR_INVALID_ARG;
   if (p.H % 128 != 0 || p.I % 64 != 0 || p.I_shared % 64 != 0) return MOE_ERR_INVALID_ARG;
-  if (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+  if (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32 &&
+      !(allow_e4m3 && p.dtype == MOE_DTYPE_E4M3))
+    return MOE_ERR_INVALID_ARG;
+  // E4M3 GEMMs take 128 codes of K per stage.
+  if (p.dtype == MOE_DTYPE_E4M3 && (p.I % 128 != 0 || p.I_shared % 128 != 0))
+    return MOE_ERR_INVALID_ARG;
   if (p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM) return MOE_ERR_INVALID_ARG;
   if (p.renorm != 0 && p.renorm != 1) return MOE_ERR_INVALID_ARG;
   if (p.out_f32 != 0 && p.out_f32 != 1) return MOE_ERR_INVALID_ARG;
@@ -162,7 +185,7 @@ const char* moe_status_string(moe_status s) {
 }
 
 moe_status moe_workspace_size(const moe_problem* pb, size_t* bytes) {
-  moe_status s = check_problem(pb);
+  moe_status s = check_problem(pb, true);
   if (s != MOE_OK) return s;
   if (!bytes) return MOE_ERR_INVALID_ARG;
   *bytes = layout_of(*pb).total;
@@ -170,7 +193,7 @@ moe_status moe_workspace_size(const moe_problem* pb, size_t* bytes) {
 }
 
 moe_status moe_get_workspace_layout(const moe_problem* pb, moe_workspace_layout* out) {
-  moe_status s = check_problem(pb);
+  moe_status s = check_problem(pb, true);
   if (s != MOE_OK) return s;
   if (!out) return MOE_ERR_INVALID_ARG;
   const Layout L = layout_of(*pb);
@@ -382,6 +405,102 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
     e = launch_down_gemm(g, h, hs, offs, gidx, w, W_down, Ws_down, Y, status, st);
   if (e == cudaSuccess)
     e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : pb->dtype, Y, g.T, g.H,
+                       g.k + (has_s ? 1 : 0), y, g.num_sms, st);
+  return cuda_status(e);
+}
+
+moe_status moe_quantize_rows_e4m3(const void* src, int32_t src_dtype, int64_t rows,
+                                  int64_t cols, uint8_t* q, float* scale, void* stream) {
+  if (src_dtype != MOE_DTYPE_BF16 && src_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || cols <= 0 || cols % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (cols >= ((int64_t)1 << 30)) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (!src || !q || !scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(q) || !aligned16(scale)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_quantize_rows(src_dtype, src, rows, cols, q, scale, sm_count(), (cudaStream_t)stream));
+}
+
+moe_status moe_forward_fp8(const moe_problem* pb, const void* x, const void* W_router,
+                           const float* router_bias, const uint8_t* Wq_gate, const float* s_gate,
+                           const uint8_t* Wq_up, const float* s_up, const uint8_t* Wq_down,
+                           const float* s_down, const uint8_t* Wsq_gate, const float* ss_gate,
+                           const uint8_t* Wsq_up, const float* ss_up, const uint8_t* Wsq_down,
+                           const float* ss_down, void* y, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!pb || pb->dtype != MOE_DTYPE_E4M3) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_problem(pb, true);
+  if (s != MOE_OK) return s;
+  if (pb->T == 0) return MOE_OK;
+  const bool has_s = pb->I_shared > 0;
+  const void* ptrs[] = {x, W_router, Wq_gate, s_gate, Wq_up, s_up, Wq_down, s_down, y};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (router_bias && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
+  const void* sptrs[] = {Wsq_gate, ss_gate, Wsq_up, ss_up, Wsq_down, ss_down};
+  for (const void* q : sptrs) {
+    if (has_s != (q != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  }
+  const Layout L = layout_of(*pb);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return s;
+  if (!tensor_map_encoder_available()) return MOE_ERR_UNSUPPORTED;
+
+  cudaStream_t st = (cudaStream_t)stream;
+  const GemmProblem g = gemm_problem(*pb);  // dtype E4M3: the expert GEMMs
+  int* status = status_ptr(workspace);
+  float* logits = at<float>(workspace, L.logits);
+  float* part = at<float>(workspace, L.partials);
+  int32_t* ids = at<int32_t>(workspace, L.ids);
+  float* w = at<float>(workspace, L.w);
+  int32_t* offs = at<int32_t>(workspace, L.offsets);
+  int32_t* gidx = at<int32_t>(workspace, L.gather);
+  int32_t* spos = at<int32_t>(workspace, L.slotpos);
+  uint8_t* xq = at<uint8_t>(workspace, L.xq);
+  float* sx = at<float>(workspace, L.sx);
+  void* h = at<void>(workspace, L.h);
+  void* hs = has_s ? at<void>(workspace, L.hs) : nullptr;
+  uint8_t* hq = at<uint8_t>(workspace, L.hq);
+  float* sh = at<float>(workspace, L.sh);
+  uint8_t* hsq = has_s ? at<uint8_t>(workspace, L.hsq) : nullptr;
+  float* shs = has_s ? at<float>(workspace, L.shs) : nullptr;
+  float* Y = at<float>(workspace, L.Y);
+
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+  // Router, routing and permutation exactly as the bf16 layer.
+  if (e == cudaSuccess)
+    e = launch_router_logits(MOE_DTYPE_BF16, x, W_router, router_bias, g.T, g.H, g.E, L.S, part,
+                             status, g.limit_ns, st);
+  if (e == cudaSuccess)
+    e = launch_route(part, L.S, router_bias, g.T, g.E, g.k, pb->renorm,
+                     pb->n_group > 1 ? pb->n_group : 1, pb->topk_group,
+                     L.S > 1 ? logits : nullptr, ids, w, st);
+  if (e == cudaSuccess)
+    e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status,
+                       at<int32_t>(workspace, L.pscratch), st);
+  // Token rows to E4M3 (one scale per token), then the expert-ordered copy of
+  // the codes when the tiled kernel runs.
+  if (e == cudaSuccess)
+    e = launch_quantize_rows(MOE_DTYPE_BF16, x, g.T, g.H, xq, sx, g.num_sms, st);
+  void* xg = nullptr;
+  if (e == cudaSuccess && gemm_needs_expert_order_copy(g)) {
+    xg = at<void>(workspace, L.xg);
+    e = launch_gather_rows(xq, gidx, g.T * g.k, g.k, (size_t)g.H, xg, g.num_sms, st);
+  }
+  GemmScales sg = {{s_gate, s_up, ss_gate, ss_up}, {sx, sx}};
+  if (e == cudaSuccess)
+    e = launch_swiglu_gemm(g, xq, xg, offs, gidx, Wq_gate, Wq_up, Wsq_gate, Wsq_up, h, hs, status,
+                           st, &sg);
+  // h rows (bf16) to E4M3, one scale per row, for the down projection.
+  if (e == cudaSuccess)
+    e = launch_quantize_rows(MOE_DTYPE_BF16, h, (int64_t)g.T * g.k, g.I, hq, sh, g.num_sms, st);
+  if (e == cudaSuccess && has_s)
+    e = launch_quantize_rows(MOE_DTYPE_BF16, hs, g.T, g.Is, hsq, shs, g.num_sms, st);
+  GemmScales sd = {{s_down, nullptr, ss_down, nullptr}, {sh, shs}};
+  if (e == cudaSuccess)
+    e = launch_down_gemm(g, hq, hsq, offs, gidx, w, Wq_down, Wsq_down, Y, status, st, &sd);
+  if (e == cudaSuccess)
+    e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : MOE_DTYPE_BF16, Y, g.T, g.H,
                        g.k + (has_s ? 1 : 0), y, g.num_sms, st);
   return cuda_status(e);
 }

@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
       for (int kk = 0; kk < RC_BK / 16; ++kk)
-        umma_issue<false>(tmem, umma_desc_sw128(a_addr + kk * 32),
+        umma_issue<kKindF16>(tmem, umma_desc_sw128(a_addr + kk * 32),
                           umma_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
       umma_commit(empty_bar(s));
     }

@@ -49,6 +49,14 @@ def _declare(lib):
                                        _f, _L, _f]
     lib.oracle_moe_forward.argtypes = [_f, _f, _f, _f, _f, _f, _f, _f, _f, _L, _L, _L, _L, _L,
                                        _L, ctypes.c_int, _f, _f, _i, _f]
+    _u8 = ctypes.POINTER(ctypes.c_uint8)
+    lib.oracle_e4m3_decode.argtypes = [_u8, _L, _f]
+    lib.oracle_e4m3_encode.argtypes = [_f, _L, _u8]
+    lib.oracle_quantize_rows_e4m3.argtypes = [_f, _L, _L, _u8, _f]
+    lib.oracle_bf16_round.argtypes = [_f, _L, _f]
+    for n in ("oracle_e4m3_decode", "oracle_e4m3_encode", "oracle_quantize_rows_e4m3",
+              "oracle_bf16_round"):
+        getattr(lib, n).restype = None
     for n in ("oracle_router_logits", "oracle_route", "oracle_route_grouped", "oracle_permute",
               "oracle_expert_h",
               "oracle_down_combine", "oracle_ffn_combine", "oracle_moe_forward"):
@@ -171,6 +179,82 @@ class Oracle:
         if want_intermediates:
             return y, dict(logits=logits, ids=ids, w=w)
         return y
+
+
+def _u8p(a):
+    assert a.dtype == np.uint8 and a.flags.c_contiguous
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+
+
+def _fp8_methods():
+    """FP8 expert path (E4M3 codes, one power-of-two scale per row): the
+    quantization primitives, and the layer as a composition of the pinned
+    steps above with quantization between them."""
+
+    def e4m3_decode(self, codes):
+        codes = np.ascontiguousarray(codes, np.uint8)
+        out = np.empty(codes.shape, np.float32)
+        self.lib.oracle_e4m3_decode(_u8p(codes), codes.size, self._pf(out))
+        return out
+
+    def e4m3_encode(self, v):
+        v = np.ascontiguousarray(v, np.float32)
+        out = np.empty(v.shape, np.uint8)
+        self.lib.oracle_e4m3_encode(self._pf(v), v.size, _u8p(out))
+        return out
+
+    def quantize_rows_e4m3(self, src):
+        """src [..., cols] fp32 -> (codes uint8 [..., cols], scales fp32 [...])."""
+        src = np.ascontiguousarray(src, np.float32)
+        cols = src.shape[-1]
+        rows = src.size // cols
+        q = np.empty(src.shape, np.uint8)
+        sc = np.empty(src.shape[:-1], np.float32)
+        self.lib.oracle_quantize_rows_e4m3(self._pf(src), rows, cols, _u8p(q), self._pf(sc))
+        return q, sc
+
+    def dequantize_rows_e4m3(self, q, scale):
+        return self.e4m3_decode(q) * np.asarray(scale, np.float32)[..., None]
+
+    def bf16_round(self, a):
+        a = np.ascontiguousarray(a, np.float32)
+        out = np.empty(a.shape, np.float32)
+        self.lib.oracle_bf16_round(self._pf(a), a.size, self._pf(out))
+        return out
+
+    def forward_fp8(self, x, Wr, bias, Wg, Wu, Wd, k, renorm=1, Wsg=None, Wsu=None, Wsd=None,
+                    n_group=1, topk_group=1, want_intermediates=False):
+        """The layer with E4M3 expert weights: router and routing on x as in
+        forward; x rows, every weight row and every h row (after its bf16
+        rounding) quantized to E4M3 with a power-of-two scale; the experts and
+        the combine run on the dequantized values."""
+        T, H = x.shape
+        E, I, _ = Wg.shape
+        has_s = Wsg is not None
+        lg = self.router_logits(x, Wr, bias)
+        ids, w = self.route_grouped(lg, k, renorm, n_group, topk_group)
+        offs, gidx, spos = self.permute(ids, E, 1 if has_s else 0)
+        dq = lambda a: self.dequantize_rows_e4m3(*self.quantize_rows_e4m3(a))
+        xd = dq(x)
+        Wgd, Wud, Wdd = dq(Wg), dq(Wu), dq(Wd)
+        Wsgd, Wsud, Wsdd = (dq(Wsg), dq(Wsu), dq(Wsd)) if has_s else (None, None, None)
+        h, hs = self.expert_h(xd, offs, gidx, Wgd, Wud, k, Wsgd, Wsud)
+        hb = self.bf16_round(h)
+        hsb = self.bf16_round(hs) if has_s else None
+        y = self.down_combine(dq(hb), offs, spos, ids, w, Wdd, dq(hsb) if has_s else None, Wsdd)
+        if want_intermediates:
+            return y, dict(logits=lg, ids=ids, w=w, offsets=offs, gather_idx=gidx, h=hb, hs=hsb,
+                           h_f32=h, hs_f32=hs)
+        return y
+
+    return dict(e4m3_decode=e4m3_decode, e4m3_encode=e4m3_encode,
+                quantize_rows_e4m3=quantize_rows_e4m3,
+                dequantize_rows_e4m3=dequantize_rows_e4m3, bf16_round=bf16_round,
+                forward_fp8=forward_fp8)
+
+
+for _n, _fn in _fp8_methods().items():
+    setattr(Oracle, _n, _fn)
 
 
 def to_np(t):

@@ -74,6 +74,51 @@ void expert_ffn(const float* xr, const float* Wg, const float* Wu, const float* 
   }
 }
 
+// ---------------------------------------------------------------- FP8 rows
+// The FP8 expert path stores a matrix as E4M3 codes with one power-of-two
+// scale per row (the microscaling idea of "Hosting Qwen on Blackwell": scale
+// factors are exact powers of two, so scaling never rounds).
+//
+// E4M3 (OCP 8-bit floating point): sign bit, 4 exponent bits with bias 7, 3
+// mantissa bits. Exponent field 0 holds the subnormals m/8 * 2^-6. There are no
+// infinities; S.1111.111 is NaN, so the largest finite magnitude is
+// 1.75 * 2^8 = 448.
+double e4m3_decode_one(uint8_t c) {
+  const int s = c >> 7, ef = (c >> 3) & 15, m = c & 7;
+  if (ef == 15 && m == 7) return std::nan("");
+  const double mag = ef == 0 ? std::ldexp((double)m / 8.0, -6)
+                             : std::ldexp(1.0 + (double)m / 8.0, ef - 7);
+  return s ? -mag : mag;
+}
+
+// Nearest E4M3 value to v, ties to the even mantissa; |v| beyond 448 gives
+// 448 (callers scale rows so that this never happens).
+uint8_t e4m3_encode_one(float v) {
+  const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+  double a = std::fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;
+  // Spacing of the representable magnitudes around a: 2^(E-3) for a in
+  // [2^E, 2^(E+1)), E >= -6; 2^-9 below 2^-6 (subnormals).
+  int E = -6;
+  if (a >= std::ldexp(1.0, -6)) {
+    int e2;
+    std::frexp(a, &e2);  // a = f * 2^e2, f in [0.5, 1)
+    E = e2 - 1;
+  }
+  const double ulp = std::ldexp(1.0, E - 3);
+  double n = std::floor(a / ulp);  // exact: a / ulp is a power-of-two scaling
+  const double rem = a / ulp - n;
+  if (rem > 0.5 || (rem == 0.5 && std::fmod(n, 2.0) != 0.0)) n += 1.0;
+  const double r = n * ulp;  // the rounded magnitude
+  if (r >= 448.0) return sign | 0x7E;
+  if (r < std::ldexp(1.0, -6)) return sign | (uint8_t)n;  // subnormal: m = n
+  int e2;
+  const double f = std::frexp(r, &e2);  // r = f * 2^e2
+  const int ef = e2 - 1 + 7;
+  const int m = (int)std::lround((2.0 * f - 1.0) * 8.0);
+  return sign | (uint8_t)((ef << 3) | m);
+}
+
 }  // namespace
 
 extern "C" {
@@ -286,6 +331,51 @@ void oracle_ffn_combine(const float* x, const int32_t* ids, const float* w, cons
     for (int64_t c = 0; c < H; ++c) y[t * H + c] = (float)acc[c];
   }
 }
+
+void oracle_e4m3_decode(const uint8_t* codes, int64_t n, float* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = (float)e4m3_decode_one(codes[i]);
+}
+
+void oracle_e4m3_encode(const float* v, int64_t n, uint8_t* codes) {
+  for (int64_t i = 0; i < n; ++i) codes[i] = e4m3_encode_one(v[i]);
+}
+
+// Row quantization: scale = 2^e with e the smallest integer such that
+// max_i |src[r][i]| <= 448 * 2^e (e >= -126; e = 0 for a row of zeros), then
+// q[r][i] = E4M3(src[r][i] / 2^e), rounded to nearest even. Dividing by a
+// power of two is exact, so dequantization is q * scale.
+void oracle_quantize_rows_e4m3(const float* src, int64_t rows, int64_t cols, uint8_t* q,
+                               float* scale) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* v = src + r * cols;
+    double amax = 0.0;
+    for (int64_t i = 0; i < cols; ++i) amax = std::fmax(amax, std::fabs((double)v[i]));
+    int e = 0;
+    if (amax > 0.0) {
+      int e2;
+      const double f = std::frexp(amax, &e2);  // amax = (2f) * 2^(e2 - 1), 2f in [1, 2)
+      const int E = e2 - 1;
+      e = (2.0 * f <= 1.75) ? E - 8 : E - 7;
+      if (e < -126) e = -126;
+    }
+    scale[r] = std::ldexp(1.0f, e);
+    for (int64_t i = 0; i < cols; ++i)
+      q[r * cols + i] = e4m3_encode_one(std::ldexp(v[i], -e));
+  }
+}
+
+// bfloat16 rounding (nearest, ties to even) of fp32 values, returned as fp32.
+void oracle_bf16_round(const float* src, int64_t n, float* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t u;
+    std::memcpy(&u, &src[i], 4);
+    const uint32_t lsb = (u >> 16) & 1u;
+    u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;
+    std::memcpy(&out[i], &u, 4);
+  }
+}
+
 
 // The whole layer: steps 1-5. Every intermediate output pointer is nullable.
 void oracle_moe_forward(const float* x, const float* Wr, const float* bias, const float* Wg,

@@ -13,6 +13,7 @@ import oracle as oracle_pkg
 from oracle import Oracle, load
 
 import test_oracle as pins
+import test_oracle_fp8 as pins8
 
 MUTANTS = {
     "tie_break_to_higher_index": ("l[e] > l[best]", "l[e] >= l[best]"),
@@ -31,6 +32,11 @@ MUTANTS = {
     "group_score_is_sum": ("if (l[e] > best) best = l[e];", "best += l[e];"),
     "group_tie_break_to_higher_index": ("score[j] > score[bj]", "score[j] >= score[bj]"),
     "group_mask_ignored": ("if (taken[e] || !kept[e / G]) continue;", "if (taken[e]) continue;"),
+    "e4m3_ties_away_from_zero": ("if (rem > 0.5 || (rem == 0.5 && std::fmod(n, 2.0) != 0.0)) n += 1.0;",
+                                 "if (rem >= 0.5) n += 1.0;"),
+    "e4m3_row_scale_one_too_small": ("e = (2.0 * f <= 1.75) ? E - 8 : E - 7;", "e = E - 8;"),
+    "e4m3_exponent_bias": ("ef == 0 ? std::ldexp((double)m / 8.0, -6)\n                             : std::ldexp(1.0 + (double)m / 8.0, ef - 7);",
+                           "ef == 0 ? std::ldexp((double)m / 8.0, -6)\n                             : std::ldexp(1.0 + (double)m / 8.0, ef - 8);"),
 }
 
 PIN_CALLS = [
@@ -53,6 +59,10 @@ PIN_CALLS = [
     lambda o: pins.test_grouped_topk_matches_bruteforce(o, 64, 8, 8, 3),
     lambda o: pins.test_grouped_topk_reduces_to_plain_topk(o),
     lambda o: pins.test_grouped_topk_stays_in_kept_groups(o),
+    lambda o: pins8.test_decode_every_code_matches_torch(o),
+    lambda o: pins8.test_encode_round_trips_and_rounds_ties_to_even(o),
+    lambda o: pins8.test_encode_random_values_match_torch(o, 0),
+    lambda o: pins8.test_quantize_rows_follow_the_rule(o),
 ]
 
 
