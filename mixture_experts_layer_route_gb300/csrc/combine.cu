@@ -17,6 +17,7 @@ namespace {
 template <typename TOut>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ Y, int T, int H,
                                                       int KP, TOut* __restrict__ y) {
+  pdl_entry();
   const int h4 = H / 4;
   const size_t n = (size_t)T * h4;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
@@ -55,11 +56,10 @@ cudaError_t launch_combine(int dtype, const float* Y, int T, int H, int KP, void
   const size_t cap = (size_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (dtype == MOE_DTYPE_BF16)
-    combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(Y, T, H, KP,
-                                                                    (__nv_bfloat16*)y);
-  else
-    combine_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(Y, T, H, KP, (float*)y);
-  return cudaGetLastError();
+    return launch_chained(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0, st,
+                          1, Y, T, H, KP, (__nv_bfloat16*)y);
+  return launch_chained(combine_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, st, 1, Y, T,
+                        H, KP, (float*)y);
 }
 
 }  // namespace moe

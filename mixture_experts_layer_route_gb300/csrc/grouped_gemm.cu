@@ -104,8 +104,7 @@ cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t 
     size_t grid = (size_t)num_sms;
     if (upper_tiles < grid) grid = upper_tiles;
     if (grid == 0) return cudaSuccess;
-    fn<<<(unsigned)grid, C::THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_chained(fn, dim3((unsigned)grid), dim3(C::THREADS), smem, st, 1, a);
   }
   // Persistent grid of as many CTA pairs as can be resident at once; upper_tiles
   // counts pair units here.
@@ -128,10 +127,7 @@ cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t 
   size_t n = (size_t)clusters;
   if (upper_tiles < n) n = upper_tiles;
   if (n == 0) return cudaSuccess;
-  cfg.gridDim = dim3((unsigned)(n * CL), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, fn, a);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_chained(fn, dim3((unsigned)(n * CL)), dim3(C::THREADS), smem, st, CL, a);
 }
 
 // Upper bound of the unit count of one launch: T*k routed rows in at most

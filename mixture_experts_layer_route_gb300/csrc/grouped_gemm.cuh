@@ -173,6 +173,7 @@ __device__ __forceinline__ Tile decode_tile(int u, const int32_t* prefix, const 
 template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL>
 __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GroupedGemmArgs args) {
+  pdl_trigger();
   using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>;
   static_assert(GATED || BMODE == kTiled, "the down projection reads contiguous h rows");
   static_assert(BMODE != kGather4 || BN <= 128, "gather4 is for decode-sized token tiles");
@@ -226,6 +227,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     else
       tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
   }
+  pdl_wait();  // global memory from here on
   if (warp == 2) {
     // Schedule: the groups with rows in [m_lo, m_hi], heaviest class first
     // (> 256, > 128, > 32, the rest; group order within a class), so that the

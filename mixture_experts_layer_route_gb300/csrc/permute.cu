@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(PM_THREADS, 1)
     permute_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int has_shared,
                    int32_t* __restrict__ offsets, int32_t* __restrict__ gather_idx,
                    int32_t* __restrict__ slot_pos, int* status) {
+  pdl_entry();
   extern __shared__ int32_t sm[];
   permute_block<PM_WARPS, false>(ids, T, E, k, has_shared, offsets, gather_idx, slot_pos, status,
                                  sm);
@@ -44,6 +45,7 @@ constexpr int PM_CHUNK = 2048;
 __global__ void __launch_bounds__(PM_THREADS, 1)
     permute_count_kernel(const int32_t* __restrict__ ids, int n, int E,
                          int32_t* __restrict__ chunk_hist, int* status) {
+  pdl_entry();
   extern __shared__ int32_t sm[];
   int32_t* hist = sm;  // [E]
   const int tid = threadIdx.x, lane = tid & 31;
@@ -74,6 +76,7 @@ __global__ void __launch_bounds__(PM_THREADS, 1)
     permute_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int has_shared,
                            const int32_t* __restrict__ chunk_hist, int32_t* __restrict__ offsets,
                            int32_t* __restrict__ gather_idx, int32_t* __restrict__ slot_pos) {
+  pdl_entry();
   extern __shared__ int32_t sm[];
   int32_t* hist = sm;                        // [PM_WARPS][E]
   int32_t* total = sm + PM_WARPS * E;        // [E]: chunk base of expert e
@@ -197,6 +200,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ gather_idx,
                                                           int P, int k, int vecs_per_row,
                                                           uint4* __restrict__ xg) {
+  pdl_entry();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < P; p += warps) {
@@ -223,9 +227,9 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* gather_idx, int P, 
   const int vpr = (int)(row_bytes / 16);
   int blocks = (P + 7) / 8;
   if (blocks > 8 * num_sms) blocks = 8 * num_sms;
-  gather_rows_kernel<4><<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), gather_idx, P,
-                                                k, vpr, reinterpret_cast<uint4*>(xg));
-  return cudaGetLastError();
+  return launch_chained(gather_rows_kernel<4>, dim3(blocks), dim3(256), 0, st, 1,
+                        reinterpret_cast<const uint4*>(x), gather_idx, P, k, vpr,
+                        reinterpret_cast<uint4*>(xg));
 }
 
 size_t permute_smem_bytes(int E) { return sizeof(int32_t) * ((size_t)PM_WARPS * E + E + PM_WARPS); }
@@ -252,20 +256,18 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int has_shar
     err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (err != cudaSuccess) return err;
-    permute_kernel<<<1, PM_THREADS, smem, st>>>(ids, T, E, k, has_shared, offsets, gather_idx,
-                                                slot_pos, status);
-    return cudaGetLastError();
+    return launch_chained(permute_kernel, dim3(1), dim3(PM_THREADS), smem, st, 1, ids, T, E, k,
+                          has_shared, offsets, gather_idx, slot_pos, status);
   }
   err = cudaFuncSetAttribute(permute_scatter_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  permute_count_kernel<<<nchunk, PM_THREADS, (size_t)E * sizeof(int32_t), st>>>(
-      ids, T * k, E, chunk_hist, status);
-  err = cudaGetLastError();
+  err = launch_chained(permute_count_kernel, dim3(nchunk), dim3(PM_THREADS),
+                       (size_t)E * sizeof(int32_t), st, 1, ids, T * k, E, chunk_hist, status);
   if (err != cudaSuccess) return err;
-  permute_scatter_kernel<<<nchunk, PM_THREADS, smem, st>>>(ids, T, E, k, has_shared, chunk_hist,
-                                                           offsets, gather_idx, slot_pos);
-  return cudaGetLastError();
+  return launch_chained(permute_scatter_kernel, dim3(nchunk), dim3(PM_THREADS), smem, st, 1, ids,
+                        T, E, k, has_shared, (const int32_t*)chunk_hist, offsets, gather_idx,
+                        slot_pos);
 }
 
 }  // namespace moe

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const TIn* __restric
                                                             int64_t rows, int cols,
                                                             uint8_t* __restrict__ q,
                                                             float* __restrict__ scale) {
+  pdl_entry();
   const int lane = threadIdx.x & 31;
   const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
@@ -102,12 +103,10 @@ cudaError_t launch_quantize_rows(int dtype, const void* src, int64_t rows, int64
   int64_t blocks = (rows + 7) / 8;
   if (blocks > 16 * (int64_t)num_sms) blocks = 16 * (int64_t)num_sms;
   if (dtype == MOE_DTYPE_BF16)
-    quantize_rows_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
-        (const __nv_bfloat16*)src, rows, (int)cols, q, scale);
-  else
-    quantize_rows_kernel<float><<<(unsigned)blocks, 256, 0, st>>>((const float*)src, rows,
-                                                                  (int)cols, q, scale);
-  return cudaGetLastError();
+    return launch_chained(quantize_rows_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256),
+                          0, st, 1, (const __nv_bfloat16*)src, rows, (int)cols, q, scale);
+  return launch_chained(quantize_rows_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                        (const float*)src, rows, (int)cols, q, scale);
 }
 
 }  // namespace moe

@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TIn* __restric
                                                             const float* __restrict__ bias,
                                                             int T, int H, int E, int k_len,
                                                             float* __restrict__ out) {
+  pdl_entry();
   constexpr int VEC = 16 / sizeof(TIn);                 // elements per 16-byte load
   constexpr int LOADS = RT_BM * RT_BK / VEC / 256;       // per thread per operand
   __shared__ __align__(16) float As[2][RT_BK][RT_BM + RT_PAD];
@@ -190,6 +191,7 @@ template <typename TIn>
 __global__ void __launch_bounds__(256, 1) router_logits_big_kernel(
     const TIn* __restrict__ x, const TIn* __restrict__ Wr, const float* __restrict__ bias, int T,
     int H, int E, int k_len, float* __restrict__ out) {
+  pdl_entry();
   constexpr int VEC = 16 / sizeof(TIn);
   constexpr int LOADS = RL_BM * RL_BK / VEC / 256;  // per thread per operand
   extern __shared__ __align__(16) float rl_sm[];
@@ -336,6 +338,7 @@ size_t rc_smem_bytes(int n_tile) {
 
 __global__ void __launch_bounds__(128, 1)
     router_logits_tc_kernel(const __grid_constant__ RouterTcArgs a) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -366,6 +369,7 @@ __global__ void __launch_bounds__(128, 1)
     tma_prefetch_desc(&a.tmW);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_holder), (uint32_t)a.tmem_cols);
+  pdl_wait();  // global memory from here on
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -495,8 +499,7 @@ cudaError_t launch_router_logits_tc(const void* x, const void* Wr, const float* 
   }
   dim3 grid((unsigned)((T + RC_BM - 1) / RC_BM), (unsigned)((E + n_tile - 1) / n_tile),
             (unsigned)S);
-  router_logits_tc_kernel<<<grid, 128, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_chained(router_logits_tc_kernel, grid, dim3(128), smem, st, 1, a);
 }
 
 // Sum of S partial logits in ascending slice order, then the bias: identical
@@ -524,6 +527,7 @@ __device__ __forceinline__ float reduce_partials(const float* __restrict__ part,
 
 __global__ void logits_reduce_kernel(const float* __restrict__ part, int S, int T, int E,
                                      const float* __restrict__ bias, float* __restrict__ logits) {
+  pdl_entry();
   const size_t n = (size_t)T * E;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -646,6 +650,7 @@ __global__ void __launch_bounds__(256, 2) route_kernel(const float* __restrict__
                                                     float* __restrict__ logits_out,
                                                     int32_t* __restrict__ ids,
                                                     float* __restrict__ w) {
+  pdl_entry();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -785,28 +790,25 @@ cudaError_t launch_router_logits(int dtype, const void* x, const void* Wr, const
       e = cudaFuncSetAttribute(router_logits_big_kernel<__nv_bfloat16>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RL_SMEM);
       if (e != cudaSuccess) return e;
-      router_logits_big_kernel<__nv_bfloat16><<<grid, 256, RL_SMEM, st>>>(
-          (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wr, bias, T, H, E, k_len,
-          out_partials);
+      return launch_chained(router_logits_big_kernel<__nv_bfloat16>, grid, dim3(256),
+                            (size_t)RL_SMEM, st, 1, (const __nv_bfloat16*)x,
+                            (const __nv_bfloat16*)Wr, bias, T, H, E, k_len, out_partials);
     } else {
       e = cudaFuncSetAttribute(router_logits_big_kernel<float>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RL_SMEM);
       if (e != cudaSuccess) return e;
-      router_logits_big_kernel<float><<<grid, 256, RL_SMEM, st>>>(
-          (const float*)x, (const float*)Wr, bias, T, H, E, k_len, out_partials);
+      return launch_chained(router_logits_big_kernel<float>, grid, dim3(256), (size_t)RL_SMEM,
+                            st, 1, (const float*)x, (const float*)Wr, bias, T, H, E, k_len,
+                            out_partials);
     }
-    return cudaGetLastError();
   }
   dim3 grid((E + RT_BN - 1) / RT_BN, (T + RT_BM - 1) / RT_BM, S);
-  if (dtype == MOE_DTYPE_BF16) {
-    router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wr, bias, T, H, E, k_len, out_partials);
-  } else {
-    router_logits_kernel<float>
-        <<<grid, 256, 0, st>>>((const float*)x, (const float*)Wr, bias, T, H, E, k_len,
-                               out_partials);
-  }
-  return cudaGetLastError();
+  if (dtype == MOE_DTYPE_BF16)
+    return launch_chained(router_logits_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, 1,
+                          (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wr, bias, T, H, E, k_len,
+                          out_partials);
+  return launch_chained(router_logits_kernel<float>, grid, dim3(256), 0, st, 1, (const float*)x,
+                        (const float*)Wr, bias, T, H, E, k_len, out_partials);
 }
 
 cudaError_t launch_logits_reduce(const float* partials, int S, int T, int E, const float* bias,
@@ -815,8 +817,8 @@ cudaError_t launch_logits_reduce(const float* partials, int S, int T, int E, con
   if (n == 0) return cudaSuccess;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 8 * num_sms) blocks = 8 * num_sms;
-  logits_reduce_kernel<<<blocks, 256, 0, st>>>(partials, S, T, E, bias, logits);
-  return cudaGetLastError();
+  return launch_chained(logits_reduce_kernel, dim3(blocks), dim3(256), 0, st, 1, partials, S, T,
+                        E, bias, logits);
 }
 
 cudaError_t launch_route(const float* src, int S, const float* bias, int T, int E, int k,
@@ -827,8 +829,8 @@ cudaError_t launch_route(const float* src, int S, const float* bias, int T, int 
   const int blocks = (T + warps - 1) / warps;
   const int nv = (E + 31) / 32;
 #define MOE_ROUTE_CASE(NV)                                                                  \
-  route_kernel<NV><<<blocks, warps * 32, 0, st>>>(src, S, bias, T, E, k, renorm, n_group,   \
-                                                   topk_group, logits_out, ids, w)
+  return launch_chained(route_kernel<NV>, dim3(blocks), dim3(warps * 32), 0, st, 1, src, S, bias, \
+                        T, E, k, renorm, n_group, topk_group, logits_out, ids, w)
   if (nv <= 1) MOE_ROUTE_CASE(1);
   else if (nv <= 2) MOE_ROUTE_CASE(2);
   else if (nv <= 4) MOE_ROUTE_CASE(4);
