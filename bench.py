@@ -373,12 +373,21 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The slowest rank's time: every rank's replica must finish before the
+    job's tokens count as done."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tokens_per_s(world, T, steps, ms_total):
+    """Whole-job throughput of `world` independent replicas, each running
+    `steps` layer passes over T tokens in ms_total (the max over ranks)."""
+    return world * T * steps / (ms_total / 1e3)
 
 
 def measure_config(cfg, args, world, local, with_clocks):
@@ -464,7 +473,7 @@ def summarize(r, peaks, world, prefix_src):
     cfg = r["cfg"]
     steps = r["steps"]
     ms_step = r["ms_total"] / steps
-    value = world * cfg.T * steps / (r["ms_total"] / 1e3)
+    value = job_tokens_per_s(world, cfg.T, steps, r["ms_total"])
     rl = r["rl"]
     st = dict(zip(STAGES, r["per_stage"]))
     g_ms = st["swiglu_gemm"]
