@@ -222,18 +222,17 @@ def _fp8_methods():
         self.lib.oracle_bf16_round(self._pf(a), a.size, self._pf(out))
         return out
 
-    def forward_fp8(self, x, Wr, bias, Wg, Wu, Wd, k, renorm=1, Wsg=None, Wsu=None, Wsd=None,
-                    n_group=1, topk_group=1, want_intermediates=False):
-        """The layer with E4M3 expert weights: router and routing on x as in
-        forward; x rows, every weight row and every h row (after its bf16
-        rounding) quantized to E4M3 with a power-of-two scale; the experts and
-        the combine run on the dequantized values."""
-        T, H = x.shape
-        E, I, _ = Wg.shape
+    def ffn_combine_fp8(self, x, ids, w, Wg, Wu, Wd, Wsg=None, Wsu=None, Wsd=None,
+                        want_intermediates=False):
+        """The experts and the combine of the FP8 layer for given routing: x
+        rows, every weight row and every h row (after its bf16 rounding)
+        quantized to E4M3 with a power-of-two scale; the experts and the
+        combine run on the dequantized values."""
+        E = Wg.shape[0]
+        k = ids.shape[1]
         has_s = Wsg is not None
-        lg = self.router_logits(x, Wr, bias)
-        ids, w = self.route_grouped(lg, k, renorm, n_group, topk_group)
-        offs, gidx, spos = self.permute(ids, E, 1 if has_s else 0)
+        offs, gidx, spos = self.permute(np.ascontiguousarray(ids, np.int32), E,
+                                        1 if has_s else 0)
         dq = lambda a: self.dequantize_rows_e4m3(*self.quantize_rows_e4m3(a))
         xd = dq(x)
         Wgd, Wud, Wdd = dq(Wg), dq(Wu), dq(Wd)
@@ -241,16 +240,29 @@ def _fp8_methods():
         h, hs = self.expert_h(xd, offs, gidx, Wgd, Wud, k, Wsgd, Wsud)
         hb = self.bf16_round(h)
         hsb = self.bf16_round(hs) if has_s else None
-        y = self.down_combine(dq(hb), offs, spos, ids, w, Wdd, dq(hsb) if has_s else None, Wsdd)
+        y = self.down_combine(dq(hb), offs, spos, np.ascontiguousarray(ids, np.int32),
+                              np.ascontiguousarray(w, np.float32), Wdd,
+                              dq(hsb) if has_s else None, Wsdd)
         if want_intermediates:
-            return y, dict(logits=lg, ids=ids, w=w, offsets=offs, gather_idx=gidx, h=hb, hs=hsb,
-                           h_f32=h, hs_f32=hs)
+            return y, dict(offsets=offs, gather_idx=gidx, h=hb, hs=hsb, h_f32=h, hs_f32=hs)
+        return y
+
+    def forward_fp8(self, x, Wr, bias, Wg, Wu, Wd, k, renorm=1, Wsg=None, Wsu=None, Wsd=None,
+                    n_group=1, topk_group=1, want_intermediates=False):
+        """The layer with E4M3 expert weights: router and routing on x as in
+        forward, then ffn_combine_fp8."""
+        lg = self.router_logits(x, Wr, bias)
+        ids, w = self.route_grouped(lg, k, renorm, n_group, topk_group)
+        y, inter = self.ffn_combine_fp8(x, ids, w, Wg, Wu, Wd, Wsg, Wsu, Wsd,
+                                        want_intermediates=True)
+        if want_intermediates:
+            return y, dict(logits=lg, ids=ids, w=w, **inter)
         return y
 
     return dict(e4m3_decode=e4m3_decode, e4m3_encode=e4m3_encode,
                 quantize_rows_e4m3=quantize_rows_e4m3,
                 dequantize_rows_e4m3=dequantize_rows_e4m3, bf16_round=bf16_round,
-                forward_fp8=forward_fp8)
+                ffn_combine_fp8=ffn_combine_fp8, forward_fp8=forward_fp8)
 
 
 for _n, _fn in _fp8_methods().items():

@@ -105,3 +105,35 @@ def test_output_sample(run, oracle):
         ref.append(y[0])
         got.append(run["y"][t])
     assert_close(np.stack(got), np.stack(ref), f"{cfg.name} sampled y")
+
+
+def test_fp8_output_sample(run, oracle):
+    """The E4M3-weight layer (moe_forward_fp8) at full size: sampled tokens
+    recomputed alone by the oracle's FP8 experts and combine, with its routing
+    and only the token's experts' weights, quantized by the oracle itself."""
+    cfg, d = run["cfg"], run["d"]
+    if cfg.dtype != "bf16":
+        pytest.skip("E4M3 weights come with bf16 activations")
+    layer = m.MoELayerFP8(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k,
+                          router_bias=d["router_bias"], Ws_gate=d["Ws_gate"], Ws_up=d["Ws_up"],
+                          Ws_down=d["Ws_down"], renorm=cfg.renorm)
+    y32 = layer(d["x"], out_f32=True).cpu().numpy()
+    torch.cuda.synchronize()
+    assert m.get_device_status(layer.workspace(cfg.T)) == m.MOE_OK
+    n = 4 if cfg.T >= 4 else cfg.T
+    toks = np.unique(np.linspace(0, cfg.T - 1, n).astype(np.int64))
+    got, ref = [], []
+    for t in toks:
+        xt = to_np(d["x"][t:t + 1])
+        lg = oracle.router_logits(xt, to_np(d["W_router"]), to_np(d["router_bias"]))
+        ids, w = oracle.route(lg, cfg.k, cfg.renorm)
+        sel = torch.from_numpy(ids[0].astype(np.int64)).to(DEV)
+        local = np.arange(cfg.k, dtype=np.int32).reshape(1, cfg.k)
+        y = oracle.ffn_combine_fp8(xt, local, w, to_np(d["W_gate"][sel]), to_np(d["W_up"][sel]),
+                                   to_np(d["W_down"][sel]), to_np(d["Ws_gate"]),
+                                   to_np(d["Ws_up"]), to_np(d["Ws_down"]))
+        ref.append(y[0])
+        got.append(y32[t])
+    del layer
+    torch.cuda.empty_cache()
+    assert_close(np.stack(got), np.stack(ref), f"{cfg.name} sampled fp8 y")
