@@ -384,6 +384,58 @@ def test_forward_grouped_routing_vs_oracle(oracle, T, dtype):
     assert_close(y32.cpu().numpy(), ref, "y")
 
 
+def _forward_vs_oracle(oracle, cfg, d, **layer_kw):
+    """moe_forward against the oracle: the oracle routes the logits the forward
+    pass stored (ids then match bit for bit, even where inputs without a
+    routing margin leave near ties), and y is the oracle's experts and combine
+    on those ids."""
+    layer = m.MoELayer(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k,
+                       router_bias=d["router_bias"], Ws_gate=d["Ws_gate"], Ws_up=d["Ws_up"],
+                       Ws_down=d["Ws_down"], renorm=cfg.renorm, **layer_kw)
+    y32 = layer(d["x"], out_f32=True)
+    ws = layer.workspace(cfg.T)
+    finish(ws)
+    T, E, k = cfg.T, cfg.E, cfg.k
+    lay = m.workspace_layout(layer.problem(T))
+    logits = ws[lay["logits"]:lay["logits"] + T * E * 4].view(torch.float32).view(T, E)
+    gids = ws[lay["topk_ids"]:lay["topk_ids"] + T * k * 4].view(torch.int32).view(T, k)
+    rid, rw = oracle.route(logits.cpu().numpy(), k, cfg.renorm)
+    np.testing.assert_array_equal(gids.cpu().numpy(), rid)
+    n = {kk: to_np(v) for kk, v in d.items()}
+    ref = oracle.ffn_combine(n["x"], rid, rw, n["W_gate"], n["W_up"], n["W_down"], n["Ws_gate"],
+                             n["Ws_up"], n["Ws_down"])
+    assert_close(y32.cpu().numpy(), ref, "y")
+
+
+def test_forward_most_experts_and_top32(oracle):
+    """E = 1024 (the largest expert count), k = 32 (the largest top-k): most
+    experts hold a handful of rows, many none."""
+    cfg = MoEConfig("wide", T=256, H=256, E=1024, k=32, I=128, I_shared=128)
+    _forward_vs_oracle(oracle, cfg, generate(cfg, seed=21, device=DEV))
+
+
+@pytest.mark.parametrize("tile", TILES, ids=TILE_IDS)
+def test_forward_one_expert_takes_every_token(oracle, tile):
+    """A router bias sends every token's first choice to expert 0: one group of
+    T rows (many token tiles) next to small ones."""
+    cfg = MoEConfig("dominant", T=1000, H=256, E=16, k=2, I=128)
+    d = generate(cfg, seed=22, device=DEV, enforce_margin=False)
+    bias = torch.zeros(cfg.E, dtype=torch.float32, device=DEV)
+    bias[0] = 50.0
+    d["router_bias"] = bias
+    _forward_vs_oracle(oracle, cfg, d, tile=tile)
+
+
+def test_forward_empty_batch_touches_nothing():
+    cfg = MoEConfig("empty", T=8, H=256, E=8, k=2, I=128)
+    d = generate(cfg, seed=23, device=DEV)
+    layer = m.MoELayer(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k)
+    x0 = d["x"][:0]
+    y0 = torch.full((0, cfg.H), 7.0, dtype=cfg.torch_dtype, device=DEV)
+    assert layer(x0, out=y0) is y0
+    torch.cuda.synchronize()
+
+
 def test_forward_is_bitwise_reproducible():
     cfg = MoEConfig("r", T=300, H=256, E=16, k=4, I=128, I_shared=64)
     d = generate(cfg, seed=5, device=DEV)
