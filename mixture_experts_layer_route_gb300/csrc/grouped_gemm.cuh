@@ -146,6 +146,23 @@ struct Tile {
   int n_valid;  // rows of this tile
 };
 
+// Position i of the round-robin deal -> unit of the class-ordered list, whose
+// first uh units belong to groups of more than 128 rows (tensor-bound tiles)
+// and the rest to lighter groups (weight-streaming tiles). The heavy units are
+// spread evenly over the first 7/8 of the positions (unit j at position
+// floor(j * S / uh)) and the light units fill the other positions in order, so
+// that SMs computing heavy tiles run beside SMs streaming light experts'
+// weights, and the last positions hold short light units. A bijection.
+__device__ __forceinline__ int remap_unit(int i, int total, int uh) {
+  if (uh <= 0 || uh >= total) return i;
+  int64_t S = (int64_t)total * 7 / 8;
+  if (S < uh) S = uh;
+  if (i >= S) return i;  // every heavy unit sits below S
+  const int64_t j = ((int64_t)i * uh + S - 1) / S;  // heavy positions below i
+  if (j < uh && j * S / uh == i) return (int)j;
+  return uh + (i - (int)j);
+}
+
 // Unit u of the schedule: the scheduled groups are listed in `order` (heaviest
 // first), `prefix[i]` = units of order[0..i); a group's units run feature block
 // by feature block, token tile fastest, so consecutive units share weights.
@@ -188,6 +205,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* epi_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* n_sched = reinterpret_cast<int*>(tmem_holder + 2);
+  int* n_heavy = reinterpret_cast<int*>(tmem_holder + 3);  // units of groups > 128 rows
   int32_t* prefix = reinterpret_cast<int32_t*>(tmem_holder + 4);
   int32_t* offs = prefix + (args.E + 2);
   int32_t* order = offs + (args.E + 2);
@@ -303,6 +321,8 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       prefix[ng] = incl;
       *n_sched = ng;
     }
+    __syncwarp();
+    if (lane == 0) *n_heavy = prefix[t0 + t1];
   }
   tc_fence_before();
   __syncthreads();
@@ -310,6 +330,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int ngroups = *n_sched;
+  const int heavy_units = *n_heavy;
   const int total = prefix[ngroups];
   const uint64_t limit = args.limit_ns;
 
@@ -324,7 +345,8 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     bool ok = true;
     bool skip_once = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
     for (int u = cid; u < total && ok; u += ncl) {
-      Tile tl = decode_tile(u, prefix, order, offs, ngroups, args.tile_n);
+      Tile tl = decode_tile(remap_unit(u, total, heavy_units), prefix, order, offs, ngroups,
+                            args.tile_n);
       tl.nb = tl.nb * CL + crank;
       const bool shared = tl.g == E;
       const int kdim = shared ? args.kdim_shared : args.kdim_routed;
@@ -438,7 +460,8 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       constexpr uint32_t fmt = UmmaOf<TIn>::fmt;
       bool ok = true;
       for (int u = cid; u < total && ok; u += ncl, ++lt) {
-        Tile tl = decode_tile(u, prefix, order, offs, ngroups, args.tile_n);
+        Tile tl = decode_tile(remap_unit(u, total, heavy_units), prefix, order, offs, ngroups,
+                            args.tile_n);
         const int kdim = (tl.g == E) ? args.kdim_shared : args.kdim_routed;
         const uint32_t acc = lt & 1u, around = lt >> 1;
         if (!mbar_wait(tempty_bar(acc), (around & 1u) ^ 1u, args.status, limit)) break;
@@ -492,7 +515,8 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t lt = 0;
     for (int u = cid; u < total; u += ncl, ++lt) {
-      Tile tl = decode_tile(u, prefix, order, offs, ngroups, args.tile_n);
+      Tile tl = decode_tile(remap_unit(u, total, heavy_units), prefix, order, offs, ngroups,
+                            args.tile_n);
       tl.nb = tl.nb * CL + crank;
       const bool shared = tl.g == E;
       const uint32_t acc = lt & 1u, around = lt >> 1;
