@@ -200,7 +200,7 @@ def stage_sequence(layer, d, T, ws, lay, stream):
                                 stream),
         lambda: m.route(logits, k, layer.renorm, ids, w, stream),
         lambda: m.permute(ids, E, 1 if layer.I_shared else 0, offs, gidx, spos, ws, stream),
-        lambda: m.grouped_swiglu_gemm(pb, d["x"], offs, gidx, layer.W_gate, layer.W_up,
+        lambda: m.grouped_swiglu_gemm(pb, d["x"], offs, gidx, spos, layer.W_gate, layer.W_up,
                                       layer.Ws_gate, layer.Ws_up, h, hs, ws, stream),
         lambda: m.down_combine(pb, h, hs, offs, gidx, w, layer.W_down, layer.Ws_down, y, ws,
                                stream),

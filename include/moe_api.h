@@ -156,7 +156,8 @@ moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
                        void* stream);
 
 /* Step a4, grouped gate/up GEMM with fused SwiGLU (DeepSeek page "GroupGEMM";
- * Qwen3.5/TPU write-up 4.2.1-4.2.2). For every routed position p of expert e
+ * Qwen3.5/TPU write-up 4.2.1-4.2.2). expert_offsets, gather_idx and slot_pos
+ * are moe_permute's outputs. For every routed position p of expert e
  * (token t = gather_idx[p] / k):
  *   h[p][i] = silu(x[t] . W_gate[e][i]) * (x[t] . W_up[e][i])
  * and, when I_shared > 0, h_shared[t][i] likewise with Ws_gate, Ws_up.
@@ -168,9 +169,10 @@ moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
  * fp32 accumulation, one rounding to the dtype. */
 moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
                                    const int32_t* expert_offsets, const int32_t* gather_idx,
-                                   const void* W_gate, const void* W_up, const void* Ws_gate,
-                                   const void* Ws_up, void* h, void* h_shared,
-                                   void* workspace, size_t workspace_bytes, void* stream);
+                                   const int32_t* slot_pos, const void* W_gate, const void* W_up,
+                                   const void* Ws_gate, const void* Ws_up, void* h,
+                                   void* h_shared, void* workspace, size_t workspace_bytes,
+                                   void* stream);
 
 /* Step a5 (+a6), down projection and gate-weighted combine (DeepSeek page
  * "Expert Parallelism": weighted sum of the routed outputs plus the shared

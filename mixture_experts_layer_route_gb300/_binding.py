@@ -76,7 +76,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_route_grouped": [_P, _I64, _I64, _I64, ctypes.c_int, _I64, _I64, _P, _P, _P],
             "moe_permute": [_P, _I64, _I64, _I64, ctypes.c_int, _P, _P, _P, _P, ctypes.c_size_t,
                             _P],
-            "moe_grouped_swiglu_gemm": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+            "moe_grouped_swiglu_gemm": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         ctypes.c_size_t, _P],
             "moe_down_combine": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_forward": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -172,12 +172,12 @@ def permute(topk_ids, E, has_shared, expert_offsets, gather_idx, slot_pos, works
         _stream(stream)))
 
 
-def grouped_swiglu_gemm(problem, x, expert_offsets, gather_idx, W_gate, W_up, Ws_gate, Ws_up,
-                        h, h_shared, workspace, stream=None):
+def grouped_swiglu_gemm(problem, x, expert_offsets, gather_idx, slot_pos, W_gate, W_up, Ws_gate,
+                        Ws_up, h, h_shared, workspace, stream=None):
     _check("moe_grouped_swiglu_gemm", load_library().moe_grouped_swiglu_gemm(
-        ctypes.byref(problem), _ptr(x), _ptr(expert_offsets), _ptr(gather_idx), _ptr(W_gate),
-        _ptr(W_up), _ptr(Ws_gate), _ptr(Ws_up), _ptr(h), _ptr(h_shared), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        ctypes.byref(problem), _ptr(x), _ptr(expert_offsets), _ptr(gather_idx), _ptr(slot_pos),
+        _ptr(W_gate), _ptr(W_up), _ptr(Ws_gate), _ptr(Ws_up), _ptr(h), _ptr(h_shared),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def down_combine(problem, h, h_shared, expert_offsets, gather_idx, topk_w, W_down, Ws_down, y,

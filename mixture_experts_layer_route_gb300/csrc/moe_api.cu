@@ -282,18 +282,20 @@ moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
 
 moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
                                    const int32_t* expert_offsets, const int32_t* gather_idx,
-                                   const void* W_gate, const void* W_up, const void* Ws_gate,
-                                   const void* Ws_up, void* h, void* h_shared,
-                                   void* workspace, size_t workspace_bytes, void* stream) {
+                                   const int32_t* slot_pos, const void* W_gate, const void* W_up,
+                                   const void* Ws_gate, const void* Ws_up, void* h,
+                                   void* h_shared, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
   moe_status s = check_problem(pb);
   if (s != MOE_OK) return s;
   if (pb->T == 0) return MOE_OK;
   const bool has_s = pb->I_shared > 0;
-  if (!x || !expert_offsets || !gather_idx || !W_gate || !W_up || !h) return MOE_ERR_INVALID_ARG;
+  if (!x || !expert_offsets || !gather_idx || !slot_pos || !W_gate || !W_up || !h)
+    return MOE_ERR_INVALID_ARG;
   if (has_s != (Ws_gate != nullptr) || has_s != (Ws_up != nullptr) ||
       has_s != (h_shared != nullptr))
     return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, expert_offsets, gather_idx, W_gate, W_up, h};
+  const void* ptrs[] = {x, expert_offsets, gather_idx, slot_pos, W_gate, W_up, h};
   for (const void* q : ptrs)
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
   if (has_s && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(h_shared)))
@@ -307,7 +309,7 @@ moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
   cudaError_t e = cudaSuccess;
   if (gemm_needs_expert_order_copy(g)) {
     xg = at<void>(workspace, L.xg);
-    e = launch_gather_rows(x, gather_idx, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
+    e = launch_gather_rows(x, slot_pos, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
                            g.num_sms, st);
   }
   if (e == cudaSuccess)
@@ -395,7 +397,7 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
   void* xg = nullptr;
   if (e == cudaSuccess && gemm_needs_expert_order_copy(g)) {
     xg = at<void>(workspace, L.xg);
-    e = launch_gather_rows(x, gidx, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
+    e = launch_gather_rows(x, spos, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
                            g.num_sms, st);
   }
   if (e == cudaSuccess)
@@ -485,7 +487,7 @@ moe_status moe_forward_fp8(const moe_problem* pb, const void* x, const void* W_r
   void* xg = nullptr;
   if (e == cudaSuccess && gemm_needs_expert_order_copy(g)) {
     xg = at<void>(workspace, L.xg);
-    e = launch_gather_rows(xq, gidx, g.T * g.k, g.k, (size_t)g.H, xg, g.num_sms, st);
+    e = launch_gather_rows(xq, spos, g.T * g.k, g.k, (size_t)g.H, xg, g.num_sms, st);
   }
   GemmScales sg = {{s_gate, s_up, ss_gate, ss_up}, {sx, sx}};
   if (e == cudaSuccess)

@@ -191,21 +191,27 @@ __global__ void __launch_bounds__(PM_THREADS, 1)
 }
 
 // Dispatch copy ("CuTeDSL at Perplexity", "Local": tokens are copied into
-// buffers, optionally padded, for the MoE GEMM; here unpadded): row p of xg
-// is x[gather_idx[p] / k], so every expert's rows are contiguous and the
-// grouped GEMM reads them as one TMA box per stage. One warp per row, 16-byte
-// vectors; grid sized to a multiple of the SM count.
+// buffers, optionally padded, for the MoE GEMM; here unpadded): row
+// slot_pos[s] of xg is x[s / k], so every expert's rows are contiguous and the
+// grouped GEMM reads them as one TMA box per stage. One warp per slot, in slot
+// order: the k warps that copy one token's row run together and read it from
+// L2 (x is read from DRAM once), while each writes a whole row. (In position
+// order, the 8x larger stream of written rows evicted x from L2 between
+// re-reads: 0.136 against 0.097 ms for the 8192-token prefill batch.) Slots
+// with slot_pos < 0 (out-of-range ids) have no row. 16-byte vectors, 4 KB per
+// warp in flight; streaming stores.
 template <int VB>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
-                                                          const int32_t* __restrict__ gather_idx,
+                                                          const int32_t* __restrict__ slot_pos,
                                                           int P, int k, int vecs_per_row,
                                                           uint4* __restrict__ xg) {
   pdl_entry();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < P; p += warps) {
-    const int t = gather_idx[p] / k;
-    const uint4* src = x + (size_t)t * vecs_per_row;
+  for (int s = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < P; s += warps) {
+    const int p = slot_pos[s];
+    if (p < 0) continue;
+    const uint4* src = x + (size_t)(s / k) * vecs_per_row;
     uint4* dst = xg + (size_t)p * vecs_per_row;
     for (int v = lane; v < vecs_per_row; v += 32 * VB) {
       uint4 r[VB];
@@ -214,21 +220,21 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
         if (v + 32 * j < vecs_per_row) r[j] = __ldg(src + v + 32 * j);
 #pragma unroll
       for (int j = 0; j < VB; ++j)
-        if (v + 32 * j < vecs_per_row) dst[v + 32 * j] = r[j];
+        if (v + 32 * j < vecs_per_row) __stcs(dst + v + 32 * j, r[j]);
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_gather_rows(const void* x, const int32_t* gather_idx, int P, int k,
+cudaError_t launch_gather_rows(const void* x, const int32_t* slot_pos, int P, int k,
                                size_t row_bytes, void* xg, int num_sms, cudaStream_t st) {
   if (P == 0) return cudaSuccess;
   const int vpr = (int)(row_bytes / 16);
   int blocks = (P + 7) / 8;
-  if (blocks > 8 * num_sms) blocks = 8 * num_sms;
-  return launch_chained(gather_rows_kernel<4>, dim3(blocks), dim3(256), 0, st, 1,
-                        reinterpret_cast<const uint4*>(x), gather_idx, P, k, vpr,
+  if (blocks > 16 * num_sms) blocks = 16 * num_sms;
+  return launch_chained(gather_rows_kernel<8>, dim3(blocks), dim3(256), 0, st, 1,
+                        reinterpret_cast<const uint4*>(x), slot_pos, P, k, vpr,
                         reinterpret_cast<uint4*>(xg));
 }
 

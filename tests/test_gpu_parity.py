@@ -265,15 +265,15 @@ def _gemm_case(case, dtype):
 def test_grouped_swiglu_gemm(oracle, case, dtype, tile):
     cfg, d, ids, _ = _gemm_case(case, dtype)
     T, k, E = cfg.T, cfg.k, cfg.E
-    offs, gidx, _ = oracle.permute(ids, E, 1 if cfg.I_shared else 0)
+    offs, gidx, spos = oracle.permute(ids, E, 1 if cfg.I_shared else 0)
     pb = m.make_problem(T, cfg.H, E, k, cfg.I, cfg.I_shared, dtype=dtype, tile=tile)
     ws = ws_for(pb)
     h = torch.full((T * k, cfg.I), float("nan"), dtype=cfg.torch_dtype, device=DEV)
     hs = (torch.full((T, cfg.I_shared), float("nan"), dtype=cfg.torch_dtype, device=DEV)
           if cfg.I_shared else None)
     m.grouped_swiglu_gemm(pb, d["x"], torch.from_numpy(offs).to(DEV),
-                          torch.from_numpy(gidx).to(DEV), d["W_gate"], d["W_up"], d["Ws_gate"],
-                          d["Ws_up"], h, hs, ws)
+                          torch.from_numpy(gidx).to(DEV), torch.from_numpy(spos).to(DEV),
+                          d["W_gate"], d["W_up"], d["Ws_gate"], d["Ws_up"], h, hs, ws)
     finish(ws)
     n = {kk: to_np(v) for kk, v in d.items()}
     rh, rhs = oracle.expert_h(n["x"], offs, gidx, n["W_gate"], n["W_up"], k, n["Ws_gate"],
