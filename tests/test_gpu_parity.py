@@ -18,6 +18,8 @@ as tf32, which keeps 10 mantissa bits by truncation: each product can be off by
 2^-9 relative, so a sum of H of them deviates by ~2^-9 rms(sum) per element
 with tails several times that, and a = 1e-2 for fp32. rel-L2 <= 5e-3 always.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -42,6 +44,11 @@ def assert_close(got, ref, what="", stage=False, tf32=False):
     rms = float(np.sqrt(np.mean(ref ** 2)))
     d = np.abs(got - ref)
     l2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+    log = os.environ.get("MOE_TEST_ERRLOG")
+    if log and not stage:
+        with open(log, "a") as f:
+            test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+            f.write(f"{test}\t{what}\t{float(d.max()) / max(rms, 1e-30):.5f}\t{l2:.3e}\n")
     if stage:
         bound = 2.0 ** -8 * np.abs(ref) + (1e-2 if tf32 else 2e-3) * rms
         worst = int(np.argmax(d - bound))
