@@ -167,6 +167,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                : "memory");
 }
 
+// Relaxed arrives, for barriers that order no global or shared memory: a
+// release arrive makes the thread wait until its earlier global stores are
+// visible at the barrier's scope, which a signal that only hands back tensor
+// memory (already read, tcgen05.wait::ld) does not need.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
 // 2-D tiled load into this CTA's shared memory whose completion bytes are
 // signalled on an mbarrier of either CTA of the pair (`bar_cluster` is a
 // shared::cluster address): the pair's loads all count on the leader's barrier.

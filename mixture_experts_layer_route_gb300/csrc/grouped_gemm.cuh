@@ -658,11 +658,15 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         tc_fence_before();
         named_barrier_sync(1, 128);
       }
+      // The accumulator goes back to the MMA issuer. Its tensor-memory reads
+      // completed (tcgen05.wait::ld) before the fence and barrier above; the
+      // arrive is relaxed because it orders no memory: the tile's global stores
+      // are read only by later kernels.
       if (et == 0) {
         if constexpr (PAIR)
-          mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+          mbar_arrive_relaxed_cluster(mapa_shared(tempty_bar(acc), 0));
         else
-          mbar_arrive(tempty_bar(acc));
+          mbar_arrive_relaxed(tempty_bar(acc));
       }
     }
   }
