@@ -118,7 +118,14 @@ struct GemmCfg {
   // Epilogue staging: GATED, the 128 x 32 accumulator chunk (gate and up rows
   // meet in one thread); DOWN, per-token row index and gate weight.
   static constexpr int EPI_FLOATS = GATED ? 128 * 33 + (F8 ? BN : 0) : 2 * BN;
-  static constexpr int THREADS = 192;
+  // Epilogue warps: 4, one per TMEM lane quarter; E4M3 DOWN, 8 (two per
+  // quarter taking alternate 32-column chunks). With 1-byte operands a down
+  // tile has half the k-blocks (K = I), and its stores (128 features x up to
+  // 256 fp32 columns per CTA) would set the pace with one warp per quarter:
+  // E4M3 prefill layer -3.4%, bf16 layers unchanged or slower by < 1%.
+  static constexpr int EPI_WARPS = (!GATED && F8) ? 8 : 4;
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS;
   static_assert(CL == 1 || (CL == 2 && BMODE == kTiled && BN >= 64),
                 "CTA pairs split tiled token boxes of >= 64 rows");
   // Pair MMAs round N up to 32 (each CTA's half a multiple of 16 rows).
@@ -511,7 +518,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int et = threadIdx.x - 64;        // 0..127
+    const int et = threadIdx.x - 64;        // 0..EPI_THREADS-1
+    const int half = (warp - 2) >> 2;       // DOWN: which of a quarter's warps
+    constexpr int NH = C::EPI_WARPS / 4;    // warps per TMEM lane quarter
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t lt = 0;
     for (int u = cid; u < total; u += ncl, ++lt) {
@@ -525,7 +534,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         // Per-token destination row in Y and gate weight of this tile.
         int32_t* yrow = reinterpret_cast<int32_t*>(epi);
         float* wt = epi + BN;
-        for (int j = et; j < tl.n_valid; j += 128) {
+        for (int j = et; j < tl.n_valid; j += C::EPI_THREADS) {
           int row;
           float wv;
           if (shared) {
@@ -546,12 +555,12 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       } else if constexpr (C::F8) {
         // Scale of each column's token row (x quantized per token).
         float* cs = epi + 128 * 33;
-        for (int j = et; j < tl.n_valid; j += 128) {
+        for (int j = et; j < tl.n_valid; j += C::EPI_THREADS) {
           const int t = shared ? tl.p0 - offs[E] + j : args.gather_idx[tl.p0 + j] / args.k;
           cs[j] = args.sB[0][t];
         }
       }
-      named_barrier_sync(1, 128);
+      named_barrier_sync(1, C::EPI_THREADS);
       if (!*epi_flag) break;  // every epilogue thread sees the same flag
       tc_fence_after();
       const uint32_t t_acc = tmem_base + lane_base + acc * BN;
@@ -581,7 +590,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
             else
               epi[(q * 32 + lane) * 33 + i] = v[i];
           }
-          named_barrier_sync(1, 128);
+          named_barrier_sync(1, C::EPI_THREADS);
           const int j = c0 + jj;
           if (j < tl.n_valid) {
             float hv[16];
@@ -612,7 +621,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
             }
           }
           tc_fence_before();
-          named_barrier_sync(1, 128);
+          named_barrier_sync(1, C::EPI_THREADS);
         }
       } else {
         // Thread = output feature c (its TMEM lane); for each token column a
@@ -630,7 +639,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         if constexpr (C::F8)
           rs = args.sA[shared ? 2 : 0][(shared ? 0 : (size_t)tl.g * H) + tl.nb * 128 + q * 32 +
                                        lane];
-        for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+        for (int c0 = 32 * half; c0 < tl.n_valid; c0 += 32 * NH) {
           float v[32];
           tmem_ld32(t_acc + c0, v);
           if constexpr (C::F8) {
@@ -656,7 +665,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
           }
         }
         tc_fence_before();
-        named_barrier_sync(1, 128);
+        named_barrier_sync(1, C::EPI_THREADS);
       }
       // The accumulator goes back to the MMA issuer. Its tensor-memory reads
       // completed (tcgen05.wait::ld) before the fence and barrier above; the
