@@ -104,10 +104,6 @@ typedef struct {
                         moe_route_grouped); E % n_group == 0, n_group <= 32 */
   int32_t topk_group; /* groups kept per token when n_group > 1: 1 <= topk_group <=
                          n_group and k <= topk_group * (E / n_group) */
-  int32_t weights_tiled; /* 1: the expert weights (W_gate, W_up, W_down and the shared
-                            expert's, or their E4M3 codes) are packed by
-                            moe_pack_weights; 0: row-major as documented below.
-                            W_router is always row-major. */
 } moe_problem;
 
 /* Bytes of workspace every call below needs for problem `pb`. */
@@ -233,23 +229,6 @@ typedef struct {
   int64_t logits, topk_ids, topk_w, expert_offsets, gather_idx, slot_pos, h, h_shared;
 } moe_workspace_layout;
 moe_status moe_get_workspace_layout(const moe_problem* pb, moe_workspace_layout* out);
-
-/* Weight packing (a layout for streaming, no arithmetic). A row-major matrix
- * src [rows][cols] of dtype (MOE_DTYPE_BF16, MOE_DTYPE_F32, or MOE_DTYPE_E4M3
- * for 1-byte codes) is rewritten into dst as tiles of 64 rows x 128 bytes:
- * tile (rb, kb) holds rows 64*rb .. 64*rb+63, bytes 128*kb .. 128*kb+127 of
- * each row, row after row, and starts at byte ((rb * (cols*es/128)) + kb) *
- * 8192 of dst. The grouped GEMMs then read the weights of one k-step of a
- * 64-row block as one contiguous 8 KB tile instead of 64 pieces of 128 bytes
- * a row apart; measured layer effect: 2-5% faster at 1K+ tokens per call
- * (prefill, DeepSeek-V3- and Zipf-shaped layers), ~1% slower on decode steps
- * of a few tokens per expert. Pack each expert weight array as one matrix:
- * W_gate and W_up as [E*I][H], W_down as [E*H][I], the shared expert's
- * [I_s][H], [I_s][H], [H][I_s]; then set moe_problem.weights_tiled = 1. Requires rows % 64 == 0 and
- * cols * es % 128 == 0 (es = element bytes); src and dst are device pointers,
- * 16-byte aligned, not overlapping, rows*cols*es bytes each. */
-moe_status moe_pack_weights(const void* src, int32_t dtype, int64_t rows, int64_t cols, void* dst,
-                            void* stream);
 
 /* FP8 expert weights ("Hosting Qwen on Blackwell": Qwen3-235B served with FP8
  * microscaled weights converted statically). A matrix is stored as E4M3 codes

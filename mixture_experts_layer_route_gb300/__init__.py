@@ -15,8 +15,7 @@ from ._binding import (  # noqa: F401
     EXPORTED, MOE_DTYPE_BF16, MOE_DTYPE_E4M3, MOE_DTYPE_F32, MOE_FLAG_TEST_SKIP_SIGNAL, MOE_OK,
     MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_MEDIUM, MOE_TILE_PREFILL, STATUS_NAMES, MoEError, MoEProblem,
     down_combine, down_combine_noalloc, forward, forward_fp8, get_device_status, grouped_swiglu_gemm, load_library, make_problem,
-    pack_weights, permute, quantize_rows_e4m3, reset_device_status, route, route_grouped,
-    router_logits,
+    permute, quantize_rows_e4m3, reset_device_status, route, route_grouped, router_logits,
     status_string, workspace_layout,
     workspace_size)
 
@@ -28,22 +27,15 @@ class MoELayer:
     W_router [E,H], W_gate/W_up [E,I,H], W_down [E,H,I], optional router_bias
     fp32 [E] and shared expert Ws_gate/Ws_up [Is,H], Ws_down [H,Is].
     n_group > 1 limits each token's experts to its topk_group best groups of
-    E / n_group consecutive experts (moe_route_grouped). tiled=True keeps
-    copies of the expert weights packed by moe_pack_weights (64-row x 128-byte
-    tiles): 2-5% faster layers at 1K+ tokens per call, ~1% slower decode steps
-    of a few tokens per expert; tiled=False (default) uses the tensors in place.
+    E / n_group consecutive experts (moe_route_grouped).
     """
 
     def __init__(self, W_router, W_gate, W_up, W_down, k, router_bias=None, Ws_gate=None,
                  Ws_up=None, Ws_down=None, renorm=1, tile=MOE_TILE_AUTO, n_group=1,
-                 topk_group=1, tiled=False):
-        self.tiled = bool(tiled)
-        p = pack_weights if self.tiled else (lambda w: w)
-        self.W_router = W_router
-        self.W_gate, self.W_up, self.W_down = p(W_gate), p(W_up), p(W_down)
+                 topk_group=1):
+        self.W_router, self.W_gate, self.W_up, self.W_down = W_router, W_gate, W_up, W_down
         self.router_bias = router_bias
-        self.Ws_gate, self.Ws_up, self.Ws_down = (None if w is None else p(w)
-                                                  for w in (Ws_gate, Ws_up, Ws_down))
+        self.Ws_gate, self.Ws_up, self.Ws_down = Ws_gate, Ws_up, Ws_down
         self.E, self.I, self.H = W_gate.shape
         self.I_shared = 0 if Ws_gate is None else Ws_gate.shape[0]
         self.k, self.renorm, self.tile = k, renorm, tile
@@ -55,7 +47,7 @@ class MoELayer:
                 out_f32: bool = False) -> MoEProblem:
         return make_problem(T, self.H, self.E, self.k, self.I, self.I_shared, self.renorm,
                             "bf16" if self.dtype == torch.bfloat16 else "f32", self.tile, flags,
-                            wait_limit_us, out_f32, self.n_group, self.topk_group, self.tiled)
+                            wait_limit_us, out_f32, self.n_group, self.topk_group)
 
     def workspace(self, T: int) -> torch.Tensor:
         ws = self._ws.get(T)
@@ -92,27 +84,21 @@ def quantize_e4m3(W: torch.Tensor):
 class MoELayerFP8:
     """The layer with E4M3 expert weights (moe_forward_fp8). Takes the same bf16
     weights as MoELayer and quantizes the expert matrices once, row by row, on
-    the GPU; x, W_router and y stay bf16. tiled=True: the codes are then packed
-    by moe_pack_weights, as in MoELayer."""
+    the GPU; x, W_router and y stay bf16."""
 
     def __init__(self, W_router, W_gate, W_up, W_down, k, router_bias=None, Ws_gate=None,
                  Ws_up=None, Ws_down=None, renorm=1, tile=MOE_TILE_AUTO, n_group=1,
-                 topk_group=1, tiled=False):
+                 topk_group=1):
         self.W_router, self.router_bias = W_router, router_bias
         self.E, self.I, self.H = W_gate.shape
         self.I_shared = 0 if Ws_gate is None else Ws_gate.shape[0]
         self.k, self.renorm, self.tile = k, renorm, tile
         self.n_group, self.topk_group = n_group, topk_group
-        self.tiled = bool(tiled)
         self.dtype = torch.bfloat16  # activations (x, y)
-
-        def q(W):
-            codes, scales = quantize_e4m3(W)
-            return (pack_weights(codes) if self.tiled else codes), scales
-
-        self.gate, self.up, self.down = (q(W) for W in (W_gate, W_up, W_down))
+        self.gate, self.up, self.down = (quantize_e4m3(W) for W in (W_gate, W_up, W_down))
         if self.I_shared:
-            self.s_gate, self.s_up, self.s_down = (q(W) for W in (Ws_gate, Ws_up, Ws_down))
+            self.s_gate, self.s_up, self.s_down = (quantize_e4m3(W) for W in (Ws_gate, Ws_up,
+                                                                             Ws_down))
         else:
             self.s_gate = self.s_up = self.s_down = (None, None)
         self._ws = {}
@@ -121,7 +107,7 @@ class MoELayerFP8:
                 out_f32: bool = False) -> MoEProblem:
         return make_problem(T, self.H, self.E, self.k, self.I, self.I_shared, self.renorm,
                             "e4m3", self.tile, flags, wait_limit_us, out_f32, self.n_group,
-                            self.topk_group, self.tiled)
+                            self.topk_group)
 
     def workspace(self, T: int) -> torch.Tensor:
         ws = self._ws.get(T)

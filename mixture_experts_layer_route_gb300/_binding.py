@@ -28,7 +28,7 @@ EXPORTED = ("moe_workspace_size", "moe_router_logits", "moe_route", "moe_route_g
             "moe_grouped_swiglu_gemm", "moe_down_combine", "moe_forward",
             "moe_get_workspace_layout", "moe_get_device_status", "moe_reset_device_status",
             "moe_status_string", "moe_down_combine_noalloc", "moe_quantize_rows_e4m3",
-            "moe_forward_fp8", "moe_pack_weights")
+            "moe_forward_fp8")
 
 
 class MoEError(RuntimeError):
@@ -43,7 +43,7 @@ class MoEProblem(ctypes.Structure):
                 ("renorm", ctypes.c_int32), ("dtype", ctypes.c_int32), ("tile", ctypes.c_int32),
                 ("flags", ctypes.c_uint32), ("wait_limit_us", ctypes.c_uint32),
                 ("out_f32", ctypes.c_int32), ("n_group", ctypes.c_int32),
-                ("topk_group", ctypes.c_int32), ("weights_tiled", ctypes.c_int32)]
+                ("topk_group", ctypes.c_int32)]
 
 
 class MoEWorkspaceLayout(ctypes.Structure):
@@ -84,7 +84,6 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_get_device_status": [_P, _P, ctypes.POINTER(ctypes.c_int)],
             "moe_reset_device_status": [_P, _P],
             "moe_quantize_rows_e4m3": [_P, ctypes.c_int32, _I64, _I64, _P, _P, _P],
-            "moe_pack_weights": [_P, ctypes.c_int32, _I64, _I64, _P, _P],
             "moe_forward_fp8": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                 _P, _P, ctypes.c_size_t, _P],
             "moe_down_combine_noalloc": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -124,11 +123,11 @@ def _check(name: str, code: int):
 
 def make_problem(T, H, E, k, I, I_shared=0, renorm=1, dtype="bf16", tile=MOE_TILE_AUTO,
                  flags=0, wait_limit_us=0, out_f32=False, n_group=1,
-                 topk_group=1, weights_tiled=False) -> MoEProblem:
+                 topk_group=1) -> MoEProblem:
     dt = (MOE_DTYPE_BF16 if dtype in ("bf16", torch.bfloat16)
           else MOE_DTYPE_E4M3 if dtype == "e4m3" else MOE_DTYPE_F32)
     return MoEProblem(T, H, E, k, I, I_shared, renorm, dt, tile, flags, wait_limit_us,
-                      1 if out_f32 else 0, n_group, topk_group, 1 if weights_tiled else 0)
+                      1 if out_f32 else 0, n_group, topk_group)
 
 
 def workspace_size(problem: MoEProblem) -> int:
@@ -199,21 +198,6 @@ def down_combine_noalloc(problem, h, h_shared, expert_offsets, gather_idx, topk_
         _ptr(topk_w), _ptr(W_down), _ptr(Ws_down), _ptr(y), _stream(stream),
         ctypes.byref(st) if want_status else None))
     return int(st.value) if want_status else None
-
-
-def pack_weights(src, dst=None, stream=None):
-    """src (bf16, fp32, or uint8 E4M3 codes), viewed as rows of its last
-    dimension, packed by moe_pack_weights into dst (a new tensor of src's shape
-    and dtype unless given; its bytes are in the tiled layout)."""
-    cols = src.shape[-1]
-    rows = src.numel() // cols
-    dt = {torch.bfloat16: MOE_DTYPE_BF16, torch.float32: MOE_DTYPE_F32,
-          torch.uint8: MOE_DTYPE_E4M3}[src.dtype]
-    if dst is None:
-        dst = torch.empty_like(src)
-    _check("moe_pack_weights", load_library().moe_pack_weights(
-        _ptr(src), dt, rows, cols, _ptr(dst), _stream(stream)))
-    return dst
 
 
 def quantize_rows_e4m3(src, q, scale, stream=None):

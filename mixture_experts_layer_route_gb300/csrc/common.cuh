@@ -142,20 +142,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// 4-D tiled load (c0 = innermost); used for weights stored as tiles of 64
-// rows x 128 bytes (moe_pack_weights), whose k-block of a 64-row block is one
-// contiguous 8 KB tile.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, int32_t c0,
-                                            int32_t c1, int32_t c2, int32_t c3, uint32_t bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
-      "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -194,18 +180,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
-      : "memory");
-}
-
-// tma_load_4d for a CTA pair (completion on `bar_cluster`, see tma_load_2d_pair).
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* m, int32_t c0,
-                                                 int32_t c1, int32_t c2, int32_t c3,
-                                                 uint32_t bar_cluster, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar_cluster),
-      "l"(policy)
       : "memory");
 }
 

@@ -58,32 +58,6 @@ bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
-// Weight matrix [rows][cols] for the A operand, row-major (2-D map, box of
-// box_rows x 128 bytes) or packed in 64-row x 128-byte tiles, tile (rb, kb) at
-// ((rb * (cols_bytes / 128) + kb) * 8 KB) (4-D map {128-byte row piece, 64
-// rows, k-block, row block}, box {.., 64, 1, box_rows / 64}). Both put the same
-// box_rows x 128-byte, 128-byte-swizzled block in shared memory.
-bool make_a_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
-                uint32_t box_rows, bool tiled) {
-  if (!tiled) return make_tma_map(m, base, dtype, rows, cols, box_rows);
-  auto enc = encoder();
-  if (!enc) return false;
-  const uint32_t es = dtype == MOE_DTYPE_BF16 ? 2 : (dtype == MOE_DTYPE_E4M3 ? 1 : 4);
-  const CUtensorMapDataType dt = dtype == MOE_DTYPE_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                 : dtype == MOE_DTYPE_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  const uint64_t kb_elems = 128 / es;
-  if (rows % 64 != 0 || cols % kb_elems != 0 || box_rows % 64 != 0) return false;
-  cuuint64_t dims[4] = {kb_elems, 64, cols / kb_elems, rows / 64};
-  cuuint64_t strides[3] = {128, 64 * 128, (cols / kb_elems) * 64 * 128};
-  cuuint32_t box[4] = {(cuuint32_t)kb_elems, 64, 1, box_rows / 64};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 namespace {
 
 constexpr int kMaxExperts = 1024;  // the C ABI's limit on E
@@ -201,7 +175,6 @@ void fill_common(GroupedGemmArgs& a, const GemmProblem& p, const int32_t* offset
   a.m_lo = 1;
   a.m_hi = 1 << 30;
   a.tile_n = tile_n;
-  a.a_tiled = p.a_tiled ? 1 : 0;
 }
 
 template <typename TIn>
@@ -242,12 +215,11 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
   const int tile_n = dec ? 32 : tiled_tile_n(p);
   GroupedGemmArgs a;
   memset(&a, 0, sizeof(a));
-  const bool t = p.a_tiled != 0;
-  bool ok = make_a_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64, t) &&
-            make_a_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64, t);
+  bool ok = make_tma_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
+            make_tma_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64);
   if (ok && has_s)
-    ok = make_a_map(&a.tmA[2], Wsg, p.dtype, p.Is, p.H, 64, t) &&
-         make_a_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64, t);
+    ok = make_tma_map(&a.tmA[2], Wsg, p.dtype, p.Is, p.H, 64) &&
+         make_tma_map(&a.tmA[3], Wsu, p.dtype, p.Is, p.H, 64);
   if (ok) {
     if (dec) {
       ok = make_tma_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
@@ -301,11 +273,10 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
   const uint32_t br = dec ? 32 : (pair ? tile_n / 2 : 256), b1 = br / 2 < 16 ? 16 : br / 2;
   GroupedGemmArgs a;
   memset(&a, 0, sizeof(a));
-  const bool t = p.a_tiled != 0;
-  bool ok = make_a_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128, t) &&
+  bool ok = make_tma_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
             make_b_maps(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, br, b1);
   if (ok && has_s)
-    ok = make_a_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128, t) &&
+    ok = make_tma_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128) &&
          make_b_maps(&a.tmB[3], hs, p.dtype, p.T, p.Is, br, b1);
   if (!ok) return cudaErrorInvalidValue;
   if (!has_s) {

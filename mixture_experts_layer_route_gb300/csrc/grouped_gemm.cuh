@@ -97,9 +97,6 @@ struct GroupedGemmArgs {
   unsigned flags;
   int m_lo, m_hi;             // groups with m_lo <= rows <= m_hi are scheduled
   int tile_n;                 // token tile (<= BN): a group of m rows has ceil(m / tile_n)
-  // Weights (tmA) stored as 64-row x 128-byte tiles (4-D maps, coordinates
-  // {0, 0, k-block, row / 64}) instead of row-major (2-D maps, {k, row}).
-  int a_tiled;
 };
 
 enum BMode : int { kGather4 = 0, kTiled = 2 };
@@ -412,9 +409,6 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         my_off = C::A_BYTES;
         my_pol = pol_t;
       }
-      // Weight lanes of a tiled layout load one 64-row x 128-byte tile per
-      // 64 rows of their box (rows are multiples of 64).
-      const bool tiled_a = args.a_tiled != 0 && lane < NA;
       const int nkb = kdim / C::BK;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % STAGES;
@@ -436,18 +430,13 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         if constexpr (PAIR) {
           if (leader && lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
           __syncwarp();
-          const uint32_t bar = mapa_shared(full_bar(s), 0);
-          if (tiled_a)
-            tma_load_4d_pair(a_dst + my_off, my_map, 0, 0, kb, my_row >> 6, bar, my_pol);
-          else if (lane < NLOADS)
-            tma_load_2d_pair(a_dst + my_off, my_map, kx, my_row, bar, my_pol);
+          if (lane < NLOADS)
+            tma_load_2d_pair(a_dst + my_off, my_map, kx, my_row, mapa_shared(full_bar(s), 0),
+                             my_pol);
         } else {
           if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
           __syncwarp();
-          if (tiled_a)
-            tma_load_4d(a_dst + my_off, my_map, 0, 0, kb, my_row >> 6, full_bar(s), my_pol);
-          else if (lane < NLOADS)
-            tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
+          if (lane < NLOADS) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
         }
         if constexpr (BMODE == kGather4) {
 #pragma unroll

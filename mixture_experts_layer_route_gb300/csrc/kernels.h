@@ -49,7 +49,6 @@ struct GemmProblem {
   int dtype;  // MOE_DTYPE_*
   int tile;   // moe_tile: AUTO chooses per expert from its row count
   int T, H, E, k, I, Is;
-  int a_tiled;  // expert weights packed in 64-row x 128-byte tiles (moe_pack_weights)
   unsigned flags;
   unsigned long long limit_ns;
   int num_sms;
@@ -75,11 +74,6 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
                              const float* topk_w, const void* Wd, const void* Wsd, float* Y,
                              int* status, cudaStream_t st, const GemmScales* sc = nullptr);
 bool tensor_map_encoder_available();
-
-// Weight packing into 64-row x 128-byte tiles (pack.cu); rows % 64 == 0,
-// row_bytes % 128 == 0.
-cudaError_t launch_pack_tiles(const void* src, int64_t rows, int64_t row_bytes, void* dst,
-                              int num_sms, cudaStream_t st);
 
 // Row quantization to E4M3 with a power-of-two scale per row (quantize.cu):
 // src [rows][cols] of MOE_DTYPE_BF16 or MOE_DTYPE_F32, cols a multiple of 16.

@@ -125,7 +125,6 @@ moe_status check_problem(const moe_problem* pb, bool allow_e4m3 = false) {
   if (p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM) return MOE_ERR_INVALID_ARG;
   if (p.renorm != 0 && p.renorm != 1) return MOE_ERR_INVALID_ARG;
   if (p.out_f32 != 0 && p.out_f32 != 1) return MOE_ERR_INVALID_ARG;
-  if (p.weights_tiled != 0 && p.weights_tiled != 1) return MOE_ERR_INVALID_ARG;
   if (!groups_valid(p.E, p.k, p.n_group, p.topk_group)) return MOE_ERR_INVALID_ARG;
   const int64_t lim = (int64_t)1 << 30;
   if (p.T * (p.k + 1) >= lim || p.H >= lim || p.I >= lim || p.E * p.I >= lim ||
@@ -144,7 +143,6 @@ GemmProblem gemm_problem(const moe_problem& p) {
   g.k = (int)p.k;
   g.I = (int)p.I;
   g.Is = (int)p.I_shared;
-  g.a_tiled = p.weights_tiled;
   g.flags = p.flags;
   g.limit_ns = (unsigned long long)(p.wait_limit_us ? p.wait_limit_us : 1000000u) * 1000ull;
   g.num_sms = sm_count();
@@ -411,22 +409,6 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
     e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : pb->dtype, Y, g.T, g.H,
                        g.k + (has_s ? 1 : 0), y, g.num_sms, st);
   return cuda_status(e);
-}
-
-moe_status moe_pack_weights(const void* src, int32_t dtype, int64_t rows, int64_t cols, void* dst,
-                            void* stream) {
-  if (dtype != MOE_DTYPE_BF16 && dtype != MOE_DTYPE_F32 && dtype != MOE_DTYPE_E4M3)
-    return MOE_ERR_INVALID_ARG;
-  if (rows < 0 || cols <= 0 || rows % 64 != 0) return MOE_ERR_INVALID_ARG;
-  const int64_t row_bytes = cols * (int64_t)elem_bytes(dtype);
-  if (row_bytes % 128 != 0) return MOE_ERR_INVALID_ARG;
-  if (rows == 0) return MOE_OK;
-  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return MOE_ERR_INVALID_ARG;
-  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
-  const uintptr_t n = (uintptr_t)(rows * row_bytes);
-  if (s0 < d0 + n && d0 < s0 + n) return MOE_ERR_INVALID_ARG;  // overlapping
-  return cuda_status(
-      launch_pack_tiles(src, rows, row_bytes, dst, sm_count(), (cudaStream_t)stream));
 }
 
 moe_status moe_quantize_rows_e4m3(const void* src, int32_t src_dtype, int64_t rows,

@@ -68,8 +68,7 @@ extern "C" moe_status moe_down_combine_noalloc(const moe_problem* pb, const void
   if (p.T < 0 || p.H <= 0 || p.E <= 0 || p.k <= 0 || p.I <= 0 || p.I_shared < 0 ||
       p.k > p.E || p.k > 32 || p.E > 1024 || p.H % 128 != 0 || p.I % 64 != 0 ||
       p.I_shared % 64 != 0 || (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32) ||
-      p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM || (p.out_f32 != 0 && p.out_f32 != 1) ||
-      (p.weights_tiled != 0 && p.weights_tiled != 1))
+      p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM || (p.out_f32 != 0 && p.out_f32 != 1))
     return MOE_ERR_INVALID_ARG;
   if (p.T == 0) return MOE_OK;
   const bool has_s = p.I_shared > 0;
@@ -103,7 +102,6 @@ extern "C" moe_status moe_down_combine_noalloc(const moe_problem* pb, const void
   g.k = (int)p.k;
   g.I = (int)p.I;
   g.Is = (int)p.I_shared;
-  g.a_tiled = p.weights_tiled;
   g.flags = p.flags;
   g.limit_ns = (unsigned long long)(p.wait_limit_us ? p.wait_limit_us : 1000000u) * 1000ull;
   g.num_sms = sms;

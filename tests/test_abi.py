@@ -115,24 +115,3 @@ def test_zero_tokens_is_ok_without_launch(lib):
     rc = lib.moe_forward(ctypes.byref(pb), None, None, None, None, None, None, None, None, None,
                          None, None, 0, None)
     assert rc == 0
-
-
-def test_pack_weights_bad_arguments_rejected_on_host(lib):
-    bf16, f32, e4m3 = m.MOE_DTYPE_BF16, m.MOE_DTYPE_F32, m.MOE_DTYPE_E4M3
-    assert lib.moe_pack_weights(0x1000, bf16, 96, 128, 0x900000, None) == 1   # rows % 64
-    assert lib.moe_pack_weights(0x1000, bf16, 64, 96, 0x900000, None) == 1    # 192-byte rows
-    assert lib.moe_pack_weights(0x1000, f32, 64, 48, 0x900000, None) == 1     # 192-byte rows
-    assert lib.moe_pack_weights(0x1000, e4m3, 64, 64, 0x900000, None) == 1    # 64-byte rows
-    assert lib.moe_pack_weights(0x1000, 7, 64, 128, 0x900000, None) == 1      # dtype
-    assert lib.moe_pack_weights(0x1008, bf16, 64, 128, 0x900000, None) == 1   # misaligned
-    assert lib.moe_pack_weights(None, bf16, 64, 128, 0x900000, None) == 1
-    # src [64][128] bf16 spans 16 KB: a destination inside it overlaps
-    assert lib.moe_pack_weights(0x100000, bf16, 64, 128, 0x102000, None) == 1
-    assert lib.moe_pack_weights(0x1000, bf16, 0, 128, 0x900000, None) == 0    # nothing to do
-
-
-def test_weights_tiled_flag_validated_on_host(lib):
-    pb = m.make_problem(64, 256, 8, 2, 128)
-    pb.weights_tiled = 2
-    n = ctypes.c_size_t(0)
-    assert lib.moe_workspace_size(ctypes.byref(pb), ctypes.byref(n)) == 1
