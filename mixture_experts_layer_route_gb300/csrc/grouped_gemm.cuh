@@ -40,7 +40,8 @@
 // Schedule: every CTA derives the same list of units (group, feature block,
 // token tile) from the offsets: the groups with rows in [m_lo, m_hi], heaviest
 // first, each cut into token tiles of tile_n rows. Units are dealt round-robin
-// to the persistent CTAs (or CTA pairs).
+// to the persistent CTAs (or CTA pairs) through remap_unit, which interleaves
+// the units of heavy groups with the light ones.
 //
 // CTA pairs (CL = 2, the 128- and 256-token variants): one tcgen05.mma with
 // cta_group::2 spans the tensor cores of the cluster's two SMs, M = 256, N =
@@ -55,7 +56,8 @@
 // accumulator on the leader's barrier.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread) and
-// TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each).
+// TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each; the E4M3
+// down GEMM has warps 2-9, two per quarter).
 // A STAGES-deep shared-memory ring (full/empty mbarriers) feeds the MMA; two
 // TMEM accumulators (tfull/tempty mbarriers) let the epilogue of one tile run
 // under the main loop of the next. Every wait is bounded (status word).
