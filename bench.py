@@ -14,7 +14,8 @@ the dominant kernel's achieved bandwidth or FLOP rate against the measured peak;
 layer_roofline = t_roof / t_measured for the whole layer with
 t_roof = max(routed FLOPs / bf16 peak, touched bytes / HBM bandwidth);
 e2e = the same metric through MoELayer.forward with the tokens copied from
-pinned host memory and the output copied back inside the timed region;
+pinned host memory and the output copied back inside the timed region (on
+copy streams, double-buffered, overlapping the next step's compute);
 cpu_baseline = the CPU oracle on a bounded sample of the same workload.
 
 Multi-GPU (torchrun): each rank runs an independent replica of the layer on its
@@ -261,26 +262,50 @@ def time_stages(layer, d, steps, warmup, stream):
 
 
 def time_e2e(layer, d, steps, warmup, stream):
-    """Public API end to end: pinned host tokens -> device, forward, -> host."""
+    """Public API end to end: each step copies its tokens from pinned host memory
+    to the device, runs the layer, and copies y back to pinned host memory. The
+    copies run on their own streams, double-buffered, so that step i+1's tokens
+    arrive and step i's result leaves while the next layer computes (as a
+    serving loop would); every step's copies are inside the timed region."""
     x_dev = d["x"]
     T, H = x_dev.shape
     x_host = x_dev.cpu().pin_memory()
     y_host = torch.empty((T, H), dtype=layer.dtype).pin_memory()
-    x_in = torch.empty_like(x_dev)
-    y = torch.empty_like(x_dev)
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            x_in.copy_(x_host, non_blocking=True)
-            layer.forward(x_in, out=y, stream=stream)
-            y_host.copy_(y, non_blocking=True)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            x_in.copy_(x_host, non_blocking=True)
-            layer.forward(x_in, out=y, stream=stream)
-            y_host.copy_(y, non_blocking=True)
-        e1.record(stream)
+    x_in = [torch.empty_like(x_dev) for _ in range(2)]
+    y = [torch.empty_like(x_dev) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_x = [torch.cuda.Event() for _ in range(2)]   # x_in[b] filled
+    ev_y = [torch.cuda.Event() for _ in range(2)]   # y[b] computed (x_in[b] read)
+    ev_o = [torch.cuda.Event() for _ in range(2)]   # y[b] copied out
+
+    def run(n):
+        with torch.cuda.stream(h2d):
+            x_in[0].copy_(x_host, non_blocking=True)
+            ev_x[0].record(h2d)
+        for i in range(n):
+            b = i & 1
+            stream.wait_event(ev_x[b])
+            if i >= 2:
+                stream.wait_event(ev_o[b])
+            layer.forward(x_in[b], out=y[b], stream=stream)
+            ev_y[b].record(stream)
+            if i + 1 < n:
+                if i >= 1:
+                    h2d.wait_event(ev_y[1 - b])
+                with torch.cuda.stream(h2d):
+                    x_in[1 - b].copy_(x_host, non_blocking=True)
+                    ev_x[1 - b].record(h2d)
+            d2h.wait_event(ev_y[b])
+            with torch.cuda.stream(d2h):
+                y_host.copy_(y[b], non_blocking=True)
+                ev_o[b].record(d2h)
+
+    run(warmup)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(h2d)
+    run(steps)
+    e1.record(d2h)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     nb = T * H * x_dev.element_size()
