@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,  /* bad pointer, shape, alignment or dtype */
-  MOE_ERR_UNSUPPORTED = 2,  /* valid but not supported by this build/device */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but not supported by the library or device */
   MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
   MOE_ERR_TIMEOUT = 5,      /* (device status) a bounded wait ran out */
