@@ -350,9 +350,14 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     // fetches the next k-block's half line, which must survive until used.)
     const uint64_t pol_w = (BN <= 64) ? l2_policy_evict_first() : l2_policy_evict_normal();
     const uint64_t pol_t = l2_policy_evict_last();
-    uint32_t it = 0;
+    // Test hook (MOE_FLAG_TEST_SKIP_SIGNAL): the first stage of the first unit
+    // is never signalled nor loaded, so the MMA issuer's wait on it runs out.
+    // It is taken here, outside the k-loop: a per-k-block check in that loop
+    // cost the decode step 1%.
+    const bool skip_first = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
+    uint32_t it = skip_first ? 1u : 0u;
+    int kb_first = skip_first ? 1 : 0;  // first k-block of the next unit
     bool ok = true;
-    bool skip_once = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
     for (int u = cid; u < total && ok; u += ncl) {
       Tile tl = decode_tile(remap_unit(u, total, heavy_units), prefix, order, offs, ngroups,
                             args.tile_n);
@@ -412,7 +417,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         my_pol = pol_t;
       }
       const int nkb = kdim / C::BK;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
+      const int kb0 = kb_first;
+      kb_first = 0;
+      for (int kb = kb0; kb < nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
         int wok = 1;
@@ -425,10 +432,6 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         const uint32_t a_dst = smem_u32(stages + (size_t)s * C::STAGE_BYTES);
         const uint32_t b_dst = a_dst + C::A_BYTES;
         const int kx = kb * C::BK;
-        if (skip_once) {  // test hook: withhold this stage's signal and loads
-          skip_once = false;
-          continue;
-        }
         if constexpr (PAIR) {
           if (leader && lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
           __syncwarp();
