@@ -226,10 +226,12 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   const int crank = PAIR ? (int)cluster_ctarank() : 0;
   const bool leader = crank == 0;
   const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
-  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
-  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
-  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
+  const uint32_t bars_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bars_base + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bars_base + 8u * (uint32_t)(STAGES + s); };
+  auto tfull_bar = [&](int a) { return bars_base + 8u * (uint32_t)(2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bars_base + 8u * (uint32_t)(2 * STAGES + 2 + a); };
+  const uint32_t stages_base = smem_u32(stages);
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
 
   if (threadIdx.x == 0) {
@@ -356,6 +358,10 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     // cost the decode step 1%.
     const bool skip_first = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
     uint32_t it = skip_first ? 1u : 0u;
+    // Ring position of `it`, kept incrementally (the k-loop is on the decode
+    // step's critical path): stage it % STAGES and phase (it / STAGES) & 1.
+    int stg = (int)it;
+    uint32_t ph = 0;
     int kb_first = skip_first ? 1 : 0;  // first k-block of the next unit
     bool ok = true;
     for (int u = cid; u < total && ok; u += ncl) {
@@ -419,17 +425,21 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       const int nkb = kdim / C::BK;
       const int kb0 = kb_first;
       kb_first = 0;
-      for (int kb = kb0; kb < nkb; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t round = it / STAGES;
+      for (int kb = kb0; kb < nkb; ++kb) {
+        const int s = stg;
         int wok = 1;
-        if (lane == 0) wok = mbar_wait(empty_bar(s), (round & 1u) ^ 1u, args.status, limit);
+        if (lane == 0) wok = mbar_wait(empty_bar(s), ph ^ 1u, args.status, limit);
         wok = __shfl_sync(0xffffffffu, wok, 0);
         if (!wok) {
           ok = false;
           break;
         }
-        const uint32_t a_dst = smem_u32(stages + (size_t)s * C::STAGE_BYTES);
+        ++it;
+        if (++stg == STAGES) {
+          stg = 0;
+          ph ^= 1u;
+        }
+        const uint32_t a_dst = stages_base + (uint32_t)s * C::STAGE_BYTES;
         const uint32_t b_dst = a_dst + C::A_BYTES;
         const int kx = kb * C::BK;
         if constexpr (PAIR) {
@@ -468,7 +478,9 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      uint32_t it = 0, lt = 0;
+      uint32_t lt = 0;
+      int stg = 0;       // ring stage of the next k-block
+      uint32_t ph = 0;   // its phase parity
       constexpr uint32_t fmt = UmmaOf<TIn>::fmt;
       bool ok = true;
       for (int u = cid; u < total && ok; u += ncl, ++lt) {
@@ -481,15 +493,18 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         const uint32_t d_tmem = tmem_base + acc * BN;
         const int n_mma = (tl.n_valid + C::N_ROUND - 1) / C::N_ROUND * C::N_ROUND;
         const uint32_t idesc = umma_idesc(fmt, C::BM * CL, (uint32_t)n_mma);
-        for (int kb = 0; kb < kdim / C::BK; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t round = it / STAGES;
-          if (!mbar_wait(full_bar(s), round & 1u, args.status, limit)) {
+        for (int kb = 0; kb < kdim / C::BK; ++kb) {
+          const int s = stg;
+          if (!mbar_wait(full_bar(s), ph, args.status, limit)) {
             ok = false;
             break;
           }
+          if (++stg == STAGES) {
+            stg = 0;
+            ph ^= 1u;
+          }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stages + (size_t)s * C::STAGE_BYTES);
+          const uint32_t a_addr = stages_base + (uint32_t)s * C::STAGE_BYTES;
           const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
