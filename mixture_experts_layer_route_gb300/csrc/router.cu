@@ -537,12 +537,36 @@ __global__ void logits_reduce_kernel(const float* __restrict__ part, int S, int 
 }
 
 // One warp per token. NV = values per lane (E <= 32 * NV).
+// Order-preserving key of a float: for non-NaN a, b, a > b exactly when
+// key(a) > key(b). -0 is taken as +0 first, so the two zeros tie as they do
+// under float comparison. key_value inverts it (returning +0 for either zero).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+constexpr uint32_t kNoExpert = 0xffffffffu;
+
+// Arg-max over the warp: the largest key among the lanes' candidates (bi !=
+// kNoExpert), and among equal keys the lowest index. Two warp reductions.
+__device__ __forceinline__ uint32_t warp_argmax(uint32_t bk, uint32_t bi, uint32_t* best_key) {
+  const uint32_t mx = __reduce_max_sync(0xffffffffu, bi == kNoExpert ? 0u : bk);
+  *best_key = mx;
+  return __reduce_min_sync(0xffffffffu, (bi != kNoExpert && bk == mx) ? bi : kNoExpert);
+}
+
 // S == 1: `src` holds final logits (bias already added). S > 1: `src` holds S
 // partial slices; they are reduced here and, if logits_out != nullptr, the
 // reduced logits are written out.
 // Top-k and gate weights of one token by one warp. v[i] holds the logit of
-// expert lane + 32 i (-inf past E). k rounds of warp arg-max over the not yet
-// chosen values, ties to the lower expert index; lane r keeps round r.
+// expert lane + 32 i. k rounds of warp arg-max over the experts not yet
+// chosen, ties to the lower expert index; lane r keeps round r. Values are
+// compared as order-preserving integer keys, so a round is a lane-local scan
+// and two warp reductions.
 // Group-limited form (n_group > 1, the DeepSeek router of the same section, of
 // which plain top-k is the one-group case): the experts form n_group
 // contiguous groups of E / n_group; a group's score is its largest logit; only
@@ -554,77 +578,60 @@ __device__ __forceinline__ void route_warp(const float (&v)[NV], int E, int k, i
                                            int32_t* __restrict__ ids_row,
                                            float* __restrict__ w_row) {
   const int lane = threadIdx.x & 31;
-  float vs[NV];  // selection values: v, or -inf outside the kept groups
+  uint32_t key[NV];
+  uint32_t live = 0;  // bit i: expert lane + 32 i exists and can still be chosen
 #pragma unroll
-  for (int i = 0; i < NV; ++i) vs[i] = v[i];
+  for (int i = 0; i < NV; ++i) {
+    key[i] = order_key(v[i]);
+    if (lane + 32 * i < E) live |= 1u << i;
+  }
   if (n_group > 1) {
     const int G = E / n_group;
     int grp[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) grp[i] = (lane + 32 * i) / G;  // >= n_group past E
-    float gscore = -INFINITY;  // lane j: score of group j
+    uint32_t gkey = 0;  // lane j < n_group: key of group j's largest logit
     for (int j = 0; j < n_group; ++j) {
-      float mx = -INFINITY;
+      uint32_t mk = 0;
 #pragma unroll
       for (int i = 0; i < NV; ++i)
-        if (grp[i] == j) mx = fmaxf(mx, v[i]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      if (lane == j) gscore = mx;
+        if (grp[i] == j) mk = max(mk, key[i]);
+      mk = __reduce_max_sync(0xffffffffu, mk);
+      if (lane == j) gkey = mk;
     }
     uint32_t kept = 0;
     for (int r = 0; r < topk_group; ++r) {
       const bool cand = lane < n_group && !((kept >> lane) & 1u);
-      float bv = cand ? gscore : -INFINITY;
-      int bi = cand ? lane : 0x7fffffff;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      kept |= 1u << bi;
+      uint32_t unused;
+      const uint32_t g = warp_argmax(gkey, cand ? (uint32_t)lane : kNoExpert, &unused);
+      if (g < 32u) kept |= 1u << g;
     }
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-      if (grp[i] >= n_group || !((kept >> grp[i]) & 1u)) vs[i] = -INFINITY;
+      if (grp[i] >= n_group || !((kept >> grp[i]) & 1u)) live &= ~(1u << i);
   }
-  uint32_t taken = 0;
-  float my_val = 0.f;
+  uint32_t my_key = 0;
   int my_idx = 0;
   for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    uint32_t bk = 0, bi = kNoExpert;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      const bool free_ = !((taken >> i) & 1u) && e < E;
-      if (free_ && (vs[i] > bv || bi == 0x7fffffff)) {  // ascending e: first max wins
-        bv = vs[i];
-        bi = e;
+    for (int i = 0; i < NV; ++i) {  // ascending expert index: the first maximum wins
+      if (((live >> i) & 1u) && (bi == kNoExpert || key[i] > bk)) {
+        bk = key[i];
+        bi = (uint32_t)(lane + 32 * i);
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    uint32_t mx;
+    const uint32_t win = warp_argmax(bk, bi, &mx);
+    if (win != kNoExpert && (int)(win & 31u) == lane) live &= ~(1u << (win >> 5));
     if (lane == r) {
-      my_val = bv;
-      my_idx = bi;
+      my_key = mx;
+      my_idx = (int)win;
     }
   }
 
-  const float m = __shfl_sync(0xffffffffu, my_val, 0);
-  float p = (lane < k) ? expf(my_val - m) : 0.f;
+  const float m = key_value(__shfl_sync(0xffffffffu, my_key, 0));
+  const float p = (lane < k) ? expf(key_value(my_key) - m) : 0.f;
   float ssum;
   if (renorm) {
     ssum = p;
@@ -632,7 +639,7 @@ __device__ __forceinline__ void route_warp(const float (&v)[NV], int E, int k, i
     ssum = 0.f;
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-      if (lane + 32 * i < E) ssum += expf(v[i] - m);
+      if (lane + 32 * i < E) ssum += expf(key_value(key[i]) - m);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, off);
@@ -642,7 +649,10 @@ __device__ __forceinline__ void route_warp(const float (&v)[NV], int E, int k, i
   }
 }
 
-template <int NV>
+// B: partial slices loaded together (all of a batch's loads are issued before
+// any of them is added). One-slice batches need the fewest registers and suit
+// S <= 2; larger batches cut the dependent load round trips when S is larger.
+template <int NV, int B>
 __global__ void __launch_bounds__(256, 2) route_kernel(const float* __restrict__ src, int S,
                                                     const float* __restrict__ bias, int T, int E,
                                                     int k, int renorm, int n_group,
@@ -664,9 +674,7 @@ __global__ void __launch_bounds__(256, 2) route_kernel(const float* __restrict__
     }
   } else {
     // Sum of the S partial slices in ascending slice order, then the bias (the
-    // arithmetic of reduce_partials). All loads of a batch of B slices, for
-    // all of the lane's experts, are issued before any of them is added.
-    constexpr int B = NV >= 32 ? 1 : 32 / NV;
+    // arithmetic of reduce_partials).
     const size_t stride = (size_t)T * E;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -828,9 +836,16 @@ cudaError_t launch_route(const float* src, int S, const float* bias, int T, int 
   const int warps = 8;
   const int blocks = (T + warps - 1) / warps;
   const int nv = (E + 31) / 32;
-#define MOE_ROUTE_CASE(NV)                                                                  \
-  return launch_chained(route_kernel<NV>, dim3(blocks), dim3(warps * 32), 0, st, 1, src, S, bias, \
-                        T, E, k, renorm, n_group, topk_group, logits_out, ids, w)
+  // Batches of 32 / NV slices (one load round trip for up to 8 slices when
+  // NV <= 4) unless at most one slice is added to the first.
+  const bool wide = S > 2;
+#define MOE_ROUTE_CASE(NV)                                                                     \
+  return wide ? launch_chained(route_kernel<NV, (NV >= 32 ? 1 : 32 / NV)>, dim3(blocks),      \
+                               dim3(warps * 32), 0, st, 1, src, S, bias, T, E, k, renorm,      \
+                               n_group, topk_group, logits_out, ids, w)                        \
+              : launch_chained(route_kernel<NV, 1>, dim3(blocks), dim3(warps * 32), 0, st, 1, \
+                               src, S, bias, T, E, k, renorm, n_group, topk_group, logits_out, \
+                               ids, w)
   if (nv <= 1) MOE_ROUTE_CASE(1);
   else if (nv <= 2) MOE_ROUTE_CASE(2);
   else if (nv <= 4) MOE_ROUTE_CASE(4);

@@ -152,6 +152,26 @@ def test_route_grouped_bitexact(oracle, T, E, k, n_group, topk_group, renorm, ti
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=1e-6)
 
 
+@pytest.mark.parametrize("T,E,k,n_group,topk_group", [
+    (200, 128, 8, 1, 1), (64, 40, 5, 1, 1), (100, 256, 8, 8, 4), (50, 64, 6, 4, 2),
+])
+def test_route_signed_zeros_tie(oracle, T, E, k, n_group, topk_group):
+    """-0 and +0 compare equal, so among zero logits the lower expert index
+    wins whatever the signs; the logits mix both zeros with small integers."""
+    g = np.random.default_rng(T + E + k)
+    logits = g.integers(-1, 2, size=(T, E)).astype(np.float32)
+    zero = g.random((T, E)) < 0.6
+    logits[zero] = np.where(g.random(int(zero.sum())) < 0.5, np.float32(0.0), np.float32(-0.0))
+    lt = torch.from_numpy(logits).to(DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    m.route_grouped(lt, k, 1, n_group, topk_group, ids, w)
+    torch.cuda.synchronize()
+    rid, rw = oracle.route_grouped(logits, k, 1, n_group, topk_group)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=1e-6)
+
+
 def test_route_grouped_rejects_bad_groups():
     lt = torch.zeros(4, 64, dtype=torch.float32, device=DEV)
     ids = torch.empty(4, 8, dtype=torch.int32, device=DEV)
