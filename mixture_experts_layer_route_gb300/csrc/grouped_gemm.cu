@@ -177,6 +177,14 @@ void fill_common(GroupedGemmArgs& a, const GemmProblem& p, const int32_t* offset
   a.tile_n = tile_n;
 }
 
+// Pre-wait weight prefetch (GroupedGemmArgs::pf_first): decode-sized launches
+// without a shared expert, with at least 4 routed slots per expert on average
+// (an expert then holds no rows with probability ~e^-4 under uniform routing,
+// and none holds more than a 32-row tile, so the schedule is index order).
+bool prefetch_first_units(const GemmProblem& p, bool dec) {
+  return dec && p.Is == 0 && (int64_t)p.T * p.k >= 4 * (int64_t)p.E;
+}
+
 template <typename TIn>
 cudaError_t launch_gated(const GroupedGemmArgs& a, const GemmProblem& p, bool dec, bool pair,
                          int tile_n, size_t ub, cudaStream_t st) {
@@ -236,6 +244,9 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
     a.tmA[3] = a.tmA[1];
   }
   fill_common(a, p, offsets, gather_idx, status, tile_n);
+  a.pf_first = prefetch_first_units(p, dec) ? 1 : 0;
+  a.pf_base[0] = Wg;
+  a.pf_base[1] = Wu;
   a.topk_w = nullptr;
   if (sc) {
     for (int i = 0; i < 4; ++i) a.sA[i] = sc->a[i];
@@ -286,6 +297,9 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
   a.tmA[1] = a.tmA[0];
   a.tmA[3] = a.tmA[2];
   fill_common(a, p, offsets, gather_idx, status, tile_n);
+  a.pf_first = prefetch_first_units(p, dec) ? 1 : 0;
+  a.pf_base[0] = Wd;
+  a.pf_base[1] = Wd;
   a.topk_w = topk_w;
   if (sc) {
     for (int i = 0; i < 4; ++i) a.sA[i] = sc->a[i];

@@ -99,6 +99,11 @@ struct GroupedGemmArgs {
   unsigned flags;
   int m_lo, m_hi;             // groups with m_lo <= rows <= m_hi are scheduled
   int tile_n;                 // token tile (<= BN): a group of m rows has ceil(m / tile_n)
+  // Decode-sized launches only (0 otherwise): ask L2 for the weight rows of the
+  // unit each CTA is likely to take first, before waiting for the preceding
+  // kernel. pf_base: raw routed A operands (GATED: gate, up; DOWN: down, unused).
+  int pf_first;
+  const void* pf_base[2];
 };
 
 enum BMode : int { kGather4 = 0, kTiled = 2 };
@@ -154,6 +159,9 @@ struct Tile {
   int p0;       // first position (routed) / first token (shared)
   int n_valid;  // rows of this tile
 };
+
+// Bytes per L2 bulk prefetch instruction of the pre-wait weight prefetch.
+constexpr size_t kPrefetchChunk = 32768;
 
 // Position i of the round-robin deal -> unit of the class-ordered list, whose
 // first uh units belong to groups of more than 128 rows (tensor-bound tiles)
@@ -255,6 +263,35 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
     else
       tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+  }
+  // Weight prefetch while the preceding kernel finishes (pf_first: the host
+  // sets it for decode-sized launches without a shared expert in which nearly
+  // every expert holds rows, so all groups are light and scheduled in index
+  // order): CTA cid's first unit would then be feature block cid % nf of
+  // expert cid / nf. Until the routing is known HBM is otherwise idle; a
+  // wrong guess only fetches rows that another unit reads later or that no
+  // unit reads. Weights are never written by a preceding kernel, so reading
+  // them before pdl_wait is safe.
+  if constexpr (!PAIR) {
+    if (warp == 0 && args.pf_first) {
+      const int nf = args.n_out_routed / C::WM;
+      const int g = cid / nf;
+      if (g < E) {
+        const size_t row_bytes = (size_t)args.kdim_routed * sizeof(TIn);
+        const size_t bytes = (size_t)C::WM * row_bytes;
+        const size_t first =
+            ((size_t)g * args.n_out_routed + (size_t)(cid - g * nf) * C::WM) * row_bytes;
+        constexpr int NOP = GATED ? 2 : 1;
+        const int nch = (int)((bytes + kPrefetchChunk - 1) / kPrefetchChunk);
+        for (int c = lane; c < NOP * nch; c += 32) {
+          const int op = c / nch;
+          const size_t off = (size_t)(c - op * nch) * kPrefetchChunk;
+          const size_t rem = bytes - off;
+          prefetch_l2_bulk(static_cast<const uint8_t*>(args.pf_base[op]) + first + off,
+                           (uint32_t)(rem < kPrefetchChunk ? rem : kPrefetchChunk));
+        }
+      }
+    }
   }
   pdl_wait();  // global memory from here on
   if (warp == 2) {
