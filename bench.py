@@ -618,8 +618,12 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = ALL_CONFIGS[args.config]
-    torch.cuda.set_device(0)
-    layer, d = build_layer(cfg, "cuda", seed=args.seed)
+    # Inputs only: the same seeded generator as the native arm (on the GPU when
+    # there is one, for speed); nothing of the native library is loaded.
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cuda":
+        torch.cuda.set_device(0)
+    d = generate(cfg, seed=args.seed, device=dev)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
     for _ in range(args.warmup):
         cpu_baseline(cfg, d, budget_s=0.0, max_tokens=8)
