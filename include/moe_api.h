@@ -110,8 +110,9 @@ typedef struct {
 moe_status moe_workspace_size(const moe_problem* pb, size_t* bytes);
 
 /* Step a1, router logits: logits[t][e] = sum_h x[t][h] W_router[e][h]
- * (+ router_bias[e]), fp32 accumulation on the CUDA cores (the "Gate" at the
- * end of stage 2 in the DeepSeek page's five-stage layer breakdown).
+ * (+ router_bias[e]), fp32 accumulation (the "Gate" at the end of stage 2 in
+ * the DeepSeek page's five-stage layer breakdown): bf16 problems on the tensor
+ * cores (bf16 products are exact in fp32), fp32 problems on the CUDA cores.
  * router_bias: fp32 [E] or NULL. logits: fp32 [T][E]. */
 moe_status moe_router_logits(const moe_problem* pb, const void* x, const void* W_router,
                              const float* router_bias, float* logits, void* workspace,
