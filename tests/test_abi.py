@@ -115,3 +115,40 @@ def test_zero_tokens_is_ok_without_launch(lib):
     rc = lib.moe_forward(ctypes.byref(pb), None, None, None, None, None, None, None, None, None,
                          None, None, 0, None)
     assert rc == 0
+
+
+LAYOUT_CASES = [dict(T=c.T, H=c.H, E=c.E, k=c.k, I=c.I, I_shared=c.I_shared, dtype=c.dtype)
+                for c in CONFIGS.values()] + [
+    dict(T=64, H=4096, E=128, k=8, I=1536, I_shared=0, dtype="e4m3"),
+    dict(T=4096, H=7168, E=256, k=8, I=2048, I_shared=2048, dtype="e4m3"),
+    dict(T=1, H=128, E=4, k=4, I=64, I_shared=64, dtype="bf16"),
+    dict(T=513, H=256, E=1024, k=32, I=128, I_shared=0, dtype="f32"),
+]
+
+
+@pytest.mark.parametrize("c", LAYOUT_CASES, ids=[f"{c['T']}x{c['E']}x{c['k']}-{c['dtype']}"
+                                                 for c in LAYOUT_CASES])
+def test_workspace_layout_regions_are_disjoint_and_inside(lib, c):
+    """moe_get_workspace_layout: every intermediate lies after the status
+    header, 256-byte aligned, inside moe_workspace_size(), and no two regions
+    overlap (sizes from the layouts the header states)."""
+    pb = m.make_problem(c["T"], c["H"], c["E"], c["k"], c["I"], c["I_shared"], 1, c["dtype"])
+    size = m.workspace_size(pb)
+    lay = m.workspace_layout(pb)
+    T, E, k, I, Is = c["T"], c["E"], c["k"], c["I"], c["I_shared"]
+    act = 4 if c["dtype"] == "f32" else 2  # h is bf16 for E4M3 layers
+    sizes = dict(logits=T * E * 4, topk_ids=T * k * 4, topk_w=T * k * 4,
+                 expert_offsets=(E + 2) * 4, gather_idx=T * k * 4, slot_pos=T * k * 4,
+                 h=T * k * I * act, h_shared=T * Is * act)
+    regions = []
+    for name, nbytes in sizes.items():
+        off = lay[name]
+        if name == "h_shared" and not Is:
+            assert off == -1
+            continue
+        assert off >= 256 and off % 256 == 0, name
+        assert off + nbytes <= size, name
+        regions.append((off, off + nbytes, name))
+    regions.sort()
+    for (a0, a1, an), (b0, b1, bn) in zip(regions, regions[1:]):
+        assert a1 <= b0, (an, bn)
