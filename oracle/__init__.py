@@ -186,6 +186,43 @@ def _u8p(a):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
 
 
+def ffn_combine_fp8(self, x, ids, w, Wg, Wu, Wd, Wsg=None, Wsu=None, Wsd=None,
+                    want_intermediates=False):
+    """The experts and the combine of the FP8 layer for given routing.
+
+    Definition (the microscaled-FP8 serving of "Hosting Qwen on Blackwell",
+    with one power-of-two scale per matrix row as the block): every tensor the
+    layer stores between its steps is a bf16 activation (x as given, h after
+    the SwiGLU), and every FP8 GEMM quantizes its operands on entry, one scale
+    per row along the contraction axis:
+      - each x row (over H) and each weight row (W_gate/W_up rows over H,
+        W_down rows over I) is quantized to E4M3 with its scale;
+      - h = bf16(silu(g) * u), g and u exact dot products of the dequantized
+        rows (rounded to fp32, then to the bf16 activation);
+      - each h row (over I) is quantized like x;
+      - y = sum_r w_r * (W_down[e_r] . h_r) (+ the shared expert, weight 1) on
+        the dequantized values.
+    """
+    E = Wg.shape[0]
+    k = ids.shape[1]
+    has_s = Wsg is not None
+    offs, gidx, spos = self.permute(np.ascontiguousarray(ids, np.int32), E,
+                                    1 if has_s else 0)
+    dq = lambda a: self.dequantize_rows_e4m3(*self.quantize_rows_e4m3(a))
+    xd = dq(x)
+    Wgd, Wud, Wdd = dq(Wg), dq(Wu), dq(Wd)
+    Wsgd, Wsud, Wsdd = (dq(Wsg), dq(Wsu), dq(Wsd)) if has_s else (None, None, None)
+    h, hs = self.expert_h(xd, offs, gidx, Wgd, Wud, k, Wsgd, Wsud)
+    hb = self.bf16_round(h)
+    hsb = self.bf16_round(hs) if has_s else None
+    y = self.down_combine(dq(hb), offs, spos, np.ascontiguousarray(ids, np.int32),
+                          np.ascontiguousarray(w, np.float32), Wdd,
+                          dq(hsb) if has_s else None, Wsdd)
+    if want_intermediates:
+        return y, dict(offsets=offs, gather_idx=gidx, h=hb, hs=hsb, h_f32=h, hs_f32=hs)
+    return y
+
+
 def _fp8_methods():
     """FP8 expert path (E4M3 codes, one power-of-two scale per row): the
     quantization primitives, and the layer as a composition of the pinned
@@ -221,31 +258,6 @@ def _fp8_methods():
         out = np.empty(a.shape, np.float32)
         self.lib.oracle_bf16_round(self._pf(a), a.size, self._pf(out))
         return out
-
-    def ffn_combine_fp8(self, x, ids, w, Wg, Wu, Wd, Wsg=None, Wsu=None, Wsd=None,
-                        want_intermediates=False):
-        """The experts and the combine of the FP8 layer for given routing: x
-        rows, every weight row and every h row (after its bf16 rounding)
-        quantized to E4M3 with a power-of-two scale; the experts and the
-        combine run on the dequantized values."""
-        E = Wg.shape[0]
-        k = ids.shape[1]
-        has_s = Wsg is not None
-        offs, gidx, spos = self.permute(np.ascontiguousarray(ids, np.int32), E,
-                                        1 if has_s else 0)
-        dq = lambda a: self.dequantize_rows_e4m3(*self.quantize_rows_e4m3(a))
-        xd = dq(x)
-        Wgd, Wud, Wdd = dq(Wg), dq(Wu), dq(Wd)
-        Wsgd, Wsud, Wsdd = (dq(Wsg), dq(Wsu), dq(Wsd)) if has_s else (None, None, None)
-        h, hs = self.expert_h(xd, offs, gidx, Wgd, Wud, k, Wsgd, Wsud)
-        hb = self.bf16_round(h)
-        hsb = self.bf16_round(hs) if has_s else None
-        y = self.down_combine(dq(hb), offs, spos, np.ascontiguousarray(ids, np.int32),
-                              np.ascontiguousarray(w, np.float32), Wdd,
-                              dq(hsb) if has_s else None, Wsdd)
-        if want_intermediates:
-            return y, dict(offsets=offs, gather_idx=gidx, h=hb, hs=hsb, h_f32=h, hs_f32=hs)
-        return y
 
     def forward_fp8(self, x, Wr, bias, Wg, Wu, Wd, k, renorm=1, Wsg=None, Wsu=None, Wsd=None,
                     n_group=1, topk_group=1, want_intermediates=False):
