@@ -41,9 +41,12 @@
  *    Kernels never trap.
  *  - Results are bitwise reproducible run to run: no floating-point atomics,
  *    fixed reduction orders.
- *  - Thread-compatible: calls on distinct workspaces may run concurrently; the
- *    only global state is a per-device cache (SM count, kernel attributes)
- *    guarded by a mutex.
+ *  - Thread-compatible: calls on distinct workspaces may run concurrently.
+ *    Global state: a per-device cache (SM count, kernel attributes, the
+ *    address of the scratch array below) guarded by a mutex, and the one
+ *    static scratch array of moe_down_combine_noalloc per device, which every
+ *    call of that function uses: its calls must not overlap on one device
+ *    (the caller serialises them); the other calls never touch it.
  */
 #ifndef MOE_API_H_
 #define MOE_API_H_

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "moe_api.h"
+
 namespace moe {
 
 // TMA tensor map of a row-major [rows][cols] matrix of MOE_DTYPE_* elements:
@@ -74,6 +76,16 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
                              const float* topk_w, const void* Wd, const void* Wsd, float* Y,
                              int* status, cudaStream_t st, const GemmScales* sc = nullptr);
 bool tensor_map_encoder_available();
+
+// Entry-point helpers (moe_api.cu), shared by every C ABI call so that all of
+// them validate and describe a problem the same way.
+// SM count of the current device, cached per device under a mutex.
+int sm_count();
+// Argument checks of a moe_problem (shapes, dtype, tile, the int32 index
+// ranges the kernels rely on); MOE_OK or the error to return before any launch.
+moe_status check_problem(const moe_problem* pb, bool allow_e4m3 = false);
+// The grouped-GEMM description of a checked problem.
+GemmProblem gemm_problem(const moe_problem& p);
 
 // Row quantization to E4M3 with a power-of-two scale per row (quantize.cu):
 // src [rows][cols] of MOE_DTYPE_BF16 or MOE_DTYPE_F32, cols a multiple of 16.

@@ -23,22 +23,6 @@ struct Layout {
   int S;  // router split count
 };
 
-std::mutex g_sm_mu;
-int g_sm_count[64] = {0};
-
-int sm_count() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  std::lock_guard<std::mutex> lk(g_sm_mu);
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      return 148;
-    g_sm_count[dev] = n;
-  }
-  return g_sm_count[dev];
-}
-
 // Number of SMs used to size the router split; a fixed value keeps the
 // workspace size independent of the device queried.
 constexpr int kRouterSplitSms = 152;
@@ -107,9 +91,45 @@ bool groups_valid(int64_t E, int64_t k, int64_t n_group, int64_t topk_group) {
   return k <= topk_group * (E / n_group);
 }
 
-// allow_e4m3: the entry points that take E4M3 weights (workspace queries and
-// moe_forward_fp8); the bf16/fp32 sub-calls reject that dtype.
-moe_status check_problem(const moe_problem* pb, bool allow_e4m3 = false) {
+int* status_ptr(void* ws) { return reinterpret_cast<int*>(ws); }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(reinterpret_cast<uint8_t*>(ws) + off);
+}
+
+moe_status check_ws(const void* ws, size_t have, size_t need) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  if (have < need) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+std::mutex g_sm_mu;
+int g_sm_count[64] = {0};
+
+}  // namespace
+
+// ---- shared with the other entry points of the library (declared in kernels.h)
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(g_sm_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 148;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+// Host-side validation of a problem, before any launch. allow_e4m3: the entry
+// points that take E4M3 weights (workspace queries and moe_forward_fp8); the
+// bf16/fp32 sub-calls reject that dtype.
+moe_status check_problem(const moe_problem* pb, bool allow_e4m3) {
   if (!pb) return MOE_ERR_INVALID_ARG;
   const moe_problem& p = *pb;
   if (p.T < 0 || p.H <= 0 || p.E <= 0 || p.k <= 0 || p.I <= 0 || p.I_shared < 0)
@@ -149,22 +169,6 @@ GemmProblem gemm_problem(const moe_problem& p) {
   return g;
 }
 
-int* status_ptr(void* ws) { return reinterpret_cast<int*>(ws); }
-
-moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
-
-template <typename P>
-P* at(void* ws, size_t off) {
-  return reinterpret_cast<P*>(reinterpret_cast<uint8_t*>(ws) + off);
-}
-
-moe_status check_ws(const void* ws, size_t have, size_t need) {
-  if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
-  if (have < need) return MOE_ERR_WORKSPACE;
-  return MOE_OK;
-}
-
-}  // namespace
 }  // namespace moe
 
 using namespace moe;

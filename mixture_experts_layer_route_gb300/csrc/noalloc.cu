@@ -63,13 +63,10 @@ extern "C" moe_status moe_down_combine_noalloc(const moe_problem* pb, const void
                                                const int32_t* gather_idx, const float* topk_w,
                                                const void* W_down, const void* Ws_down, void* y,
                                                void* stream, moe_status* device_status) {
-  if (!pb) return MOE_ERR_INVALID_ARG;
+  // The same checks as moe_down_combine, int32 index ranges included.
+  moe_status s = check_problem(pb);
+  if (s != MOE_OK) return s;
   const moe_problem& p = *pb;
-  if (p.T < 0 || p.H <= 0 || p.E <= 0 || p.k <= 0 || p.I <= 0 || p.I_shared < 0 ||
-      p.k > p.E || p.k > 32 || p.E > 1024 || p.H % 128 != 0 || p.I % 64 != 0 ||
-      p.I_shared % 64 != 0 || (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32) ||
-      p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM || (p.out_f32 != 0 && p.out_f32 != 1))
-    return MOE_ERR_INVALID_ARG;
   if (p.T == 0) return MOE_OK;
   const bool has_s = p.I_shared > 0;
   if (!h || !expert_offsets || !gather_idx || !topk_w || !W_down || !y) return MOE_ERR_INVALID_ARG;
@@ -89,23 +86,7 @@ extern "C" moe_status moe_down_combine_noalloc(const moe_problem* pb, const void
   int* status = reinterpret_cast<int*>(scratch);
   float* Y = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(scratch) + kNoAllocHeader);
 
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  GemmProblem g;
-  g.dtype = p.dtype;
-  g.tile = p.tile;
-  g.T = (int)p.T;
-  g.H = (int)p.H;
-  g.E = (int)p.E;
-  g.k = (int)p.k;
-  g.I = (int)p.I;
-  g.Is = (int)p.I_shared;
-  g.flags = p.flags;
-  g.limit_ns = (unsigned long long)(p.wait_limit_us ? p.wait_limit_us : 1000000u) * 1000ull;
-  g.num_sms = sms;
-
+  const GemmProblem g = gemm_problem(p);
   cudaStream_t st = (cudaStream_t)stream;
   // The status word must start each call at MOE_OK; the slot rows are all
   // overwritten by the down-projection epilogue before the combine reads them.
@@ -114,7 +95,8 @@ extern "C" moe_status moe_down_combine_noalloc(const moe_problem* pb, const void
     e = launch_down_gemm(g, h, h_shared, expert_offsets, gather_idx, topk_w, W_down, Ws_down, Y,
                          status, st);
   if (e == cudaSuccess)
-    e = launch_combine(p.out_f32 ? MOE_DTYPE_F32 : p.dtype, Y, g.T, g.H, (int)KP, y, sms, st);
+    e = launch_combine(p.out_f32 ? MOE_DTYPE_F32 : p.dtype, Y, g.T, g.H, (int)KP, y, g.num_sms,
+                       st);
   if (e == cudaSuccess && device_status) {
     int v = 0;
     e = cudaMemcpyAsync(&v, status, sizeof(int), cudaMemcpyDeviceToHost, st);

@@ -152,3 +152,33 @@ def test_workspace_layout_regions_are_disjoint_and_inside(lib, c):
     regions.sort()
     for (a0, a1, an), (b0, b1, bn) in zip(regions, regions[1:]):
         assert a1 <= b0, (an, bn)
+
+
+@pytest.mark.parametrize("dims", [
+    dict(T=1, H=1 << 22, E=1024, k=1, I=64),   # E*H = 2^32 rows of W_down
+    dict(T=1, H=128, E=1, k=1, I=1 << 31),     # I beyond int32
+    dict(T=1 << 27, H=128, E=8, k=8, I=64),    # T*(k+1) beyond the index range
+])
+def test_noalloc_rejects_index_ranges_on_host(lib, dims):
+    """moe_down_combine_noalloc applies the same int32 index limits as the
+    workspace entry points (MOE_ERR_UNSUPPORTED), before its own scratch-size
+    check and before any launch; the first case would fit the scratch array."""
+    pb = m.make_problem(dims["T"], dims["H"], dims["E"], dims["k"], dims["I"])
+    st = ctypes.c_int(-1)
+    rc = lib.moe_down_combine_noalloc(ctypes.byref(pb), 0x1000, None, 0x2000, 0x3000, 0x4000,
+                                      0x5000, None, 0x6000, None, ctypes.byref(st))
+    assert rc == 2  # MOE_ERR_UNSUPPORTED
+    assert st.value == -1  # nothing ran, nothing was written
+
+
+def test_noalloc_rejects_bad_problems_like_the_workspace_call(lib):
+    for kw in (dict(k=9, E=8), dict(H=200), dict(I=100), dict(T=-1)):
+        base = dict(T=64, H=256, E=8, k=2, I=128)
+        base.update(kw)
+        pb = m.make_problem(**base)
+        rc = lib.moe_down_combine_noalloc(ctypes.byref(pb), 0x1000, None, 0x2000, 0x3000,
+                                          0x4000, 0x5000, None, 0x6000, None, None)
+        assert rc == 1, kw
+    pb = m.make_problem(64, 256, 8, 2, 128, dtype="e4m3")
+    assert lib.moe_down_combine_noalloc(ctypes.byref(pb), 0x1000, None, 0x2000, 0x3000, 0x4000,
+                                        0x5000, None, 0x6000, None, None) == 1

@@ -5,8 +5,9 @@ the library's static scratch array instead of a caller workspace.
 
 Checked through the C ABI against the workspace entry point moe_down_combine
 on the same inputs, for two calls in a row (the static array keeps the last
-call's contents, so the second call must not depend on them), with the float
-tolerance the other parity tests use, plus the host-side size limit.
+call's contents, so the second call must not depend on them), and against the
+CPU oracle's down projection + combine on the same h and routing, with the
+float tolerance the other parity tests use; plus the host-side size limit.
 This file is collected last on purpose.
 """
 import numpy as np
@@ -15,7 +16,7 @@ import torch
 
 import mixture_experts_layer_route_gb300 as m
 from moe_inputs import MoEConfig, generate, generate_hidden, generate_routing
-from oracle import Oracle
+from oracle import Oracle, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -26,19 +27,26 @@ def _case(seed, shared):
     Is = 128 if shared else 0
     ids, w = generate_routing(T, E, k, seed=seed)
     ids = np.ascontiguousarray(ids.numpy().astype(np.int32))
-    offs, gidx, _ = Oracle().permute(ids, E, 1 if shared else 0)
+    offs, gidx, spos = Oracle().permute(ids, E, 1 if shared else 0)
     cfg = MoEConfig("n", T=T, H=H, E=E, k=k, I=I, I_shared=Is)
     d = generate(cfg, seed=seed, device=DEV, enforce_margin=False)
     h = generate_hidden(T * k, I, seed=seed + 1, device=DEV)
     hs = generate_hidden(T, Is, seed=seed + 2, device=DEV) if shared else None
     return cfg, d, h, hs, torch.from_numpy(offs).to(DEV), torch.from_numpy(gidx).to(DEV), \
-        w.to(DEV)
+        w.to(DEV), (ids, offs, spos)
+
+
+def _within_layer_bound(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    rms = float(np.sqrt(np.mean(b ** 2)))
+    return (float(np.abs(a - b).max()) <= 2e-2 * rms
+            and float(np.linalg.norm(a - b) / np.linalg.norm(b)) <= 5e-3)
 
 
 @pytest.mark.parametrize("shared", [False, True])
 def test_noalloc_matches_workspace_entry_point_twice(shared):
     for call, seed in enumerate((11, 12)):  # two calls in a row, different inputs
-        cfg, d, h, hs, offs, gidx, w = _case(seed, shared)
+        cfg, d, h, hs, offs, gidx, w, (ids, offs_np, spos) = _case(seed, shared)
         pb = m.make_problem(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.I_shared, out_f32=True)
         ws = torch.zeros(m.workspace_size(pb), dtype=torch.uint8, device=DEV)
         y_ref = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=DEV)
@@ -51,13 +59,15 @@ def test_noalloc_matches_workspace_entry_point_twice(shared):
         assert m.get_device_status(ws) == m.MOE_OK
         a, b = y.cpu().numpy().astype(np.float64), y_ref.cpu().numpy().astype(np.float64)
         assert np.isfinite(a).all(), f"call {call}: non-finite output"
-        rms = float(np.sqrt(np.mean(b ** 2)))
-        assert float(np.abs(a - b).max()) <= 2e-2 * rms, f"call {call}"
-        assert float(np.linalg.norm(a - b) / np.linalg.norm(b)) <= 5e-3, f"call {call}"
+        assert _within_layer_bound(a, b), f"call {call}: against moe_down_combine"
+        # and against the CPU oracle on the same h, routing and weights
+        ref = Oracle().down_combine(to_np(h), offs_np, spos, ids, to_np(w), to_np(d["W_down"]),
+                                    to_np(hs), to_np(d["Ws_down"]))
+        assert _within_layer_bound(a, ref), f"call {call}: against the oracle"
 
 
 def test_noalloc_bf16_output_and_no_status_request():
-    cfg, d, h, hs, offs, gidx, w = _case(13, False)
+    cfg, d, h, hs, offs, gidx, w, _ = _case(13, False)
     pb = m.make_problem(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
     ws = torch.zeros(m.workspace_size(pb), dtype=torch.uint8, device=DEV)
     y_ref = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=DEV)
