@@ -5,14 +5,20 @@ gate/up GEMM with SwiGLU, down GEMM with the weighted combine) over one batch of
 synthetic tokens whose weights and inputs are resident in HBM.
 
 Default workload: the Qwen3-235B-shaped decode step (T=64, H=4096, E=128, k=8,
-I=1536, bf16). The prefill chunk of the same layer (T=8192) is measured too and
-reported under "prefill". Every input is larger than L2 except the token batch
-itself (the expert weights are ~4.8 GB), so no L2 flush is needed between steps.
+I=1536, bf16). The other four layer shapes are measured in the same run and
+reported under "workloads" (the prefill chunk of the same layer, T=8192, also
+under "prefill"): the Qwen3.5-397B-shaped Zipf-skewed layer, the
+DeepSeek-V3-shaped layer with its shared expert, and the tiny fp32 layer. Each
+carries its own roofline, per-stage times and a sampled parity error against
+the CPU oracle. Every layer's expert weights are larger than L2 except the tiny
+layer's, whose steps are timed one by one with a 512 MiB L2 flush between them.
 
 Printed: one JSON line (rank 0). value = tokens/s of the whole job; roofline =
 the dominant kernel's achieved bandwidth or FLOP rate against the measured peak;
 layer_roofline = t_roof / t_measured for the whole layer with
-t_roof = max(routed FLOPs / bf16 peak, touched bytes / HBM bandwidth);
+t_roof = max(routed FLOPs / bf16 peak, touched bytes / HBM bandwidth), the bf16
+peak being the burst figure (the timed regions last tens of milliseconds; the
+fraction against the sustained figure is given beside it);
 e2e = the same metric through MoELayer.forward with the tokens copied from
 pinned host memory and the output copied back inside the timed region (on
 copy streams, double-buffered, overlapping the next step's compute);
@@ -215,22 +221,37 @@ def stage_sequence(layer, d, T, ws, lay, stream):
     return steps, offs
 
 
-def time_forward(layer, d, steps, warmup, stream):
+def time_forward(layer, d, steps, warmup, stream, flush=None):
+    """K steps of the layer between CUDA events on `stream`. flush: a buffer
+    larger than L2 written between steps, outside the timed intervals (the
+    steps are then timed one by one and their durations summed)."""
     x = d["x"]
     T = x.shape[0]
     y = torch.empty(T, layer.H, dtype=layer.dtype, device=x.device)
     for _ in range(warmup):
         layer.forward(x, out=y, stream=stream)
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    if flush is None:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(steps):
+                layer.forward(x, out=y, stream=stream)
+                ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+        return ev[0].elapsed_time(ev[-1]), per
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     with torch.cuda.stream(stream):
-        ev[0].record(stream)
         for i in range(steps):
+            flush.fill_(i & 0xFF)
+            e0[i].record(stream)
             layer.forward(x, out=y, stream=stream)
-            ev[i + 1].record(stream)
+            e1[i].record(stream)
     torch.cuda.synchronize()
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
-    return ev[0].elapsed_time(ev[-1]), per
+    per = [e0[i].elapsed_time(e1[i]) for i in range(steps)]
+    return sum(per), per
 
 
 def time_stages(layer, d, steps, warmup, stream):
@@ -338,6 +359,48 @@ def time_graph(layer, d, steps, warmup, stream):
     return e0.elapsed_time(e1)
 
 
+def parity_sample(cfg, layer, d, n_tokens=8):
+    """The layer's fp32 output (out_f32) on n_tokens tokens spread over the
+    batch, against the CPU oracle on the same tokens (router, top-k, experts,
+    combine; only the experts those tokens use are copied to the host, one
+    token at a time). Also checks that the routed ids agree."""
+    import numpy as np
+
+    import mixture_experts_layer_route_gb300 as m
+    import oracle
+    o = oracle.Oracle()
+    T = cfg.T
+    y = layer.forward(d["x"], out_f32=True)
+    ws = layer.workspace(T)
+    lay = m.workspace_layout(layer.problem(T, out_f32=True))
+    ids_gpu = ws[lay["topk_ids"]:lay["topk_ids"] + T * cfg.k * 4].view(torch.int32)
+    ids_gpu = ids_gpu.view(T, cfg.k).cpu().numpy()
+    torch.cuda.synchronize()
+    toks = sorted({int(i * T / n_tokens) for i in range(n_tokens)} | {T - 1})
+    Wr, bias = oracle.to_np(d["W_router"]), oracle.to_np(d["router_bias"])
+    sh = [oracle.to_np(d[n]) for n in ("Ws_gate", "Ws_up", "Ws_down")]
+    max_abs, ss_d, ss_r, sq, ids_ok = 0.0, 0.0, 0.0, 0.0, True
+    for t in toks:
+        xt = oracle.to_np(d["x"][t:t + 1])
+        ids, w = o.route(o.router_logits(xt, Wr, bias), cfg.k, cfg.renorm)
+        ids_ok &= bool((ids[0] == ids_gpu[t]).all())
+        sel = torch.from_numpy(ids[0].astype(np.int64)).to(d["W_gate"].device)
+        ref = o.ffn_combine(xt, np.arange(cfg.k, dtype=np.int32)[None, :].copy(), w,
+                            oracle.to_np(d["W_gate"][sel]), oracle.to_np(d["W_up"][sel]),
+                            oracle.to_np(d["W_down"][sel]), *sh)[0].astype(np.float64)
+        got = y[t].float().cpu().numpy().astype(np.float64)
+        max_abs = max(max_abs, float(np.abs(got - ref).max()))
+        ss_d += float(((got - ref) ** 2).sum())
+        ss_r += float((ref ** 2).sum())
+        sq += ref.size
+    rms = (ss_r / sq) ** 0.5
+    return {"tokens": len(toks), "max_abs_over_rms": max_abs / rms,
+            "rel_l2": (ss_d / ss_r) ** 0.5, "ids_match": ids_ok,
+            "bound": {"max_abs_over_rms": 2e-2, "rel_l2": 5e-3},
+            "how": "fp32 y (out_f32) of the timed layer on tokens spread over the batch "
+                   "against the CPU oracle"}
+
+
 def cpu_baseline(cfg, d, budget_s=10.0, max_tokens=None):
     """The CPU oracle, as it stands, on a bounded sample of tokens of the same
     layer: tokens/s over ~budget_s seconds of oracle work."""
@@ -421,34 +484,49 @@ def job_tokens_per_s(world, T, steps, ms_total):
     return world * T * steps / (ms_total / 1e3)
 
 
-def measure_config(cfg, args, world, local, with_clocks):
+L2_BYTES = 129 * 2 ** 20
+
+
+def fits_l2(cfg):
+    """True when the layer's weights and tokens could stay in L2 between steps."""
+    w = cfg.E * 3 * cfg.H * cfg.I + 3 * cfg.H * cfg.I_shared + cfg.E * cfg.H
+    return (w + 2 * cfg.T * cfg.H) * cfg.elem_bytes < 2 * L2_BYTES
+
+
+def measure_config(cfg, args, world, local, with_clocks, parity_tokens=8):
     import mixture_experts_layer_route_gb300 as m
     stream = torch.cuda.Stream()
     layer, d = build_layer(cfg, "cuda", seed=args.seed)
     layer.workspace(cfg.T)
     steps = args.steps if cfg.T <= 1024 else max(3, args.steps // 8)
+    flush = (torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+             if fits_l2(cfg) else None)
     # timed region: K steps of moe_forward
     sampler = ClockSampler(local) if with_clocks else None
     barrier(world)
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    ms_total, per = time_forward(layer, d, steps, args.warmup, stream)
+    ms_total, per = time_forward(layer, d, steps, args.warmup, stream, flush)
     clocks = sampler.stop() if sampler else None
     barrier(world)
     ms_total = max_over_ranks(ms_total, world)
     st = m.get_device_status(layer.workspace(cfg.T), stream)
     if st != m.MOE_OK:
         raise RuntimeError(f"device status {m.status_string(st)}")
+    del flush
     # per-kernel durations (same kernels, issued stage by stage between events)
     per_stage, counts = time_stages(layer, d, steps, args.warmup, stream)
     e2e_ms, h2d, d2h = time_e2e(layer, d, steps, args.warmup, stream)
     e2e_ms = max_over_ranks(e2e_ms, world)
     graph_ms = max_over_ranks(time_graph(layer, d, steps, args.warmup, stream), world)
     rl = roofline_numbers(cfg, counts.numpy())
+    parity = parity_sample(cfg, layer, d, parity_tokens) if parity_tokens else None
     out = dict(cfg=cfg, steps=steps, ms_total=ms_total, per=per, per_stage=per_stage,
                counts=counts, rl=rl, clocks=clocks, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
-               graph_ms=graph_ms,
+               graph_ms=graph_ms, parity=parity,
+               l2="flushed between steps (512 MiB write, outside the timed intervals)"
+               if fits_l2(cfg) else "inputs larger than L2 (expert weights), no flush",
                layer=layer, d=d)
     return out
 
@@ -457,7 +535,8 @@ def measure_fp8(cfg, args, world, peaks):
     """The same workload with E4M3 expert weights (moe_forward_fp8): weights
     quantized once, K timed steps of the layer. Roofline: weight bytes are one
     per element plus a 4-byte scale per row; the FP8 tensor peak is the
-    measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25 = 2)."""
+    measured bf16 burst peak times the nominal fp8/bf16 ratio (4.5 / 2.25 = 2),
+    the fraction against the sustained figure beside it."""
     import mixture_experts_layer_route_gb300 as m
     stream = torch.cuda.Stream()
     d = generate(cfg, seed=args.seed, device="cuda")
@@ -486,21 +565,27 @@ def measure_fp8(cfg, args, world, peaks):
     flop_layer = 2.0 * T * k * 3 * H * I + 2.0 * T * 3 * H * Is
     ms_step = ms_total / steps
     t_mem = bytes_layer / (peaks["hbm_gbs"] * 1e9) * 1e3
-    p8 = 2.0 * peaks["bf16_tflops_sustained"]
+    p8 = 2.0 * peaks["bf16_tflops"]
     t_tc = flop_layer / (p8 * 1e12) * 1e3
     t_roof = max(t_mem, t_tc)
+    t_roof_sus = max(t_mem, flop_layer / (2e12 * peaks["bf16_tflops_sustained"]) * 1e3)
     return {"value": world * T * steps / (ms_total / 1e3), "unit": "tokens/s",
             "ms_per_step": ms_step, "median_ms": statistics.median(per),
             "weights": "E4M3, one power-of-two scale per row (moe_forward_fp8)",
             "layer_roofline": {"t_roof_ms": t_roof, "bound": "hbm" if t_mem >= t_tc else "tensor",
-                               "frac": t_roof / ms_step, "bytes_touched": bytes_layer,
+                               "frac": t_roof / ms_step, "frac_vs_sustained": t_roof_sus / ms_step,
+                               "bytes_touched": bytes_layer,
                                "flop_routed": flop_layer, "fp8_peak_tflops": p8,
-                               "fp8_peak_source": "2 x measured bf16_tflops_sustained (nominal "
+                               "fp8_peak_source": "2 x measured bf16_tflops (burst; nominal "
                                                   "fp8/bf16 ratio)"},
             "experts_touched": touched}
 
 
 def summarize(r, peaks, world, prefix_src):
+    """Throughput, the layer's roofline fraction and the dominant kernel's
+    roofline for one measured workload. The tensor peak is the measured burst
+    bf16 figure (each timed region lasts tens of milliseconds); fractions
+    against the sustained figure are given beside it."""
     cfg = r["cfg"]
     steps = r["steps"]
     ms_step = r["ms_total"] / steps
@@ -509,22 +594,24 @@ def summarize(r, peaks, world, prefix_src):
     st = dict(zip(STAGES, r["per_stage"]))
     g_ms = st["swiglu_gemm"]
     hbm = peaks["hbm_gbs"]
-    tc = peaks["bf16_tflops_sustained"]
+    tc, tc_sus = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
     t_mem = rl["bytes_layer"] / (hbm * 1e9) * 1e3
     t_tc = rl["flop_layer"] / (tc * 1e12) * 1e3
     t_roof = max(t_mem, t_tc)
+    t_roof_sus = max(t_mem, rl["flop_layer"] / (tc_sus * 1e12) * 1e3)
     bound = "hbm" if t_mem >= t_tc else "tensor"
+    kname = f"grouped_gemm_kernel<{cfg.dtype},gated>"
     if bound == "hbm":
         ach = rl["bytes_gated"] / (g_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": "grouped_gemm_kernel<bf16,gated>", "achieved": ach,
+        roof = {"bound": "hbm", "kernel": kname, "achieved": ach,
                 "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                 "algorithmic_bytes_per_launch": rl["bytes_gated"]}
     else:
         ach = rl["flop_gated"] / (g_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": "grouped_gemm_kernel<bf16,gated>", "achieved": ach,
-                "peak": tc, "unit": "TFLOP/s", "frac": ach / tc,
+        roof = {"bound": "tensor", "kernel": kname, "achieved": ach,
+                "peak": tc, "unit": "TFLOP/s", "frac": ach / tc, "frac_vs_sustained": ach / tc_sus,
                 "algorithmic_flops_per_launch": rl["flop_gated"]}
-    roof["peak_source"] = f"{prefix_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops_sustained'})"
+    roof["peak_source"] = f"{prefix_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops, burst'})"
     roof["kernel_ms"] = g_ms
     roof["traffic"] = traffic_for(cfg.name, "swiglu_gemm")
     counts = r["counts"].numpy()
@@ -535,8 +622,9 @@ def summarize(r, peaks, world, prefix_src):
         p90_ms=sorted(r["per"])[(9 * len(r["per"])) // 10],
         roofline=roof,
         layer_roofline={"t_roof_ms": t_roof, "bound": bound, "frac": t_roof / ms_step,
-                         "flop_routed": rl["flop_layer"], "bytes_touched": rl["bytes_layer"],
-                         "experts_touched": rl["touched"]},
+                        "frac_vs_sustained": t_roof_sus / ms_step,
+                        "flop_routed": rl["flop_layer"], "bytes_touched": rl["bytes_layer"],
+                        "experts_touched": rl["touched"]},
         stages_ms=st,
         expert_load={"touched": int(len(loads)), "empty": int((counts == 0).sum()),
                      "max": int(counts.max()), "mean": float(counts.mean()),
@@ -548,7 +636,21 @@ def summarize(r, peaks, world, prefix_src):
                "ms_per_step": r["graph_ms"] / steps,
                "layer_roofline_frac": t_roof / (r["graph_ms"] / steps),
                "how": "the same moe_forward captured once in a CUDA graph, replayed"},
+        parity=r["parity"], l2=r["l2"],
     )
+
+
+WORKLOAD_ORDER = ["qwen3_235b_prefill", "qwen35_397b_zipf", "deepseek_v3", "tiny_f32"]
+
+
+def workload_entry(cfg, s, fp8):
+    return {"config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
+                       "I": cfg.I, "I_shared": cfg.I_shared, "dtype": cfg.dtype,
+                       "zipf_s": cfg.zipf_s, "l2": s["l2"]},
+            **{k: s[k] for k in ("value", "ms_per_step", "median_ms", "roofline",
+                                 "layer_roofline", "stages_ms", "expert_load", "graph", "e2e",
+                                 "parity")},
+            "unit": "tokens/s", "steps": s["steps"], "fp8": fp8}
 
 
 def run_native(args):
@@ -560,28 +662,33 @@ def run_native(args):
     barrier(world)
     peaks, src = load_peaks()
     cfg = ALL_CONFIGS[args.config]
-    r = measure_config(cfg, args, world, local, with_clocks=True)
+    r = measure_config(cfg, args, world, local, with_clocks=True,
+                       parity_tokens=args.parity_tokens if rank == 0 else 0)
     s = summarize(r, peaks, world, src)
     clocks = r["clocks"]
-    prefill = None
-    if args.prefill and args.config != "qwen3_235b_prefill":
-        del r
-        torch.cuda.empty_cache()
-        rp = measure_config(CONFIGS["qwen3_235b_prefill"], args, world, local,
-                            with_clocks=False)
-        sp = summarize(rp, peaks, world, src)
-        prefill = {"config": {"workload": "qwen3_235b_prefill", "T": 8192, "H": 4096, "E": 128,
-                              "k": 8, "I": 1536},
-                   **{k: sp[k] for k in ("value", "ms_per_step", "roofline", "layer_roofline",
-                                         "stages_ms", "expert_load", "graph")}}
-        del rp
-        if args.fp8:
-            torch.cuda.empty_cache()
-            prefill["fp8"] = measure_fp8(CONFIGS["qwen3_235b_prefill"], args, world, peaks)
+    del r
     fp8 = None
     if args.fp8 and cfg.dtype == "bf16" and cfg.I % 128 == 0 and cfg.I_shared % 128 == 0:
         torch.cuda.empty_cache()
         fp8 = measure_fp8(cfg, args, world, peaks)
+    # The other layer shapes, each measured the same way (one at a time: the
+    # DeepSeek-V3-shaped layer alone holds ~23 GB of weights).
+    others = {}
+    names = [n for n in WORKLOAD_ORDER if n != args.config] if args.all_workloads else []
+    if args.prefill and not args.all_workloads and args.config != "qwen3_235b_prefill":
+        names = ["qwen3_235b_prefill"]
+    for name in names:
+        torch.cuda.empty_cache()
+        c = CONFIGS[name]
+        rp = measure_config(c, args, world, local, with_clocks=False,
+                            parity_tokens=args.parity_tokens if rank == 0 else 0)
+        sp = summarize(rp, peaks, world, src)
+        del rp
+        f8 = None
+        if args.fp8 and c.dtype == "bf16" and c.I % 128 == 0 and c.I_shared % 128 == 0:
+            torch.cuda.empty_cache()
+            f8 = measure_fp8(c, args, world, peaks)
+        others[name] = workload_entry(c, sp, f8)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         torch.cuda.empty_cache()
@@ -590,6 +697,7 @@ def run_native(args):
         del layer, d
     if rank != 0:
         return
+    n_launch = kernels_per_step(cfg) * s["steps"]
     line = {
         "metric": "MoE-layer tokens/sec at 1 GB300 (decode & prefill) + % of HBM / bf16-TC roofline",
         "value": s["value"], "unit": "tokens/s", "n_gpus": world, "steps": s["steps"],
@@ -598,15 +706,16 @@ def run_native(args):
         "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
                    "I": cfg.I, "I_shared": cfg.I_shared, "renorm": cfg.renorm,
-                   "seed": args.seed, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (expert weights), no flush"},
+                   "seed": args.seed, "parallelism": f"replicas{world}", "l2": s["l2"]},
         "median_ms": s["median_ms"], "p10_ms": s["p10_ms"], "p90_ms": s["p90_ms"],
         "roofline": s["roofline"], "layer_roofline": s["layer_roofline"],
         "stages_ms": s["stages_ms"], "expert_load": s["expert_load"],
-        "e2e": s["e2e"], "graph": s["graph"], "fp8": fp8,
-        "gpu_launches": kernels_per_step(cfg) * s["steps"],
+        "e2e": s["e2e"], "graph": s["graph"], "fp8": fp8, "parity": s["parity"],
+        "gpu_launches": n_launch,
         "clocks": clocks,
-        "cpu_baseline": cpu, "prefill": prefill,
+        "cpu_baseline": cpu,
+        "prefill": others.get("qwen3_235b_prefill"),
+        "workloads": {k: v for k, v in others.items() if k != "qwen3_235b_prefill"},
     }
     print(json.dumps(line))
 
@@ -656,7 +765,12 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="qwen3_235b_decode", choices=sorted(ALL_CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false",
+                    help="with --no-other-workloads: skip the prefill chunk too")
+    ap.add_argument("--no-other-workloads", dest="all_workloads", action="store_false",
+                    help="measure only the headline workload (and the prefill chunk)")
+    ap.add_argument("--parity-tokens", type=int, default=8,
+                    help="tokens per workload checked against the CPU oracle (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", dest="fp8", action="store_false",
                     help="skip the E4M3-weight measurement of the same workload")
