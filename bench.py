@@ -674,9 +674,10 @@ def run_native(args):
     # The other layer shapes, each measured the same way (one at a time: the
     # DeepSeek-V3-shaped layer alone holds ~23 GB of weights).
     others = {}
-    names = [n for n in WORKLOAD_ORDER if n != args.config] if args.all_workloads else []
-    if args.prefill and not args.all_workloads and args.config != "qwen3_235b_prefill":
-        names = ["qwen3_235b_prefill"]
+    names = []
+    if args.prefill:
+        names = WORKLOAD_ORDER if args.all_workloads else ["qwen3_235b_prefill"]
+        names = [n for n in names if n != args.config]
     for name in names:
         torch.cuda.empty_cache()
         c = CONFIGS[name]
@@ -766,9 +767,9 @@ def main():
     ap.add_argument("--config", default="qwen3_235b_decode", choices=sorted(ALL_CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-prefill", dest="prefill", action="store_false",
-                    help="with --no-other-workloads: skip the prefill chunk too")
+                    help="measure the chosen workload alone (no other layer shape)")
     ap.add_argument("--no-other-workloads", dest="all_workloads", action="store_false",
-                    help="measure only the headline workload (and the prefill chunk)")
+                    help="besides the chosen workload, measure only the prefill chunk")
     ap.add_argument("--parity-tokens", type=int, default=8,
                     help="tokens per workload checked against the CPU oracle (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

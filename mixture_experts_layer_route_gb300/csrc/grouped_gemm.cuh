@@ -7,9 +7,10 @@
 // positions [offsets[e], offsets[e+1]) of the permutation; group E is the
 // shared expert with one row per token.
 //
-// Orientation: the weights are the MMA's M = 128 operand and the tokens its N
-// operand ("swap AB"). N is chosen per tile at run time as the segment's
-// remaining rows rounded up to 16, so a ragged segment wastes at most 15
+// Orientation: the weights are the MMA's M = 128 operand (256 on CTA pairs)
+// and the tokens its N operand ("swap AB"). N is chosen per tile at run time as
+// the segment's remaining rows rounded up to 16 (32 on CTA pairs, whose halves
+// must each be a multiple of 16), so a ragged segment wastes at most 15 (31)
 // columns, and a decode-sized segment (a handful of tokens) streams its
 // expert's weights with a narrow N. The persistent tile scheduler reads the
 // per-expert counts from device memory (no host round trip), as the same page
@@ -17,9 +18,11 @@
 //
 // Two products share the engine:
 //  GATED (step a4, SwiGLU fused): A = 64 rows of W_gate[e] stacked over the
-//    same 64 rows of W_up[e]; B = token rows of x gathered by TMA
-//    (tile::gather4, indices from the permutation; no gathered copy of x
-//    exists). Accumulator lanes 0-63 hold gate, 64-127 up; the epilogue
+//    same 64 rows of W_up[e]; B = the routed token rows: for 32-token decode
+//    tiles gathered from x by TMA (tile::gather4, indices from the
+//    permutation, no copy of x), for larger tiles read from their
+//    expert-ordered copy (the dispatch copy made by gather_rows_kernel, T*k
+//    rows, unpadded). Accumulator lanes 0-63 hold gate, 64-127 up; the epilogue
 //    computes silu(gate) * up and stores h rows (Qwen3.5-397B on TPU v7x,
 //    4.2.1 ragged gather and 4.2.2 grouped GEMM with fused SwiGLU).
 //  DOWN (step a5): A = 128 rows of W_down[e]; B = rows of h (contiguous
