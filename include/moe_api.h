@@ -199,6 +199,33 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
                        const void* Ws_down, void* y, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/* The whole layer (a1 .. a5, a6) as ONE kernel launch, for decode-sized
+ * batches: the single-launch decode path ("Lower latency and higher throughput
+ * with multi-node DeepSeek deployment", its CUDA-Graph paragraph: persistent
+ * kernels that read the per-expert counts on the device; "CuTeDSL at
+ * Perplexity": small-batch dispatch inside the kernel that moves the data).
+ * Same arguments, layouts, workspace and results as moe_forward: routing ids
+ * and the permutation are the same function of the logits; the logits are fp32
+ * sums of the same products in another order (one warp per (token, expert),
+ * lane-sequential then a fixed butterfly), and y the same computation. One
+ * cooperative persistent kernel with one CTA per SM runs: each token's logits
+ * and top-k on its own CTA; a grid barrier; the permutation; the gate/up GEMM;
+ * the down GEMM, whose units start on an expert as soon as all of that
+ * expert's gate/up units are stored (no kernel boundary between the GEMMs); a
+ * second grid barrier; the combine. Every cross-CTA wait is bounded by
+ * wait_limit_us and reports MOE_ERR_TIMEOUT in the device status.
+ * Takes problems that use the 32-token decode tiles (tile AUTO with T <= 64,
+ * or DECODE) with dtype bf16 or fp32, T at most the SM count, and whose shared
+ * memory fits one CTA per SM (E and T*k not too large); returns
+ * MOE_ERR_UNSUPPORTED otherwise, or on a device without cooperative launch.
+ * Enqueues a clear of the workspace header (status word and barrier counter)
+ * and the one kernel on `stream`. */
+moe_status moe_forward_single_launch(const moe_problem* pb, const void* x, const void* W_router,
+                                     const float* router_bias, const void* W_gate,
+                                     const void* W_up, const void* W_down, const void* Ws_gate,
+                                     const void* Ws_up, const void* Ws_down, void* y,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* moe_down_combine without a workspace, for callers that cannot allocate
  * device memory (a host that passes the layer only its inputs and outputs, a
  * plugin not allowed to call cudaMalloc, a fixed memory budget). It computes

@@ -14,7 +14,8 @@ import torch
 from ._binding import (  # noqa: F401
     EXPORTED, MOE_DTYPE_BF16, MOE_DTYPE_E4M3, MOE_DTYPE_F32, MOE_FLAG_TEST_SKIP_SIGNAL, MOE_OK,
     MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_MEDIUM, MOE_TILE_PREFILL, STATUS_NAMES, MoEError, MoEProblem,
-    down_combine, down_combine_noalloc, forward, forward_fp8, get_device_status, grouped_swiglu_gemm, load_library, make_problem,
+    down_combine, down_combine_noalloc, forward, forward_fp8, forward_single_launch,
+    get_device_status, grouped_swiglu_gemm, load_library, make_problem,
     permute, quantize_rows_e4m3, reset_device_status, route, route_grouped, router_logits,
     status_string, workspace_layout,
     workspace_size)
@@ -57,15 +58,17 @@ class MoELayer:
             self._ws[T] = ws
         return ws
 
-    def forward(self, x, out=None, stream=None, out_f32=False):
+    def forward(self, x, out=None, stream=None, out_f32=False, single_launch=False):
         """y = the layer applied to x [T,H]. out_f32: return y in fp32 (the value
-        before its final rounding to a bf16 layer's dtype)."""
+        before its final rounding to a bf16 layer's dtype). single_launch: run
+        moe_forward_single_launch (one kernel; decode-sized batches only)."""
         T = x.shape[0]
         odt = torch.float32 if out_f32 else self.dtype
         y = out if out is not None else torch.empty((T, self.H), dtype=odt, device=x.device)
-        forward(self.problem(T, out_f32=out_f32), x, self.W_router, self.router_bias,
-                self.W_gate, self.W_up, self.W_down, self.Ws_gate, self.Ws_up, self.Ws_down, y,
-                self.workspace(T), stream)
+        fn = forward_single_launch if single_launch else forward
+        fn(self.problem(T, out_f32=out_f32), x, self.W_router, self.router_bias,
+           self.W_gate, self.W_up, self.W_down, self.Ws_gate, self.Ws_up, self.Ws_down, y,
+           self.workspace(T), stream)
         return y
 
     __call__ = forward

@@ -28,7 +28,7 @@ EXPORTED = ("moe_workspace_size", "moe_router_logits", "moe_route", "moe_route_g
             "moe_grouped_swiglu_gemm", "moe_down_combine", "moe_forward",
             "moe_get_workspace_layout", "moe_get_device_status", "moe_reset_device_status",
             "moe_status_string", "moe_down_combine_noalloc", "moe_quantize_rows_e4m3",
-            "moe_forward_fp8")
+            "moe_forward_fp8", "moe_forward_single_launch")
 
 
 class MoEError(RuntimeError):
@@ -80,6 +80,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                         ctypes.c_size_t, _P],
             "moe_down_combine": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
             "moe_forward": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+            "moe_forward_single_launch": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          ctypes.c_size_t, _P],
             "moe_get_workspace_layout": [pb, ctypes.POINTER(MoEWorkspaceLayout)],
             "moe_get_device_status": [_P, _P, ctypes.POINTER(ctypes.c_int)],
             "moe_reset_device_status": [_P, _P],
@@ -221,6 +223,16 @@ def forward_fp8(problem, x, W_router, router_bias, Wq_gate, s_gate, Wq_up, s_up,
 def forward(problem, x, W_router, router_bias, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, y,
             workspace, stream=None):
     _check("moe_forward", load_library().moe_forward(
+        ctypes.byref(problem), _ptr(x), _ptr(W_router), _ptr(router_bias), _ptr(W_gate),
+        _ptr(W_up), _ptr(W_down), _ptr(Ws_gate), _ptr(Ws_up), _ptr(Ws_down), _ptr(y),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def forward_single_launch(problem, x, W_router, router_bias, W_gate, W_up, W_down, Ws_gate,
+                          Ws_up, Ws_down, y, workspace, stream=None):
+    """moe_forward as one kernel launch (decode-sized batches); raises
+    MoEError(MOE_ERR_UNSUPPORTED) for problems it does not take."""
+    _check("moe_forward_single_launch", load_library().moe_forward_single_launch(
         ctypes.byref(problem), _ptr(x), _ptr(W_router), _ptr(router_bias), _ptr(W_gate),
         _ptr(W_up), _ptr(W_down), _ptr(Ws_gate), _ptr(Ws_up), _ptr(Ws_down), _ptr(y),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -85,6 +85,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Invalidates an mbarrier whose phases are all complete and no longer waited
+// on, so that its word may be initialised again.
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -115,6 +121,53 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (read_status(status) != MOE_OK) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        set_status(status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ cross-CTA signals
+// (single-launch decode kernel: all CTAs are co-resident, cooperative launch)
+
+// Orders this thread's earlier generic-proxy global accesses with its later
+// async-proxy (TMA) ones, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits until *p >= need (acquire). Bounded like mbar_wait: gives up after
+// limit_ns, recording MOE_ERR_TIMEOUT, or once the status word is set.
+__device__ __forceinline__ bool wait_count_at_least(const int* p, int need, int* status,
+                                                    uint64_t limit_ns) {
+  if (ld_acquire_gpu(p) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_gpu(p) >= need) return true;
     if ((it & 15u) == 0) {
       if (read_status(status) != MOE_OK) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -386,12 +439,17 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // Whole-warp TMEM allocation; the column base address is written to smem.
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+// relinquish: give up the CTA's right to allocate again (a CTA that allocates
+// once more later, as the single-launch decode kernel's second GEMM pass does,
+// keeps it until its last allocation).
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols,
+                                           bool relinquish = true) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    dst_smem),
                "r"(ncols)
                : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if (relinquish)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {

@@ -210,18 +210,21 @@ cudaError_t launch_down(const GroupedGemmArgs& a, const GemmProblem& p, bool dec
 
 bool tensor_map_encoder_available() { return encoder() != nullptr; }
 
+bool gemm_uses_decode_tiles(const GemmProblem& p) { return use_decode_kernel(p); }
+
 bool gemm_needs_expert_order_copy(const GemmProblem& p) { return !use_decode_kernel(p); }
 
-cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* xg,
-                               const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
-                               const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,
-                               int* status, cudaStream_t st, const GemmScales* sc) {
+// Arguments of the gate/up GEMM (see kernels.h); false if a tensor map
+// cannot be made.
+bool prepare_swiglu_gemm(GroupedGemmArgs& a, const GemmProblem& p, const void* x, const void* xg,
+                         const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
+                         const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,
+                         int* status, const GemmScales* sc) {
   const bool has_s = p.Is > 0;
   const bool dec = use_decode_kernel(p);
   // CTA pairs when every group has an even number of 64-row feature blocks.
   const bool pair = !dec && (p.I / 64) % 2 == 0 && (!has_s || (p.Is / 64) % 2 == 0);
   const int tile_n = dec ? 32 : tiled_tile_n(p);
-  GroupedGemmArgs a;
   memset(&a, 0, sizeof(a));
   bool ok = make_tma_map(&a.tmA[0], Wg, p.dtype, (uint64_t)p.E * p.I, p.H, 64) &&
             make_tma_map(&a.tmA[1], Wu, p.dtype, (uint64_t)p.E * p.I, p.H, 64);
@@ -232,13 +235,13 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
     if (dec) {
       ok = make_tma_map(&a.tmB[0], x, p.dtype, p.T, p.H, 1);
     } else {  // [0..2]: routed rows in expert order; [3..5]: x itself for the shared expert
-      if (!xg) return cudaErrorInvalidValue;
+      if (!xg) return false;
       const uint32_t br = pair ? tile_n / 2 : 256, b1 = br / 2;
       ok = make_b_maps(&a.tmB[0], xg, p.dtype, (uint64_t)p.T * p.k, p.H, br, b1) &&
            make_b_maps(&a.tmB[3], x, p.dtype, p.T, p.H, br, b1);
     }
   }
-  if (!ok) return cudaErrorInvalidValue;
+  if (!ok) return false;
   if (!has_s) {
     a.tmA[2] = a.tmA[0];
     a.tmA[3] = a.tmA[1];
@@ -260,6 +263,20 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
   a.kdim_shared = p.H;
   a.ld_out_routed = p.I;
   a.ld_out_shared = has_s ? p.Is : 0;
+  return true;
+}
+
+cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* xg,
+                               const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
+                               const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,
+                               int* status, cudaStream_t st, const GemmScales* sc) {
+  GroupedGemmArgs a;
+  if (!prepare_swiglu_gemm(a, p, x, xg, offsets, gather_idx, Wg, Wu, Wsg, Wsu, h, hs, status, sc))
+    return cudaErrorInvalidValue;
+  const bool has_s = p.Is > 0;
+  const bool dec = use_decode_kernel(p);
+  const bool pair = !dec && (p.I / 64) % 2 == 0 && (!has_s || (p.Is / 64) % 2 == 0);
+  const int tile_n = a.tile_n;
   const int rb = p.I / 64, sb = has_s ? p.Is / 64 : 0;
   const size_t ub = unit_upper_bound(p.T, p.k, p.E, tile_n, rb, sb);
   switch (p.dtype) {
@@ -272,24 +289,25 @@ cudaError_t launch_swiglu_gemm(const GemmProblem& p, const void* x, const void* 
   }
 }
 
-cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
-                             const int32_t* offsets, const int32_t* gather_idx,
-                             const float* topk_w, const void* Wd, const void* Wsd, float* Y,
-                             int* status, cudaStream_t st, const GemmScales* sc) {
+// Arguments of the down GEMM (see kernels.h); false if a tensor map cannot be
+// made.
+bool prepare_down_gemm(GroupedGemmArgs& a, const GemmProblem& p, const void* h, const void* hs,
+                       const int32_t* offsets, const int32_t* gather_idx, const float* topk_w,
+                       const void* Wd, const void* Wsd, float* Y, int* status,
+                       const GemmScales* sc) {
   const bool has_s = p.Is > 0;
   const bool dec = use_decode_kernel(p);
   const bool pair = !dec && (p.H / 128) % 2 == 0;
   const int tile_n = dec ? 32 : tiled_tile_n(p);
   // Token boxes: B_ROWS and BOX1 of the variant launched (decode: 32 and 16).
   const uint32_t br = dec ? 32 : (pair ? tile_n / 2 : 256), b1 = br / 2 < 16 ? 16 : br / 2;
-  GroupedGemmArgs a;
   memset(&a, 0, sizeof(a));
   bool ok = make_tma_map(&a.tmA[0], Wd, p.dtype, (uint64_t)p.E * p.H, p.I, 128) &&
             make_b_maps(&a.tmB[0], h, p.dtype, (uint64_t)p.T * p.k, p.I, br, b1);
   if (ok && has_s)
     ok = make_tma_map(&a.tmA[2], Wsd, p.dtype, p.H, p.Is, 128) &&
          make_b_maps(&a.tmB[3], hs, p.dtype, p.T, p.Is, br, b1);
-  if (!ok) return cudaErrorInvalidValue;
+  if (!ok) return false;
   if (!has_s) {
     a.tmA[2] = a.tmA[0];
     for (int i = 0; i < 3; ++i) a.tmB[3 + i] = a.tmB[i];
@@ -313,6 +331,20 @@ cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs
   a.kdim_shared = has_s ? p.Is : p.I;
   a.ld_out_routed = p.H;
   a.ld_out_shared = p.H;
+  return true;
+}
+
+cudaError_t launch_down_gemm(const GemmProblem& p, const void* h, const void* hs,
+                             const int32_t* offsets, const int32_t* gather_idx,
+                             const float* topk_w, const void* Wd, const void* Wsd, float* Y,
+                             int* status, cudaStream_t st, const GemmScales* sc) {
+  GroupedGemmArgs a;
+  if (!prepare_down_gemm(a, p, h, hs, offsets, gather_idx, topk_w, Wd, Wsd, Y, status, sc))
+    return cudaErrorInvalidValue;
+  const bool has_s = p.Is > 0;
+  const bool dec = use_decode_kernel(p);
+  const bool pair = !dec && (p.H / 128) % 2 == 0;
+  const int tile_n = a.tile_n;
   const int rb = p.H / 128, sb = has_s ? p.H / 128 : 0;
   const size_t ub = unit_upper_bound(p.T, p.k, p.E, tile_n, rb, sb);
   switch (p.dtype) {

@@ -107,6 +107,13 @@ struct GroupedGemmArgs {
   // kernel. pf_base: raw routed A operands (GATED: gate, up; DOWN: down, unused).
   int pf_first;
   const void* pf_base[2];
+  // Single-launch decode kernel only (nullptr otherwise; see fused_decode.cu).
+  // GATED: unit_done[g] counts group g's finished units (h rows stored).
+  // DOWN: before loading a unit's h rows, wait until unit_wait[g] holds all of
+  // group g's gate/up units: ceil(rows / tile_n) * (kdim / wait_block) of them.
+  int* unit_done;
+  const int* unit_wait;
+  int wait_block;
 };
 
 enum BMode : int { kGather4 = 0, kTiled = 2 };
@@ -166,6 +173,31 @@ struct Tile {
 // Bytes per L2 bulk prefetch instruction of the pre-wait weight prefetch.
 constexpr size_t kPrefetchChunk = 32768;
 
+// The pre-wait weight prefetch of a single-CTA GEMM (pf_first, see the pass
+// below): lanes of one warp ask L2 for the WM weight rows (gate and up, or
+// down) of CTA cid's likely first unit, feature block cid % nf of expert
+// cid / nf. A hint only.
+template <typename TIn, bool GATED, int WM>
+__device__ __forceinline__ void prefetch_first_unit(const GroupedGemmArgs& args, int cid,
+                                                    int lane) {
+  if (!args.pf_first) return;
+  const int nf = args.n_out_routed / WM;
+  const int g = cid / nf;
+  if (g >= args.E) return;
+  const size_t row_bytes = (size_t)args.kdim_routed * sizeof(TIn);
+  const size_t bytes = (size_t)WM * row_bytes;
+  const size_t first = ((size_t)g * args.n_out_routed + (size_t)(cid - g * nf) * WM) * row_bytes;
+  constexpr int NOP = GATED ? 2 : 1;
+  const int nch = (int)((bytes + kPrefetchChunk - 1) / kPrefetchChunk);
+  for (int c = lane; c < NOP * nch; c += 32) {
+    const int op = c / nch;
+    const size_t off = (size_t)(c - op * nch) * kPrefetchChunk;
+    const size_t rem = bytes - off;
+    prefetch_l2_bulk(static_cast<const uint8_t*>(args.pf_base[op]) + first + off,
+                     (uint32_t)(rem < kPrefetchChunk ? rem : kPrefetchChunk));
+  }
+}
+
 // Position i of the round-robin deal -> unit of the class-ordered list, whose
 // first uh units belong to groups of more than 128 rows (tensor-bound tiles)
 // and the rest to lighter groups (weight-streaming tiles). The heavy units are
@@ -207,15 +239,33 @@ __device__ __forceinline__ Tile decode_tile(int u, const int32_t* prefix, const 
   return t;
 }
 
-template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL>
-__global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ GroupedGemmArgs args) {
-  pdl_trigger();
+// One pass of a grouped GEMM over all of its units by CTA (or CTA pair) cid of
+// ncl, in the dynamic shared memory at smem_raw (GemmCfg::smem_bytes). The
+// stand-alone kernel below is one pass; the single-launch decode kernel
+// (fused_decode.cu) makes two, the gate/up GEMM and then the down GEMM, in the
+// same shared memory: a pass leaves its mbarriers invalidated and its tensor
+// memory freed. prefetch: allow the pre-wait weight prefetch (pf_first).
+// FUSED (the single-launch decode kernel's passes): the permutation is read
+// from offsets_in and gather_in (copies in this CTA's shared memory) instead
+// of args.offsets and args.gather_idx; the gate/up pass counts its finished
+// units in args.unit_done and the down pass waits on args.unit_wait; the pass
+// keeps the CTA's right to allocate tensor memory unless last_alloc, and
+// invalidates its mbarriers at the end. Without FUSED none of this is compiled
+// in: the stand-alone kernels are the plain pass.
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL, bool FUSED = false>
+__device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
+                                                  uint8_t* smem_raw, int cid, int ncl,
+                                                  bool prefetch,
+                                                  const int32_t* offsets_in = nullptr,
+                                                  const int32_t* gather_in = nullptr,
+                                                  bool last_alloc = true) {
   using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>;
+  static_assert(!FUSED || CL == 1, "the fused passes run on single CTAs");
+  const int32_t* const offsets_src = FUSED ? offsets_in : args.offsets;
+  const int32_t* const gather_src = FUSED ? gather_in : args.gather_idx;
   static_assert(GATED || BMODE == kTiled, "the down projection reads contiguous h rows");
   static_assert(BMODE != kGather4 || BN <= 128, "gather4 is for decode-sized token tiles");
   constexpr bool PAIR = CL == 2;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -236,7 +286,6 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   // 2 * nb + crank of each pair unit.
   const int crank = PAIR ? (int)cluster_ctarank() : 0;
   const bool leader = crank == 0;
-  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
   const uint32_t bars_base = smem_u32(bars);
   auto full_bar = [&](int s) { return bars_base + 8u * (uint32_t)s; };
   auto empty_bar = [&](int s) { return bars_base + 8u * (uint32_t)(STAGES + s); };
@@ -265,7 +314,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     if constexpr (PAIR)
       tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
     else
-      tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+      tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS, !FUSED || last_alloc);
   }
   // Weight prefetch while the preceding kernel finishes (pf_first: the host
   // sets it for decode-sized launches without a shared expert in which nearly
@@ -277,25 +326,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
   // them before pdl_wait is safe. Not in the E4M3 gated GEMM: there the
   // layer measured 0.2-0.3% slower with it than without.
   if constexpr (!PAIR && !(GATED && C::F8)) {
-    if (warp == 0 && args.pf_first) {
-      const int nf = args.n_out_routed / C::WM;
-      const int g = cid / nf;
-      if (g < E) {
-        const size_t row_bytes = (size_t)args.kdim_routed * sizeof(TIn);
-        const size_t bytes = (size_t)C::WM * row_bytes;
-        const size_t first =
-            ((size_t)g * args.n_out_routed + (size_t)(cid - g * nf) * C::WM) * row_bytes;
-        constexpr int NOP = GATED ? 2 : 1;
-        const int nch = (int)((bytes + kPrefetchChunk - 1) / kPrefetchChunk);
-        for (int c = lane; c < NOP * nch; c += 32) {
-          const int op = c / nch;
-          const size_t off = (size_t)(c - op * nch) * kPrefetchChunk;
-          const size_t rem = bytes - off;
-          prefetch_l2_bulk(static_cast<const uint8_t*>(args.pf_base[op]) + first + off,
-                           (uint32_t)(rem < kPrefetchChunk ? rem : kPrefetchChunk));
-        }
-      }
-    }
+    if (warp == 0 && prefetch) prefetch_first_unit<TIn, GATED, C::WM>(args, cid, lane);
   }
   pdl_wait();  // global memory from here on
   if (warp == 2) {
@@ -305,7 +336,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     // fill the tail. Each group has ceil(m / tile_n) x (features / (WM * CL))
     // units. Every CTA derives the same schedule from the offsets.
     const int tn = args.tile_n;
-    for (int i = lane; i < G + 1; i += 32) offs[i] = args.offsets[i];
+    for (int i = lane; i < G + 1; i += 32) offs[i] = offsets_src[i];
     __syncwarp();
     auto klass = [&](int g) {
       const int m = offs[g + 1] - offs[g];
@@ -405,12 +436,45 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     uint32_t ph = 0;
     int kb_first = skip_first ? 1 : 0;  // first k-block of the next unit
     bool ok = true;
+    // Down GEMM of the single-launch decode kernel: the unit count of group
+    // seen_g as read ahead (lane 0).
+    int seen_g = -1, seen_count = 0;
     for (int u = cid; u < total && ok; u += ncl) {
       Tile tl = decode_tile(remap_unit(u, total, heavy_units), prefix, order, offs, ngroups,
                             args.tile_n);
       tl.nb = tl.nb * CL + crank;
       const bool shared = tl.g == E;
       const int kdim = shared ? args.kdim_shared : args.kdim_routed;
+      if constexpr (FUSED && !GATED) {
+        // Single-launch decode kernel: the group's h rows are complete once all
+        // of its gate/up units have counted themselves done. The count of this
+        // unit's group was read (relaxed) when the previous unit started, so
+        // its L2 round trip is usually off the critical path; a value short of
+        // the need is waited for with acquire loads.
+        {
+          int wok = 1;
+          if (lane == 0) {
+            const int m = offs[tl.g + 1] - offs[tl.g];
+            const int need = ((m + args.tile_n - 1) / args.tile_n) * (kdim / args.wait_block);
+            if (seen_g != tl.g || seen_count < need)
+              wok = wait_count_at_least(args.unit_wait + tl.g, need, args.status, limit);
+            fence_acq_rel_gpu();         // the relaxed read above, made an acquire
+            fence_proxy_async_global();  // the TMA loads below read those h rows
+            // Read ahead: the group of this CTA's next unit.
+            seen_g = -1;
+            if (u + ncl < total) {
+              const Tile nx = decode_tile(remap_unit(u + ncl, total, heavy_units), prefix, order,
+                                          offs, ngroups, args.tile_n);
+              seen_g = nx.g;
+              seen_count = ld_relaxed_gpu(args.unit_wait + nx.g);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, wok, 0)) {
+            ok = false;
+            break;
+          }
+        }
+      }
       const int a_row0 = (shared ? 0 : tl.g * args.n_out_routed) + tl.nb * C::WM;
       const CUtensorMap* mA0 = &args.tmA[shared ? 2 : 0];
       const CUtensorMap* mA1 = &args.tmA[shared ? 3 : 1];
@@ -437,7 +501,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
           for (int r = 0; r < 4; ++r) {
             const int jj = min(4 * q + r, tl.n_valid - 1);
             rows[j][r] = (q < n4) ? (shared ? tl.p0 + jj - offs[E]
-                                            : args.gather_idx[tl.p0 + jj] / args.k)
+                                            : gather_src[tl.p0 + jj] / args.k)
                                   : 0;
           }
         }
@@ -603,7 +667,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
             row = t * args.KP + args.k;
             wv = 1.0f;
           } else {
-            const int s = args.gather_idx[tl.p0 + j];
+            const int s = gather_src[tl.p0 + j];
             const int t = s / args.k;
             row = t * args.KP + (s - t * args.k);
             wv = args.topk_w[s];
@@ -617,7 +681,7 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
         // Scale of each column's token row (x quantized per token).
         float* cs = epi + 128 * 33;
         for (int j = et; j < tl.n_valid; j += C::EPI_THREADS) {
-          const int t = shared ? tl.p0 - offs[E] + j : args.gather_idx[tl.p0 + j] / args.k;
+          const int t = shared ? tl.p0 - offs[E] + j : gather_src[tl.p0 + j] / args.k;
           cs[j] = args.sB[0][t];
         }
       }
@@ -731,12 +795,25 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
       // The accumulator goes back to the MMA issuer. Its tensor-memory reads
       // completed (tcgen05.wait::ld) before the fence and barrier above; the
       // arrive is relaxed because it orders no memory: the tile's global stores
-      // are read only by later kernels.
+      // are read only by later kernels (or, below, published on their own).
       if (et == 0) {
         if constexpr (PAIR)
           mbar_arrive_relaxed_cluster(mapa_shared(tempty_bar(acc), 0));
         else
           mbar_arrive_relaxed(tempty_bar(acc));
+      }
+      if constexpr (FUSED && GATED) {
+        {
+          // Single-launch decode kernel: this unit's h rows, stored by every
+          // epilogue thread, become visible at GPU scope (and to the async
+          // proxy that the down GEMM's TMA loads use) before the group's count
+          // moves. After the accumulator's release, so that the MMA issuer
+          // does not wait for these fences.
+          fence_proxy_async_global();
+          __threadfence();
+          named_barrier_sync(1, C::EPI_THREADS);
+          if (et == 0) red_release_gpu_add(args.unit_done + tl.g, 1);
+        }
       }
     }
   }
@@ -755,6 +832,38 @@ __global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::TH
     else
       tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  if constexpr (FUSED) {
+    // Every wait on the barriers has returned (the closing barrier above):
+    // they can be invalidated, so that the next pass may initialise the same
+    // words.
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < 2 * STAGES + 5; ++i) mbar_inval(bars_base + 8u * (uint32_t)i);
+    }
+    __syncthreads();
+  }
 }
+
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL>
+__global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ GroupedGemmArgs args) {
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  grouped_gemm_pass<TIn, GATED, BN, STAGES, BMODE, CL>(args, smem_raw, blockIdx.x / CL,
+                                                       gridDim.x / CL, true);
+}
+
+// Host side (grouped_gemm.cu): the arguments launch_swiglu_gemm and
+// launch_down_gemm pass to their kernels, for kernels that run the same passes
+// (the single-launch decode kernel). False if a tensor map cannot be made.
+struct GemmProblem;
+struct GemmScales;
+bool prepare_swiglu_gemm(GroupedGemmArgs& a, const GemmProblem& p, const void* x, const void* xg,
+                         const int32_t* offsets, const int32_t* gather_idx, const void* Wg,
+                         const void* Wu, const void* Wsg, const void* Wsu, void* h, void* hs,
+                         int* status, const GemmScales* sc);
+bool prepare_down_gemm(GroupedGemmArgs& a, const GemmProblem& p, const void* h, const void* hs,
+                       const int32_t* offsets, const int32_t* gather_idx, const float* topk_w,
+                       const void* Wd, const void* Wsd, float* Y, int* status,
+                       const GemmScales* sc);
 
 }  // namespace moe

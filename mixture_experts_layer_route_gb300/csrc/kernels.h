@@ -59,6 +59,8 @@ struct GemmProblem {
 // required when gemm_needs_expert_order_copy(p) (128/256-token tiles may run),
 // ignored otherwise (32-token tiles gather rows in the GEMM's own loads).
 bool gemm_needs_expert_order_copy(const GemmProblem& p);
+// True when both GEMMs run the 32-token decode kernels (gather4 token rows).
+bool gemm_uses_decode_tiles(const GemmProblem& p);
 // Per-row power-of-two scales of E4M3 operands (dtype MOE_DTYPE_E4M3 only):
 // a[0..3] = gate, up, shared gate, shared up rows (gated GEMM) or a[0] = W_down,
 // a[2] = shared W_down rows (down GEMM); b[0] = x rows by token (gated) or h
@@ -86,6 +88,32 @@ int sm_count();
 moe_status check_problem(const moe_problem* pb, bool allow_e4m3 = false);
 // The grouped-GEMM description of a checked problem.
 GemmProblem gemm_problem(const moe_problem& p);
+
+// Single-launch decode path (fused_decode.cu): the whole layer in one
+// cooperative persistent kernel for decode-sized batches. Pointers as in
+// moe_forward; grid_ctr (zero at launch) and unit_done ([E+1]) are workspace.
+struct FusedDecodeIO {
+  const void* x;
+  const void* Wr;
+  const float* bias;
+  int renorm, n_group, topk_group, out_f32;
+  const void *Wg, *Wu, *Wd, *Wsg, *Wsu, *Wsd;
+  float* logits;
+  int32_t* ids;
+  float* w;
+  int32_t *offsets, *gather_idx, *slot_pos;
+  void *h, *hs;
+  float* Y;
+  void* y;
+  int* status;
+  int* grid_ctr;
+  int* unit_done;
+  float* router_part;  // [8][T][E]: the router's partial sums over slices of H
+};
+// True when the problem runs the decode tiles, fits one CTA per SM with a CTA
+// per token, and the device supports cooperative launches.
+bool fused_decode_supported(const GemmProblem& p);
+cudaError_t launch_fused_decode(const GemmProblem& p, const FusedDecodeIO& io, cudaStream_t st);
 
 // Row quantization to E4M3 with a power-of-two scale per row (quantize.cu):
 // src [rows][cols] of MOE_DTYPE_BF16 or MOE_DTYPE_F32, cols a multiple of 16.

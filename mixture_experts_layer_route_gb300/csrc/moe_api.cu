@@ -12,11 +12,17 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr size_t kHeader = 256;  // status word + reserved
+// Header words: the status word at int 0; the single-launch decode kernel's
+// grid-barrier counter at int 16 (its own 64-byte line). moe_forward and
+// moe_forward_single_launch clear the first kHeaderClear bytes.
+constexpr int kGridCounter = 16;
+constexpr size_t kHeaderClear = 128;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t pscratch, logits, partials, ids, w, offsets, gather, slotpos, xg, h, hs, Y, total;
+  size_t pscratch, logits, partials, ids, w, offsets, gather, slotpos, xg, h, hs, Y, units, fpart,
+      total;
   // E4M3 layers only: quantized token rows and scales, quantized h rows and
   // scales (routed and shared); 0 otherwise.
   size_t xq, sx, hq, sh, hsq, shs;
@@ -77,6 +83,11 @@ Layout layout_of(const moe_problem& p) {
   L.hsq = f8 && p.I_shared > 0 ? take(T * (size_t)p.I_shared) : 0;
   L.shs = f8 && p.I_shared > 0 ? take(T * 4) : 0;
   L.Y = take(T * KP * (size_t)p.H * 4);
+  // Single-launch decode kernel: per-group counts of finished gate/up units.
+  L.units = take((E + 2) * 4);
+  // ... and its router partial sums (at most 8 slices of H), for decode-sized
+  // batches only.
+  L.fpart = T <= 64 ? take(8 * T * E * 4) : 0;
   L.total = off;
   return L;
 }
@@ -387,7 +398,7 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
   void* hs = has_s ? at<void>(workspace, L.hs) : nullptr;
   float* Y = at<float>(workspace, L.Y);
 
-  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+  cudaError_t e = cudaMemsetAsync(status, 0, kHeaderClear, st);
   if (e == cudaSuccess)
     e = launch_router_logits(pb->dtype, x, W_router, router_bias, g.T, g.H, g.E, L.S, part,
                              status, g.limit_ns, st);
@@ -412,6 +423,68 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
   if (e == cudaSuccess)
     e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : pb->dtype, Y, g.T, g.H,
                        g.k + (has_s ? 1 : 0), y, g.num_sms, st);
+  return cuda_status(e);
+}
+
+moe_status moe_forward_single_launch(const moe_problem* pb, const void* x, const void* W_router,
+                                     const float* router_bias, const void* W_gate,
+                                     const void* W_up, const void* W_down, const void* Ws_gate,
+                                     const void* Ws_up, const void* Ws_down, void* y,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status s = check_problem(pb);
+  if (s != MOE_OK) return s;
+  if (pb->T == 0) return MOE_OK;
+  const bool has_s = pb->I_shared > 0;
+  if (!x || !W_router || !W_gate || !W_up || !W_down || !y) return MOE_ERR_INVALID_ARG;
+  if (has_s != (Ws_gate != nullptr) || has_s != (Ws_up != nullptr) ||
+      has_s != (Ws_down != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, W_router, W_gate, W_up, W_down, y};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (router_bias && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
+  if (has_s && (!aligned16(Ws_gate) || !aligned16(Ws_up) || !aligned16(Ws_down)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*pb);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return s;
+  if (!tensor_map_encoder_available()) return MOE_ERR_UNSUPPORTED;
+  const GemmProblem g = gemm_problem(*pb);
+  if (pb->T > 64 || !fused_decode_supported(g)) return MOE_ERR_UNSUPPORTED;
+
+  cudaStream_t st = (cudaStream_t)stream;
+  int* status = status_ptr(workspace);
+  FusedDecodeIO io;
+  io.x = x;
+  io.Wr = W_router;
+  io.bias = router_bias;
+  io.renorm = pb->renorm;
+  io.n_group = pb->n_group;
+  io.topk_group = pb->topk_group;
+  io.out_f32 = pb->out_f32;
+  io.Wg = W_gate;
+  io.Wu = W_up;
+  io.Wd = W_down;
+  io.Wsg = Ws_gate;
+  io.Wsu = Ws_up;
+  io.Wsd = Ws_down;
+  io.logits = at<float>(workspace, L.logits);
+  io.ids = at<int32_t>(workspace, L.ids);
+  io.w = at<float>(workspace, L.w);
+  io.offsets = at<int32_t>(workspace, L.offsets);
+  io.gather_idx = at<int32_t>(workspace, L.gather);
+  io.slot_pos = at<int32_t>(workspace, L.slotpos);
+  io.h = at<void>(workspace, L.h);
+  io.hs = has_s ? at<void>(workspace, L.hs) : nullptr;
+  io.Y = at<float>(workspace, L.Y);
+  io.y = y;
+  io.status = status;
+  io.grid_ctr = status + kGridCounter;
+  io.unit_done = at<int>(workspace, L.units);
+  io.router_part = at<float>(workspace, L.fpart);
+  // The status word and the grid-barrier counter start at zero; the rest is
+  // one kernel.
+  cudaError_t e = cudaMemsetAsync(status, 0, kHeaderClear, st);
+  if (e == cudaSuccess) e = launch_fused_decode(g, io, st);
   return cuda_status(e);
 }
 
