@@ -34,7 +34,9 @@
  *    the legacy default stream); no call synchronises except
  *    moe_get_device_status().
  *  - Asynchronous device conditions (a bounded wait that ran out, a failed
- *    device-side check) are recorded in a status word at the start of the
+ *    device-side check: an expert id, offset, gather index or slot position
+ *    out of range; the access is then skipped or kept inside the buffers) are
+ *    recorded in a status word at the start of the
  *    workspace and read with moe_get_device_status(). The word is sticky: once
  *    set, later kernels that see it give up early. moe_forward() clears it
  *    when it starts; the sub-calls do not (use moe_reset_device_status()).

@@ -338,6 +338,24 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
     const int tn = args.tile_n;
     for (int i = lane; i < G + 1; i += 32) offs[i] = offsets_src[i];
     __syncwarp();
+    {
+      // Device check of the permutation's offsets (once per launch): they
+      // start at 0, never decrease, stay within the T*k routed positions, and
+      // the shared segment holds 0 or T rows. Otherwise MOE_ERR_DEVICE_CHECK,
+      // and no unit runs (every group empty), so that no tile reads or writes
+      // out of its buffers.
+      const int P = args.T * args.k;
+      const int shared_rows = args.KP > args.k ? args.T : 0;
+      bool bad = false;
+      for (int i = lane; i < G; i += 32)
+        bad |= offs[i + 1] < offs[i] || (i < E && offs[i + 1] > P);
+      if (lane == 0) bad |= offs[0] != 0 || offs[E + 1] - offs[E] != shared_rows;
+      if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0) set_status(args.status, MOE_ERR_DEVICE_CHECK);
+        for (int i = lane; i < G + 1; i += 32) offs[i] = 0;
+        __syncwarp();
+      }
+    }
     auto klass = [&](int g) {
       const int m = offs[g + 1] - offs[g];
       if (m < args.m_lo || m > args.m_hi || m <= 0) return -1;
@@ -668,9 +686,17 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
             wv = 1.0f;
           } else {
             const int s = gather_src[tl.p0 + j];
-            const int t = s / args.k;
-            row = t * args.KP + (s - t * args.k);
-            wv = args.topk_w[s];
+            if ((unsigned)s < (unsigned)(args.T * args.k)) {
+              const int t = s / args.k;
+              row = t * args.KP + (s - t * args.k);
+              wv = args.topk_w[s];
+            } else {
+              // Device check: a slot index out of range is reported, and its
+              // column is stored as zeros into row 0 instead of out of bounds.
+              set_status(args.status, MOE_ERR_DEVICE_CHECK);
+              row = 0;
+              wv = 0.f;
+            }
           }
           // E4M3: the h row's power-of-two scale joins the gate weight (exact).
           if constexpr (C::F8) wv *= shared ? args.sB[1][tl.p0 - offs[E] + j] : args.sB[0][tl.p0 + j];
@@ -682,7 +708,12 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
         float* cs = epi + 128 * 33;
         for (int j = et; j < tl.n_valid; j += C::EPI_THREADS) {
           const int t = shared ? tl.p0 - offs[E] + j : gather_src[tl.p0 + j] / args.k;
-          cs[j] = args.sB[0][t];
+          if ((unsigned)t < (unsigned)args.T) {
+            cs[j] = args.sB[0][t];
+          } else {  // device check, as in the down epilogue
+            set_status(args.status, MOE_ERR_DEVICE_CHECK);
+            cs[j] = 0.f;
+          }
         }
       }
       named_barrier_sync(1, C::EPI_THREADS);

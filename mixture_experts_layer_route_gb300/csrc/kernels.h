@@ -42,9 +42,11 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int has_shar
                            int32_t* chunk_hist, cudaStream_t st);
 
 // Dispatch copy of the routed token rows into expert order (permute.cu).
-// Row slot_pos[s] of xg = x[s / k] for the P = T*k slots (slot order).
+// Row slot_pos[s] of xg = x[s / k] for the P = T*k slots (slot order); a
+// position beyond P sets MOE_ERR_DEVICE_CHECK in *status and is skipped.
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_pos, int P, int k,
-                               size_t row_bytes, void* xg, int num_sms, cudaStream_t st);
+                               size_t row_bytes, void* xg, int* status, int num_sms,
+                               cudaStream_t st);
 
 // Grouped GEMMs (grouped_gemm.cu).
 struct GemmProblem {

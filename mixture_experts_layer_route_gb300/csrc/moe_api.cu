@@ -3,12 +3,24 @@
 // moe_get_device_status().
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe_api.h"
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 namespace {
+
+// NVTX range around host-side work (an entry point, one launch): a profiler
+// that records NVTX shows each stage's launch under its name; without one
+// the calls return at once.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr size_t kAlign = 256;
 constexpr size_t kHeader = 256;  // status word + reserved
@@ -226,6 +238,7 @@ moe_status moe_get_workspace_layout(const moe_problem* pb, moe_workspace_layout*
 moe_status moe_router_logits(const moe_problem* pb, const void* x, const void* W_router,
                              const float* router_bias, float* logits, void* workspace,
                              size_t workspace_bytes, void* stream) {
+  NvtxRange range("moe_router_logits");
   moe_status s = check_problem(pb);
   if (s != MOE_OK) return s;
   const Layout L = layout_of(*pb);
@@ -250,6 +263,7 @@ moe_status moe_router_logits(const moe_problem* pb, const void* x, const void* W
 
 moe_status moe_route(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
                      int32_t* topk_ids, float* topk_w, void* stream) {
+  NvtxRange range("moe_route");
   if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
   if (renorm != 0 && renorm != 1) return MOE_ERR_INVALID_ARG;
   if (T * E >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
@@ -263,6 +277,7 @@ moe_status moe_route(const float* logits, int64_t T, int64_t E, int64_t k, int r
 moe_status moe_route_grouped(const float* logits, int64_t T, int64_t E, int64_t k, int renorm,
                              int64_t n_group, int64_t topk_group, int32_t* topk_ids,
                              float* topk_w, void* stream) {
+  NvtxRange range("moe_route_grouped");
   if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
   if (renorm != 0 && renorm != 1) return MOE_ERR_INVALID_ARG;
   if (!groups_valid(E, k, n_group, topk_group)) return MOE_ERR_INVALID_ARG;
@@ -279,6 +294,7 @@ moe_status moe_permute(const int32_t* topk_ids, int64_t T, int64_t E, int64_t k,
                        int has_shared, int32_t* expert_offsets, int32_t* gather_idx,
                        int32_t* slot_pos, void* workspace, size_t workspace_bytes,
                        void* stream) {
+  NvtxRange range("moe_permute");
   if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
   if (T * (k + 1) >= ((int64_t)1 << 30)) return MOE_ERR_UNSUPPORTED;
   if (!expert_offsets || (T > 0 && (!topk_ids || !gather_idx || !slot_pos)))
@@ -301,6 +317,7 @@ moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
                                    const void* Ws_gate, const void* Ws_up, void* h,
                                    void* h_shared, void* workspace, size_t workspace_bytes,
                                    void* stream) {
+  NvtxRange range("moe_grouped_swiglu_gemm");
   moe_status s = check_problem(pb);
   if (s != MOE_OK) return s;
   if (pb->T == 0) return MOE_OK;
@@ -325,7 +342,7 @@ moe_status moe_grouped_swiglu_gemm(const moe_problem* pb, const void* x,
   if (gemm_needs_expert_order_copy(g)) {
     xg = at<void>(workspace, L.xg);
     e = launch_gather_rows(x, slot_pos, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
-                           g.num_sms, st);
+                           status_ptr(workspace), g.num_sms, st);
   }
   if (e == cudaSuccess)
     e = launch_swiglu_gemm(g, x, xg, expert_offsets, gather_idx, W_gate, W_up, Ws_gate, Ws_up, h,
@@ -337,6 +354,7 @@ moe_status moe_down_combine(const moe_problem* pb, const void* h, const void* h_
                             const int32_t* expert_offsets, const int32_t* gather_idx,
                             const float* topk_w, const void* W_down, const void* Ws_down,
                             void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange range("moe_down_combine");
   moe_status s = check_problem(pb);
   if (s != MOE_OK) return s;
   if (pb->T == 0) return MOE_OK;
@@ -366,6 +384,7 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
                        const void* W_down, const void* Ws_gate, const void* Ws_up,
                        const void* Ws_down, void* y, void* workspace,
                        size_t workspace_bytes, void* stream) {
+  NvtxRange range("moe_forward");
   moe_status s = check_problem(pb);
   if (s != MOE_OK) return s;
   if (pb->T == 0) return MOE_OK;
@@ -399,30 +418,43 @@ moe_status moe_forward(const moe_problem* pb, const void* x, const void* W_route
   float* Y = at<float>(workspace, L.Y);
 
   cudaError_t e = cudaMemsetAsync(status, 0, kHeaderClear, st);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    NvtxRange r("router_logits");
     e = launch_router_logits(pb->dtype, x, W_router, router_bias, g.T, g.H, g.E, L.S, part,
                              status, g.limit_ns, st);
-  if (e == cudaSuccess)
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("route");
     e = launch_route(part, L.S, router_bias, g.T, g.E, g.k, pb->renorm,
                      pb->n_group > 1 ? pb->n_group : 1, pb->topk_group,
                      L.S > 1 ? logits : nullptr, ids, w, st);
-  if (e == cudaSuccess)
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("permute");
     e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status,
                        at<int32_t>(workspace, L.pscratch), st);
+  }
   void* xg = nullptr;
   if (e == cudaSuccess && gemm_needs_expert_order_copy(g)) {
+    NvtxRange r("dispatch_copy");
     xg = at<void>(workspace, L.xg);
     e = launch_gather_rows(x, spos, g.T * g.k, g.k, (size_t)g.H * elem_bytes(g.dtype), xg,
-                           g.num_sms, st);
+                           status, g.num_sms, st);
   }
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    NvtxRange r("gate_up_gemm");
     e = launch_swiglu_gemm(g, x, xg, offs, gidx, W_gate, W_up, Ws_gate, Ws_up, h, hs, status,
                            st);
-  if (e == cudaSuccess)
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("down_gemm");
     e = launch_down_gemm(g, h, hs, offs, gidx, w, W_down, Ws_down, Y, status, st);
-  if (e == cudaSuccess)
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("combine");
     e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : pb->dtype, Y, g.T, g.H,
                        g.k + (has_s ? 1 : 0), y, g.num_sms, st);
+  }
   return cuda_status(e);
 }
 
@@ -431,6 +463,7 @@ moe_status moe_forward_single_launch(const moe_problem* pb, const void* x, const
                                      const void* W_up, const void* W_down, const void* Ws_gate,
                                      const void* Ws_up, const void* Ws_down, void* y,
                                      void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange range("moe_forward_single_launch");
   moe_status s = check_problem(pb);
   if (s != MOE_OK) return s;
   if (pb->T == 0) return MOE_OK;
@@ -490,6 +523,7 @@ moe_status moe_forward_single_launch(const moe_problem* pb, const void* x, const
 
 moe_status moe_quantize_rows_e4m3(const void* src, int32_t src_dtype, int64_t rows,
                                   int64_t cols, uint8_t* q, float* scale, void* stream) {
+  NvtxRange range("moe_quantize_rows_e4m3");
   if (src_dtype != MOE_DTYPE_BF16 && src_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
   if (rows < 0 || cols <= 0 || cols % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (cols >= ((int64_t)1 << 30)) return MOE_ERR_UNSUPPORTED;
@@ -507,6 +541,7 @@ moe_status moe_forward_fp8(const moe_problem* pb, const void* x, const void* W_r
                            const uint8_t* Wsq_up, const float* ss_up, const uint8_t* Wsq_down,
                            const float* ss_down, void* y, void* workspace,
                            size_t workspace_bytes, void* stream) {
+  NvtxRange range("moe_forward_fp8");
   if (!pb || pb->dtype != MOE_DTYPE_E4M3) return MOE_ERR_INVALID_ARG;
   moe_status s = check_problem(pb, true);
   if (s != MOE_OK) return s;
@@ -564,7 +599,7 @@ moe_status moe_forward_fp8(const moe_problem* pb, const void* x, const void* W_r
   void* xg = nullptr;
   if (e == cudaSuccess && gemm_needs_expert_order_copy(g)) {
     xg = at<void>(workspace, L.xg);
-    e = launch_gather_rows(xq, spos, g.T * g.k, g.k, (size_t)g.H, xg, g.num_sms, st);
+    e = launch_gather_rows(xq, spos, g.T * g.k, g.k, (size_t)g.H, xg, status, g.num_sms, st);
   }
   GemmScales sg = {{s_gate, s_up, ss_gate, ss_up}, {sx, sx}};
   if (e == cudaSuccess)

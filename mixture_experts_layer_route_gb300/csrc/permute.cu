@@ -198,19 +198,24 @@ __global__ void __launch_bounds__(PM_THREADS, 1)
 // L2 (x is read from DRAM once), while each writes a whole row. (In position
 // order, the 8x larger stream of written rows evicted x from L2 between
 // re-reads: 0.136 against 0.097 ms for the 8192-token prefill batch.) Slots
-// with slot_pos < 0 (out-of-range ids) have no row. 16-byte vectors, 4 KB per
-// warp in flight; streaming stores.
+// with slot_pos < 0 (out-of-range ids) have no row; a position beyond the T*k
+// rows is a device-check failure (MOE_ERR_DEVICE_CHECK) and is not copied.
+// 16-byte vectors, 4 KB per warp in flight; streaming stores.
 template <int VB>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ slot_pos,
                                                           int P, int k, int vecs_per_row,
-                                                          uint4* __restrict__ xg) {
+                                                          uint4* __restrict__ xg, int* status) {
   pdl_entry();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int s = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < P; s += warps) {
     const int p = slot_pos[s];
     if (p < 0) continue;
+    if (p >= P) {
+      if (lane == 0) set_status(status, MOE_ERR_DEVICE_CHECK);
+      continue;
+    }
     const uint4* src = x + (size_t)(s / k) * vecs_per_row;
     uint4* dst = xg + (size_t)p * vecs_per_row;
     for (int v = lane; v < vecs_per_row; v += 32 * VB) {
@@ -228,14 +233,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }  // namespace
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* slot_pos, int P, int k,
-                               size_t row_bytes, void* xg, int num_sms, cudaStream_t st) {
+                               size_t row_bytes, void* xg, int* status, int num_sms,
+                               cudaStream_t st) {
   if (P == 0) return cudaSuccess;
   const int vpr = (int)(row_bytes / 16);
   int blocks = (P + 7) / 8;
   if (blocks > 16 * num_sms) blocks = 16 * num_sms;
   return launch_chained(gather_rows_kernel<8>, dim3(blocks), dim3(256), 0, st, 1,
                         reinterpret_cast<const uint4*>(x), slot_pos, P, k, vpr,
-                        reinterpret_cast<uint4*>(xg));
+                        reinterpret_cast<uint4*>(xg), status);
 }
 
 size_t permute_smem_bytes(int E) { return sizeof(int32_t) * ((size_t)PM_WARPS * E + E + PM_WARPS); }
