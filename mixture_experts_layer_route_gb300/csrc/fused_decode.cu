@@ -27,6 +27,7 @@
 // set; the cooperative launch guarantees that all CTAs are resident together,
 // which the cross-CTA waits need.
 #include <cmath>
+#include <mutex>
 
 #include "combine.cuh"
 #include "common.cuh"
@@ -344,25 +345,62 @@ bool fused_scratch_fits(int T, int H, int E, int G) {
   return route <= ring && perm <= ring;
 }
 
+// Per-device facts the eligibility test needs, looked up once: the opt-in
+// shared-memory limit, cooperative-launch support, the kernels' shared memory
+// attribute raised to that limit, and whether a CTA using all of it is
+// resident (then every smaller one is too).
+struct FusedDeviceInfo {
+  bool ready = false;
+  int optin = 0;
+  int coop = 0;
+  int resident = 0;
+  cudaError_t err = cudaSuccess;
+};
+std::mutex g_fd_mu;
+FusedDeviceInfo g_fd_info[64];
+
+cudaError_t fused_device_info(FusedDeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_fd_mu);
+  FusedDeviceInfo& d = g_fd_info[dev];
+  if (!d.ready) {
+    d.err = cudaDeviceGetAttribute(&d.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaFuncSetAttribute(fused_decode_kernel<__nv_bfloat16>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, d.optin);
+    if (d.err == cudaSuccess)
+      d.err = cudaFuncSetAttribute(fused_decode_kernel<float>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, d.optin);
+    int bf = 0, f32 = 0;
+    if (d.err == cudaSuccess)
+      d.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &bf, fused_decode_kernel<__nv_bfloat16>, FD_THREADS, (size_t)d.optin);
+    if (d.err == cudaSuccess)
+      d.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f32, fused_decode_kernel<float>,
+                                                            FD_THREADS, (size_t)d.optin);
+    d.resident = (bf >= 1 && f32 >= 1) ? 1 : 0;
+    d.ready = true;
+  }
+  *out = d;
+  return d.err;
+}
+
+// The kernel's shared memory for this problem, if the device can run it with
+// one CTA per SM (its shared memory allows no second CTA); else an error.
 template <typename TIn>
 cudaError_t fused_check(const GemmProblem& p, size_t* smem, size_t* perm_off, int* grid) {
   if (!fused_scratch_fits<TIn>(p.T, p.H, p.E, p.num_sms)) return cudaErrorInvalidValue;
   *smem = fused_smem_bytes<TIn>(p.T, p.E, p.k, perm_off);
-  int dev = 0, optin = 0, coop = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess)
-    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  FusedDeviceInfo info;
+  const cudaError_t e = fused_device_info(&info);
   if (e != cudaSuccess) return e;
-  if (!coop || *smem > (size_t)optin) return cudaErrorInvalidValue;
-  auto fn = fused_decode_kernel<TIn>;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)*smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, FD_THREADS, *smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidValue;
-  *grid = p.num_sms;  // one CTA per SM (the shared memory allows no second)
+  if (!info.coop || !info.resident || *smem > (size_t)info.optin) return cudaErrorInvalidValue;
+  *grid = p.num_sms;
   return cudaSuccess;
 }
 

@@ -1,6 +1,6 @@
 // Block-level stable counting sort of the routing slots by expert, shared by
-// the stand-alone permutation kernel (32 warps) and the fused small-batch
-// routing kernel (8 warps). See permute.cu for the method.
+// the stand-alone permutation kernels (32 warps) and the single-launch decode
+// kernel (6 warps, fused_decode.cu). See permute.cu for the method.
 #pragma once
 
 #include "common.cuh"
