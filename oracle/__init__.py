@@ -54,8 +54,9 @@ def _declare(lib):
     lib.oracle_e4m3_encode.argtypes = [_f, _L, _u8]
     lib.oracle_quantize_rows_e4m3.argtypes = [_f, _L, _L, _u8, _f]
     lib.oracle_bf16_round.argtypes = [_f, _L, _f]
+    lib.oracle_quantize_mx.argtypes = [_f, _L, _L, _L, _u8, _u8]
     for n in ("oracle_e4m3_decode", "oracle_e4m3_encode", "oracle_quantize_rows_e4m3",
-              "oracle_bf16_round"):
+              "oracle_bf16_round", "oracle_quantize_mx"):
         getattr(lib, n).restype = None
     for n in ("oracle_router_logits", "oracle_route", "oracle_route_grouped", "oracle_permute",
               "oracle_expert_h",
@@ -223,6 +224,93 @@ def ffn_combine_fp8(self, x, ids, w, Wg, Wu, Wd, Wsg=None, Wsu=None, Wsd=None,
     return y
 
 
+def mx_scale_cols(cols):
+    """Bytes of MX scales per row of `cols` elements: one per block of 32,
+    padded to a multiple of 16."""
+    return 16 * ((cols // 32 + 15) // 16)
+
+
+def ffn_combine_mx(self, x, ids, w, Wg, Wu, Wd, Wsg=None, Wsu=None, Wsd=None,
+                   want_intermediates=False):
+    """The experts and the combine of the MXFP8 layer for given routing.
+
+    Definition (MXFP8 serving of Qwen3-235B, "Hosting Qwen on Blackwell",
+    quantization section: weights converted statically; the 32-element blocks
+    of "CuTeDSL at Perplexity", Blackwell quantization paragraph): every
+    operand of the two expert GEMMs is quantized in blocks of 32 consecutive
+    elements along the contraction axis (quantize_mx):
+      - x rows over H, W_gate / W_up rows over H, W_down rows over I;
+      - each operand enters its GEMM as the bf16 value of code * scale (equal
+        to that value unless its block's scale is below 2^-117);
+      - h = silu(g) * u rounded to fp32, g and u exact dot products; each h
+        row is quantized over I the same way (from fp32, no bf16 step);
+      - y = sum_r w_r * (W_down[e_r] . h_r) (+ the shared expert, weight 1).
+    """
+    E = Wg.shape[0]
+    k = ids.shape[1]
+    has_s = Wsg is not None
+    offs, gidx, spos = self.permute(np.ascontiguousarray(ids, np.int32), E,
+                                    1 if has_s else 0)
+    mx = self.qdq_mx
+    xm = mx(x)
+    Wgm, Wum, Wdm = mx(Wg), mx(Wu), mx(Wd)
+    Wsgm, Wsum, Wsdm = (mx(Wsg), mx(Wsu), mx(Wsd)) if has_s else (None, None, None)
+    h, hs = self.expert_h(xm, offs, gidx, Wgm, Wum, k, Wsgm, Wsum)
+    hm = mx(h)
+    hsm = mx(hs) if has_s else None
+    y = self.down_combine(hm, offs, spos, np.ascontiguousarray(ids, np.int32),
+                          np.ascontiguousarray(w, np.float32), Wdm, hsm, Wsdm)
+    if want_intermediates:
+        return y, dict(offsets=offs, gather_idx=gidx, xm=xm, h_f32=h, hs_f32=hs, h=hm, hs=hsm)
+    return y
+
+
+def _mx_methods():
+    """MXFP8 expert path (E4M3 codes, one E8M0 scale per block of 32)."""
+
+    def quantize_mx(self, src):
+        """src [..., cols] fp32, cols a multiple of 32 -> (codes uint8
+        [..., cols], scales uint8 [..., mx_scale_cols(cols)])."""
+        src = np.ascontiguousarray(src, np.float32)
+        cols = src.shape[-1]
+        assert cols % 32 == 0, cols
+        rows = src.size // cols
+        sk = mx_scale_cols(cols)
+        q = np.empty(src.shape, np.uint8)
+        sc = np.empty(src.shape[:-1] + (sk,), np.uint8)
+        self.lib.oracle_quantize_mx(self._pf(src), rows, cols, sk, _u8p(q), _u8p(sc))
+        return q, sc
+
+    def dequantize_mx(self, q, scales):
+        """code * 2^(scale byte - 127), exact in fp32 for every code and scale
+        quantize_mx produces from finite fp32 values."""
+        q = np.ascontiguousarray(q, np.uint8)
+        cols = q.shape[-1]
+        e = np.asarray(scales, np.int64)[..., :cols // 32] - 127
+        v = self.e4m3_decode(q).astype(np.float64).reshape(q.shape[:-1] + (cols // 32, 32))
+        v = v * np.ldexp(1.0, e)[..., None]
+        return np.ascontiguousarray(v.reshape(q.shape).astype(np.float32))
+
+    def qdq_mx(self, a):
+        """The bf16 value of each element after MX quantization."""
+        return self.bf16_round(self.dequantize_mx(*self.quantize_mx(a)))
+
+    def forward_mx(self, x, Wr, bias, Wg, Wu, Wd, k, renorm=1, Wsg=None, Wsu=None, Wsd=None,
+                   n_group=1, topk_group=1, want_intermediates=False):
+        """The layer with MXFP8 expert weights: router and routing on x as in
+        forward, then ffn_combine_mx."""
+        lg = self.router_logits(x, Wr, bias)
+        ids, w = self.route_grouped(lg, k, renorm, n_group, topk_group)
+        y, inter = self.ffn_combine_mx(x, ids, w, Wg, Wu, Wd, Wsg, Wsu, Wsd,
+                                       want_intermediates=True)
+        if want_intermediates:
+            return y, dict(logits=lg, ids=ids, w=w, **inter)
+        return y
+
+    return dict(quantize_mx=quantize_mx, dequantize_mx=dequantize_mx, qdq_mx=qdq_mx,
+                ffn_combine_mx=ffn_combine_mx, forward_mx=forward_mx)
+
+
 def _fp8_methods():
     """FP8 expert path (E4M3 codes, one power-of-two scale per row): the
     quantization primitives, and the layer as a composition of the pinned
@@ -277,7 +365,7 @@ def _fp8_methods():
                 ffn_combine_fp8=ffn_combine_fp8, forward_fp8=forward_fp8)
 
 
-for _n, _fn in _fp8_methods().items():
+for _n, _fn in {**_fp8_methods(), **_mx_methods()}.items():
     setattr(Oracle, _n, _fn)
 
 

@@ -365,6 +365,44 @@ void oracle_quantize_rows_e4m3(const float* src, int64_t rows, int64_t cols, uin
   }
 }
 
+// MXFP8 block quantization ("Hosting Qwen on Blackwell", quantization
+// section: Qwen3-235B served with MXFP8 microscaled weights; "CuTeDSL at
+// Perplexity", Blackwell quantization paragraph: the absolute maximum over 32
+// elements). Each row is cut into blocks of 32 consecutive elements; a block's
+// scale is the power of two X = 2^e with e = floor(log2(amax)) - 8 (8 is the
+// exponent of E4M3's largest power of two, 256; the Microscaling format's
+// rule), held in [-127, 127], and e = -127 for a block of zeros. The scale is
+// stored as the unsigned exponent byte e + 127 (E8M0); the elements are the
+// E4M3 codes of v / X, nearest even, saturating at 448 (v / X lies in
+// [256, 512) for the block's largest element, so values above 448 are
+// clamped). Dividing by a power of two is exact, so a value decodes as
+// code * X. scales has sk bytes per row (sk >= cols / 32); bytes past the
+// row's cols / 32 blocks are zero.
+void oracle_quantize_mx(const float* src, int64_t rows, int64_t cols, int64_t sk, uint8_t* q,
+                        uint8_t* scales) {
+  const int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t j = 0; j < sk; ++j) scales[r * sk + j] = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* v = src + r * cols + b * 32;
+      double amax = 0.0;
+      for (int i = 0; i < 32; ++i) amax = std::fmax(amax, std::fabs((double)v[i]));
+      int e = -127;
+      if (amax > 0.0) {
+        int e2;
+        std::frexp(amax, &e2);  // amax = f * 2^e2, f in [0.5, 1): floor(log2) = e2 - 1
+        e = e2 - 1 - 8;
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+      }
+      scales[r * sk + b] = (uint8_t)(e + 127);
+      for (int i = 0; i < 32; ++i)
+        q[r * cols + b * 32 + i] = e4m3_encode_one(std::ldexp(v[i], -e));
+    }
+  }
+}
+
 // bfloat16 rounding (nearest, ties to even) of fp32 values, returned as fp32.
 void oracle_bf16_round(const float* src, int64_t n, float* out) {
   for (int64_t i = 0; i < n; ++i) {
