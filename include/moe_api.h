@@ -71,8 +71,16 @@ typedef enum {
 } moe_status;
 
 /* MOE_DTYPE_E4M3: bf16 activations with E4M3 expert weights, one power-of-two
- * scale per weight row (moe_quantize_rows_e4m3); only moe_forward_fp8 takes it. */
-typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1, MOE_DTYPE_E4M3 = 2 } moe_dtype;
+ * scale per weight row (moe_quantize_rows_e4m3); only moe_forward_fp8 takes it.
+ * MOE_DTYPE_MXFP8: bf16 activations with MXFP8 expert weights, E4M3 codes with
+ * one E8M0 scale per block of 32 (moe_quantize_mx); only moe_forward_mx takes
+ * it. */
+typedef enum {
+  MOE_DTYPE_F32 = 0,
+  MOE_DTYPE_BF16 = 1,
+  MOE_DTYPE_E4M3 = 2,
+  MOE_DTYPE_MXFP8 = 3
+} moe_dtype;
 
 /* Token-tile choice of the grouped GEMMs. AUTO: a batch of T <= 64 tokens
  * uses 32-token tiles (its rows gathered inside the GEMM's loads); larger
@@ -294,6 +302,46 @@ moe_status moe_forward_fp8(const moe_problem* pb, const void* x, const void* W_r
                            const uint8_t* Wsq_up, const float* ss_up, const uint8_t* Wsq_down,
                            const float* ss_down, void* y, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/* MXFP8 expert weights (the MXFP8 serving of Qwen3-235B in "Hosting Qwen on
+ * Blackwell", quantization section; the 32-element absolute maxima of "CuTeDSL
+ * at Perplexity", Blackwell quantization paragraph). A row of `cols` elements
+ * (cols a multiple of 32) is cut into blocks of 32 consecutive elements; per
+ * block, with amax its largest magnitude:
+ *   e = floor(log2(amax)) - 8, held at -127 from below; e = -127 for zeros;
+ *   scale byte = e + 127 (E8M0: the scale is 2^(byte - 127));
+ *   codes = E4M3(v / 2^e), nearest even, clamped to +-448.
+ * Scale rows are moe_mx_scale_cols(cols) = 16 * ceil(cols / 512) bytes: the
+ * row's cols / 32 scale bytes, then zeros.
+ * src [rows][cols] bf16 or fp32 (src_dtype) -> q uint8 [rows][cols], scales
+ * uint8 [rows][moe_mx_scale_cols(cols)]. Device pointers, 16-byte aligned. */
+int64_t moe_mx_scale_cols(int64_t cols);
+moe_status moe_quantize_mx(const void* src, int32_t src_dtype, int64_t rows, int64_t cols,
+                           uint8_t* q, uint8_t* scales, void* stream);
+
+/* The layer with MXFP8 expert weights: pb->dtype = MOE_DTYPE_MXFP8; x,
+ * W_router and y are bf16 (y fp32 with out_f32); routing and permutation as
+ * moe_forward (on x itself). Weights are moe_quantize_mx of the matrices viewed
+ * as rows over their contraction axis: Wq_gate, Wq_up [E*I][H] with s_gate,
+ * s_up [E*I][moe_mx_scale_cols(H)]; Wq_down [E*H][I] with s_down
+ * [E*H][moe_mx_scale_cols(I)]; the shared expert's Wsq_gate, Wsq_up [I_s][H],
+ * Wsq_down [H][I_s] with their scales (all NULL iff I_shared == 0).
+ * Per forward pass each token row of x is quantized the same way (blocks of
+ * 32 along H); both GEMMs multiply the bf16 values of the MXFP8 operands (a
+ * code times its block scale is a bf16 value, exactly for scales of 2^-117 and
+ * above) with fp32 accumulation; h = silu(g) * u is quantized from fp32 per
+ * block of 32 along I and stored as its bf16 values; the down GEMM applies the
+ * gate weight; the combine is moe_forward's. Requires I and I_shared multiples
+ * of 128 and H, I, I_shared <= 8192 (else MOE_ERR_UNSUPPORTED), and problems
+ * whose tiles fit the device's shared memory (MOE_ERR_UNSUPPORTED otherwise).
+ * Workspace: moe_workspace_size(pb). */
+moe_status moe_forward_mx(const moe_problem* pb, const void* x, const void* W_router,
+                          const float* router_bias, const uint8_t* Wq_gate, const uint8_t* s_gate,
+                          const uint8_t* Wq_up, const uint8_t* s_up, const uint8_t* Wq_down,
+                          const uint8_t* s_down, const uint8_t* Wsq_gate, const uint8_t* ss_gate,
+                          const uint8_t* Wsq_up, const uint8_t* ss_up, const uint8_t* Wsq_down,
+                          const uint8_t* ss_down, void* y, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, then copies the device status word into *out. */
 moe_status moe_get_device_status(const void* workspace, void* stream, moe_status* out);

@@ -18,7 +18,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
                 6: "MOE_ERR_DEVICE_CHECK"}
-MOE_DTYPE_F32, MOE_DTYPE_BF16, MOE_DTYPE_E4M3 = 0, 1, 2
+MOE_DTYPE_F32, MOE_DTYPE_BF16, MOE_DTYPE_E4M3, MOE_DTYPE_MXFP8 = 0, 1, 2, 3
 MOE_TILE_AUTO, MOE_TILE_DECODE, MOE_TILE_PREFILL, MOE_TILE_MEDIUM = 0, 1, 2, 3
 MOE_FLAG_TEST_SKIP_SIGNAL = 0x1
 
@@ -28,7 +28,8 @@ EXPORTED = ("moe_workspace_size", "moe_router_logits", "moe_route", "moe_route_g
             "moe_grouped_swiglu_gemm", "moe_down_combine", "moe_forward",
             "moe_get_workspace_layout", "moe_get_device_status", "moe_reset_device_status",
             "moe_status_string", "moe_down_combine_noalloc", "moe_quantize_rows_e4m3",
-            "moe_forward_fp8", "moe_forward_single_launch")
+            "moe_forward_fp8", "moe_forward_single_launch", "moe_mx_scale_cols",
+            "moe_quantize_mx", "moe_forward_mx")
 
 
 class MoEError(RuntimeError):
@@ -88,6 +89,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_quantize_rows_e4m3": [_P, ctypes.c_int32, _I64, _I64, _P, _P, _P],
             "moe_forward_fp8": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                 _P, _P, ctypes.c_size_t, _P],
+            "moe_quantize_mx": [_P, ctypes.c_int32, _I64, _I64, _P, _P, _P],
+            "moe_forward_mx": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                               _P, _P, ctypes.c_size_t, _P],
             "moe_down_combine_noalloc": [pb, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.POINTER(ctypes.c_int)],
         }
@@ -95,6 +99,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = argt
             f.restype = ctypes.c_int
+        lib.moe_mx_scale_cols.argtypes = [_I64]
+        lib.moe_mx_scale_cols.restype = _I64
         lib.moe_status_string.argtypes = [ctypes.c_int]
         lib.moe_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -127,7 +133,8 @@ def make_problem(T, H, E, k, I, I_shared=0, renorm=1, dtype="bf16", tile=MOE_TIL
                  flags=0, wait_limit_us=0, out_f32=False, n_group=1,
                  topk_group=1) -> MoEProblem:
     dt = (MOE_DTYPE_BF16 if dtype in ("bf16", torch.bfloat16)
-          else MOE_DTYPE_E4M3 if dtype == "e4m3" else MOE_DTYPE_F32)
+          else MOE_DTYPE_E4M3 if dtype == "e4m3"
+          else MOE_DTYPE_MXFP8 if dtype == "mxfp8" else MOE_DTYPE_F32)
     return MoEProblem(T, H, E, k, I, I_shared, renorm, dt, tile, flags, wait_limit_us,
                       1 if out_f32 else 0, n_group, topk_group)
 
@@ -214,6 +221,30 @@ def quantize_rows_e4m3(src, q, scale, stream=None):
 def forward_fp8(problem, x, W_router, router_bias, Wq_gate, s_gate, Wq_up, s_up, Wq_down, s_down,
                 Wsq_gate, ss_gate, Wsq_up, ss_up, Wsq_down, ss_down, y, workspace, stream=None):
     _check("moe_forward_fp8", load_library().moe_forward_fp8(
+        ctypes.byref(problem), _ptr(x), _ptr(W_router), _ptr(router_bias), _ptr(Wq_gate),
+        _ptr(s_gate), _ptr(Wq_up), _ptr(s_up), _ptr(Wq_down), _ptr(s_down), _ptr(Wsq_gate),
+        _ptr(ss_gate), _ptr(Wsq_up), _ptr(ss_up), _ptr(Wsq_down), _ptr(ss_down), _ptr(y),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mx_scale_cols(cols: int) -> int:
+    """Bytes of a row of MXFP8 scales for `cols` elements (moe_mx_scale_cols)."""
+    return int(load_library().moe_mx_scale_cols(int(cols)))
+
+
+def quantize_mx(src, q, scales, stream=None):
+    """MXFP8 codes q [rows, cols] (uint8) and E8M0 block scales
+    [rows, mx_scale_cols(cols)] (uint8) of src [rows, cols] (bf16 or fp32), as
+    moe_quantize_mx defines them."""
+    rows, cols = src.shape
+    dt = MOE_DTYPE_BF16 if src.dtype == torch.bfloat16 else MOE_DTYPE_F32
+    _check("moe_quantize_mx", load_library().moe_quantize_mx(
+        _ptr(src), dt, rows, cols, _ptr(q), _ptr(scales), _stream(stream)))
+
+
+def forward_mx(problem, x, W_router, router_bias, Wq_gate, s_gate, Wq_up, s_up, Wq_down, s_down,
+               Wsq_gate, ss_gate, Wsq_up, ss_up, Wsq_down, ss_down, y, workspace, stream=None):
+    _check("moe_forward_mx", load_library().moe_forward_mx(
         ctypes.byref(problem), _ptr(x), _ptr(W_router), _ptr(router_bias), _ptr(Wq_gate),
         _ptr(s_gate), _ptr(Wq_up), _ptr(s_up), _ptr(Wq_down), _ptr(s_down), _ptr(Wsq_gate),
         _ptr(ss_gate), _ptr(Wsq_up), _ptr(ss_up), _ptr(Wsq_down), _ptr(ss_down), _ptr(y),

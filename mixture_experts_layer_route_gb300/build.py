@@ -18,7 +18,7 @@ LIB = os.path.join(HERE, "libmoe.so")
 BUILD = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["moe_api.cu", "router.cu", "permute.cu", "grouped_gemm.cu", "combine.cu",
-           "noalloc.cu", "quantize.cu", "fused_decode.cu"]
+           "noalloc.cu", "quantize.cu", "fused_decode.cu", "quantize_mx.cu", "grouped_gemm_mx.cu"]
 
 
 def _nvcc() -> str:

@@ -58,6 +58,23 @@ bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
+// 2-D uint8 matrix [rows][cols] (cols a multiple of 16, at most 256) whose
+// box is whole rows: cols bytes x box_rows rows, no swizzle. The MX scale rows.
+bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t cols,
+                    uint32_t box_rows) {
+  auto enc = encoder();
+  if (!enc || cols % 16 != 0 || cols > 256) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 constexpr int kMaxExperts = 1024;  // the C ABI's limit on E
@@ -74,6 +91,8 @@ struct AttrCache {
 };
 AttrCache g_attr;
 
+}  // namespace
+
 cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -89,6 +108,8 @@ cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
   }
   return e;
 }
+
+namespace {
 
 template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1>
 cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t upper_tiles,
@@ -130,6 +151,8 @@ cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t 
   return launch_chained(fn, dim3((unsigned)(n * CL)), dim3(C::THREADS), smem, st, CL, a);
 }
 
+}  // namespace
+
 // Upper bound of the unit count of one launch: T*k routed rows in at most
 // min(E, T*k) groups of ceil(m / tile_n) token tiles each, plus the shared
 // expert's T rows.
@@ -139,6 +162,8 @@ size_t unit_upper_bound(int T, int k, int E, int tile_n, int routed_blocks, int 
   return (slots / tile_n + groups) * (size_t)routed_blocks +
          (size_t)((T + tile_n - 1) / tile_n) * shared_blocks;
 }
+
+namespace {
 
 // One launch per GEMM: the 32-token gather4 kernel for decode-sized batches
 // (or when forced), otherwise the tiled kernel with token tiles of tile_n rows.
@@ -152,6 +177,8 @@ bool use_decode_kernel(const GemmProblem& p) {
 // expert of 129..256 rows then streams its weights to the SMs twice.
 int tiled_tile_n(const GemmProblem& p) { return p.tile == MOE_TILE_MEDIUM ? 128 : 256; }
 
+}  // namespace
+
 // Tensor maps of a tiled token operand [rows][cols]: boxes of b_rows, box1 and
 // 16 rows (GemmCfg::B_ROWS, BOX1).
 bool make_b_maps(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
@@ -160,6 +187,8 @@ bool make_b_maps(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uin
          make_tma_map(&m[1], base, dtype, rows, cols, box1) &&
          make_tma_map(&m[2], base, dtype, rows, cols, 16);
 }
+
+namespace {
 
 void fill_common(GroupedGemmArgs& a, const GemmProblem& p, const int32_t* offsets,
                  const int32_t* gather_idx, int* status, int tile_n) {

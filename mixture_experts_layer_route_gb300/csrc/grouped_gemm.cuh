@@ -239,6 +239,112 @@ __device__ __forceinline__ Tile decode_tile(int u, const int32_t* prefix, const 
   return t;
 }
 
+// The unit schedule of one grouped GEMM launch, built by one warp (every CTA
+// builds the same): offs <- the permutation's offsets (device-checked),
+// order <- the groups with rows in [m_lo, m_hi], heaviest class first
+// (> 256, > 128, > 32, the rest; group order within a class), so that the
+// long tensor-bound units start first and short weight-streaming units fill
+// the tail; prefix[i] <- units of order[0..i), *n_sched <- the number of
+// scheduled groups, *n_heavy <- units of the groups of more than 128 rows. A
+// group of m rows has ceil(m / tile_n) x (features / UNIT_FEATURES) units.
+template <int UNIT_FEATURES>
+__device__ __forceinline__ void build_schedule(const int32_t* offsets_src, int E, int T, int k,
+                                               int KP, int m_lo, int m_hi, int tile_n,
+                                               int n_out_routed, int n_out_shared, int* status,
+                                               int32_t* offs, int32_t* order, int32_t* prefix,
+                                               int* n_sched, int* n_heavy, int lane) {
+  const int G = E + 1;
+  const int tn = tile_n;
+  for (int i = lane; i < G + 1; i += 32) offs[i] = offsets_src[i];
+  __syncwarp();
+  {
+    // Device check of the permutation's offsets (once per launch): they
+    // start at 0, never decrease, stay within the T*k routed positions, and
+    // the shared segment holds 0 or T rows. Otherwise MOE_ERR_DEVICE_CHECK,
+    // and no unit runs (every group empty), so that no tile reads or writes
+    // out of its buffers.
+    const int P = T * k;
+    const int shared_rows = KP > k ? T : 0;
+    bool bad = false;
+    for (int i = lane; i < G; i += 32)
+      bad |= offs[i + 1] < offs[i] || (i < E && offs[i + 1] > P);
+    if (lane == 0) bad |= offs[0] != 0 || offs[E + 1] - offs[E] != shared_rows;
+    if (__any_sync(0xffffffffu, bad)) {
+      if (lane == 0) set_status(status, MOE_ERR_DEVICE_CHECK);
+      for (int i = lane; i < G + 1; i += 32) offs[i] = 0;
+      __syncwarp();
+    }
+  }
+  auto klass = [&](int g) {
+    const int m = offs[g + 1] - offs[g];
+    if (m < m_lo || m > m_hi || m <= 0) return -1;
+    return m > 256 ? 0 : (m > 128 ? 1 : (m > 32 ? 2 : 3));
+  };
+  auto units = [&](int g) {
+    const int m = offs[g + 1] - offs[g];
+    const int nf = (g < E ? n_out_routed : n_out_shared) / UNIT_FEATURES;
+    return ((m + tn - 1) / tn) * nf;
+  };
+  const int per = (G + 31) / 32;
+  const int g0 = lane * per, g1 = min(G, g0 + per);
+  // Per-lane class counts, then a warp scan per class (registers only).
+  int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+  for (int g = g0; g < g1; ++g) {
+    const int c = klass(g);
+    c0 += c == 0;
+    c1 += c == 1;
+    c2 += c == 2;
+    c3 += c == 3;
+  }
+  auto excl_scan = [&](int v, int& total) {
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int w = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += w;
+    }
+    total = __shfl_sync(0xffffffffu, incl, 31);
+    return incl - v;
+  };
+  int t0, t1, t2, t3;
+  int p0 = excl_scan(c0, t0), p1 = excl_scan(c1, t1), p2 = excl_scan(c2, t2),
+      p3 = excl_scan(c3, t3);
+  p1 += t0;
+  p2 += t0 + t1;
+  p3 += t0 + t1 + t2;
+  const int base = t0 + t1 + t2 + t3;
+  for (int g = g0; g < g1; ++g) {
+    const int c = klass(g);
+    if (c == 0) order[p0++] = g;
+    else if (c == 1) order[p1++] = g;
+    else if (c == 2) order[p2++] = g;
+    else if (c == 3) order[p3++] = g;
+  }
+  const int ng = base;
+  __syncwarp();
+  const int per2 = (ng + 31) / 32;
+  const int i0 = lane * per2, i1 = min(ng, i0 + per2);
+  int local = 0;
+  for (int i = i0; i < i1; ++i) local += units(order[i]);
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - local;
+  for (int i = i0; i < i1; ++i) {
+    prefix[i] = run;
+    run += units(order[i]);
+  }
+  if (lane == 31) {
+    prefix[ng] = incl;
+    *n_sched = ng;
+  }
+  __syncwarp();
+  if (lane == 0) *n_heavy = prefix[t0 + t1];
+}
+
 // One pass of a grouped GEMM over all of its units by CTA (or CTA pair) cid of
 // ncl, in the dynamic shared memory at smem_raw (GemmCfg::smem_bytes). The
 // stand-alone kernel below is one pass; the single-launch decode kernel
@@ -329,102 +435,10 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
     if (warp == 0 && prefetch) prefetch_first_unit<TIn, GATED, C::WM>(args, cid, lane);
   }
   pdl_wait();  // global memory from here on
-  if (warp == 2) {
-    // Schedule: the groups with rows in [m_lo, m_hi], heaviest class first
-    // (> 256, > 128, > 32, the rest; group order within a class), so that the
-    // long tensor-bound units start first and short weight-streaming units
-    // fill the tail. Each group has ceil(m / tile_n) x (features / (WM * CL))
-    // units. Every CTA derives the same schedule from the offsets.
-    const int tn = args.tile_n;
-    for (int i = lane; i < G + 1; i += 32) offs[i] = offsets_src[i];
-    __syncwarp();
-    {
-      // Device check of the permutation's offsets (once per launch): they
-      // start at 0, never decrease, stay within the T*k routed positions, and
-      // the shared segment holds 0 or T rows. Otherwise MOE_ERR_DEVICE_CHECK,
-      // and no unit runs (every group empty), so that no tile reads or writes
-      // out of its buffers.
-      const int P = args.T * args.k;
-      const int shared_rows = args.KP > args.k ? args.T : 0;
-      bool bad = false;
-      for (int i = lane; i < G; i += 32)
-        bad |= offs[i + 1] < offs[i] || (i < E && offs[i + 1] > P);
-      if (lane == 0) bad |= offs[0] != 0 || offs[E + 1] - offs[E] != shared_rows;
-      if (__any_sync(0xffffffffu, bad)) {
-        if (lane == 0) set_status(args.status, MOE_ERR_DEVICE_CHECK);
-        for (int i = lane; i < G + 1; i += 32) offs[i] = 0;
-        __syncwarp();
-      }
-    }
-    auto klass = [&](int g) {
-      const int m = offs[g + 1] - offs[g];
-      if (m < args.m_lo || m > args.m_hi || m <= 0) return -1;
-      return m > 256 ? 0 : (m > 128 ? 1 : (m > 32 ? 2 : 3));
-    };
-    auto units = [&](int g) {
-      const int m = offs[g + 1] - offs[g];
-      const int nf = (g < E ? args.n_out_routed : args.n_out_shared) / (C::WM * CL);
-      return ((m + tn - 1) / tn) * nf;
-    };
-    const int per = (G + 31) / 32;
-    const int g0 = lane * per, g1 = min(G, g0 + per);
-    // Per-lane class counts, then a warp scan per class (registers only).
-    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-    for (int g = g0; g < g1; ++g) {
-      const int c = klass(g);
-      c0 += c == 0;
-      c1 += c == 1;
-      c2 += c == 2;
-      c3 += c == 3;
-    }
-    auto excl_scan = [&](int v, int& total) {
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int w = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += w;
-      }
-      total = __shfl_sync(0xffffffffu, incl, 31);
-      return incl - v;
-    };
-    int t0, t1, t2, t3;
-    int p0 = excl_scan(c0, t0), p1 = excl_scan(c1, t1), p2 = excl_scan(c2, t2),
-        p3 = excl_scan(c3, t3);
-    p1 += t0;
-    p2 += t0 + t1;
-    p3 += t0 + t1 + t2;
-    const int base = t0 + t1 + t2 + t3;
-    for (int g = g0; g < g1; ++g) {
-      const int c = klass(g);
-      if (c == 0) order[p0++] = g;
-      else if (c == 1) order[p1++] = g;
-      else if (c == 2) order[p2++] = g;
-      else if (c == 3) order[p3++] = g;
-    }
-    const int ng = base;
-    __syncwarp();
-    const int per2 = (ng + 31) / 32;
-    const int i0 = lane * per2, i1 = min(ng, i0 + per2);
-    int local = 0;
-    for (int i = i0; i < i1; ++i) local += units(order[i]);
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - local;
-    for (int i = i0; i < i1; ++i) {
-      prefix[i] = run;
-      run += units(order[i]);
-    }
-    if (lane == 31) {
-      prefix[ng] = incl;
-      *n_sched = ng;
-    }
-    __syncwarp();
-    if (lane == 0) *n_heavy = prefix[t0 + t1];
-  }
+  if (warp == 2)
+    build_schedule<C::WM * CL>(offsets_src, args.E, args.T, args.k, args.KP, args.m_lo,
+                               args.m_hi, args.tile_n, args.n_out_routed, args.n_out_shared,
+                               args.status, offs, order, prefix, n_sched, n_heavy, lane);
   tc_fence_before();
   __syncthreads();
   if constexpr (PAIR) cluster_sync();  // peers' barriers and TMEM exist before any use

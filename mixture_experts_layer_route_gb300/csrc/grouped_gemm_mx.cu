@@ -1,0 +1,714 @@
+// Grouped GEMMs of the MXFP8 layer: expert weights stored as E4M3 codes with
+// one E8M0 scale per block of 32 elements along the contraction axis
+// ("Hosting Qwen on Blackwell", quantization section: MXFP8 weights converted
+// statically; "CuTeDSL at Perplexity", Blackwell quantization paragraph: the
+// absolute maximum over 32 elements), token operands as bf16 rows holding
+// MXFP8 values (x quantized per forward pass, h quantized in the gate/up
+// epilogue).
+//
+// The weights stream from HBM as codes (1 byte per element plus 1/32 for the
+// scales) and are turned into their exact bf16 values on the SM, so the
+// product runs on the bf16 tensor-core MMA (kind::f16): a code times a power
+// of two is a bf16 value (exactly, for scales of 2^-117 and up), and the MMA
+// sums exact products in fp32, which is the block-scaled product up to the
+// order of the fp32 sums.
+//
+// Problem and schedule as grouped_gemm.cuh (the same unit list and deal); the
+// differences are in the pipeline of one CTA (no CTA pairs):
+//   warp 0, producer: per stage (K = 128) the 128 weight rows' codes (one
+//     128-byte box per 64 rows, 128-byte swizzle) and the token tile's two
+//     64-element halves (bf16, one box each); per unit the scale panel of its
+//     weight rows (all K / 32 scale bytes of each row, one box per 64 or 128
+//     rows) into one of two panel buffers.
+//   warps 6-9, converters (one per TMEM lane quarter, thread = weight row):
+//     per stage, the row's 128 codes times their block scales -> 64 bf16
+//     pairs, stored into one of four 64-column slots of tensor memory (the
+//     MMA reads operand A from there: row m in lane m, column c holding
+//     elements 2c and 2c + 1); each slot is handed back by the MMA's commit.
+//   warp 1, MMA issuer: 8 MMAs of K = 16 per stage, A from tensor memory, B
+//     from the stage's token halves (K-major, 128-byte swizzle), into one of
+//     two accumulators.
+//   warps 2-5, epilogue: GATED, silu(gate) * up, then each h row quantized per
+//     block of 32 features (the two threads holding a block's 16 + 16 values
+//     share their maximum) and stored as its bf16 values; DOWN, as the bf16
+//     layer: gate weight applied, fp32 slot rows.
+// Every wait is bounded (status word).
+#include "grouped_gemm.cuh"
+#include "kernels.h"
+#include "mx.cuh"
+
+namespace moe {
+
+struct MxGemmArgs {
+  // E4M3 weight codes, rows of K bytes. GATED: [0] routed gate, [1] routed up,
+  // [2] shared gate, [3] shared up (64-row boxes); DOWN: [0] routed down, [2]
+  // shared down (128-row boxes). 128-byte boxes, 128-byte swizzle.
+  CUtensorMap tmA[4];
+  // The E8M0 scale rows of the same weights (sk bytes per row), indexed like
+  // tmA; a box holds whole rows (sk bytes) of 64 or 128 rows, no swizzle.
+  CUtensorMap tmS[4];
+  // bf16 token rows, tiled: [0..2] routed rows by position (the expert-ordered
+  // copy of x, or h), [3..5] the shared expert's rows by token (x, or
+  // h_shared); boxes of BN, BN / 2 (at least 16) and 16 rows.
+  CUtensorMap tmB[6];
+  const int32_t* offsets;     // [E+2]
+  const int32_t* gather_idx;  // [T*k] (DOWN)
+  const float* topk_w;        // [T*k] (DOWN)
+  void* out;                  // GATED: h bf16 [T*k][I]; DOWN: Y fp32 [T][KP][H]
+  void* out_shared;           // GATED: h_shared bf16 [T][I_shared]
+  int* status;
+  unsigned long long limit_ns;
+  int T, k, E, KP;
+  int n_out_routed, n_out_shared;   // output features per group
+  int kdim_routed, kdim_shared;     // contraction length per group
+  int sk_routed, sk_shared;         // scale bytes per weight row
+  int ld_out_routed, ld_out_shared;
+  unsigned flags;
+  int m_lo, m_hi, tile_n;
+};
+
+namespace {
+
+template <bool GATED, int BN, int STAGES>
+struct MxCfg {
+  static constexpr int BM = 128;                 // weight rows per unit (MMA M)
+  static constexpr int WM = GATED ? 64 : 128;    // output features per unit
+  static constexpr int BK = 128;                 // K per stage
+  static constexpr int A8_BYTES = BM * 128;      // codes of one stage
+  static constexpr int B_HALF = BN * 128;        // one 64-element half of the token tile
+  static constexpr int STAGE_BYTES = A8_BYTES + 2 * B_HALF;
+  static constexpr int SA = 4;                   // converted-A slots in tensor memory
+  static constexpr int ACC_COLS = 2 * BN;        // two fp32 accumulators
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
+  static constexpr int THREADS = 320;            // producer, MMA, 4 epilogue, 4 converter warps
+  static constexpr int BOX1 = BN / 2 < 16 ? 16 : BN / 2;
+  // full, empty [STAGES]; cfull, cempty [SA]; pfull, pempty, tfull, tempty [2]; drain
+  static constexpr int NBARS = 2 * STAGES + 2 * SA + 9;
+  static_assert(ACC_COLS + SA * 64 <= TMEM_COLS, "tensor memory");
+  static_assert(BN % 32 == 0 && BN <= 128, "token tile");
+
+  static size_t smem_bytes(int E, int sk_max) {
+    return 1024 + (size_t)STAGES * STAGE_BYTES + 2 * (size_t)BM * sk_max + EPI_FLOATS * 4 +
+           NBARS * 8 + 16 + 3 * (size_t)(E + 2) * 4;
+  }
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// tcgen05.mma kind::f16 with operand A in tensor memory (address a_tmem).
+__device__ __forceinline__ void umma_issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Each thread of the warp writes 32 consecutive 32-bit columns of its own
+// TMEM lane (the warp's lane quarter is in taddr's lane field).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// All lanes wait (each thread's own acquire of the phase); the warp agrees on
+// the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status,
+                                          uint64_t limit) {
+  const bool ok = mbar_wait(bar, parity, status, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <bool GATED, int BN, int STAGES>
+__global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__ MxGemmArgs args) {
+  pdl_trigger();
+  using C = MxCfg<GATED, BN, STAGES>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int E = args.E;
+  const int sk_max = args.sk_routed > args.sk_shared ? args.sk_routed : args.sk_shared;
+  const int panel_bytes = C::BM * sk_max;
+  uint8_t* stages = smem;
+  uint8_t* panels = stages + (size_t)STAGES * C::STAGE_BYTES;
+  float* epi = reinterpret_cast<float*>(panels + 2 * (size_t)panel_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_FLOATS);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* epi_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* n_sched = reinterpret_cast<int*>(tmem_holder + 2);
+  int* n_heavy = reinterpret_cast<int*>(tmem_holder + 3);
+  int32_t* prefix = reinterpret_cast<int32_t*>(tmem_holder + 4);
+  int32_t* offs = prefix + (E + 2);
+  int32_t* order = offs + (E + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bars_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bars_base + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bars_base + 8u * (uint32_t)(STAGES + s); };
+  auto cfull_bar = [&](int c) { return bars_base + 8u * (uint32_t)(2 * STAGES + c); };
+  auto cempty_bar = [&](int c) { return bars_base + 8u * (uint32_t)(2 * STAGES + C::SA + c); };
+  constexpr int B0 = 2 * STAGES + 2 * C::SA;
+  auto pfull_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + p); };
+  auto pempty_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + 2 + p); };
+  auto tfull_bar = [&](int a) { return bars_base + 8u * (uint32_t)(B0 + 4 + a); };
+  auto tempty_bar = [&](int a) { return bars_base + 8u * (uint32_t)(B0 + 6 + a); };
+  const uint32_t drain_bar = bars_base + 8u * (uint32_t)(B0 + 8);
+  const uint32_t stages_base = smem_u32(stages);
+  const uint32_t panels_base = smem_u32(panels);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int c = 0; c < C::SA; ++c) {
+      mbar_init(cfull_bar(c), 4);  // one arrive per converter warp
+      mbar_init(cempty_bar(c), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(pfull_bar(i), 1);
+      mbar_init(pempty_bar(i), 4);
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), 1);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmA[i]);
+    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmS[i]);
+    for (int i = 0; i < 6; ++i) tma_prefetch_desc(&args.tmB[i]);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+  pdl_wait();  // global memory from here on
+  if (warp == 2)
+    build_schedule<C::WM>(args.offsets, E, args.T, args.k, args.KP, args.m_lo, args.m_hi,
+                          args.tile_n, args.n_out_routed, args.n_out_shared, args.status, offs,
+                          order, prefix, n_sched, n_heavy, lane);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int ngroups = *n_sched;
+  const int heavy_units = *n_heavy;
+  const int total = prefix[ngroups];
+  const uint64_t limit = args.limit_ns;
+  const int cid = blockIdx.x, ncl = gridDim.x;
+  auto tile_of = [&](int u) {
+    return decode_tile(remap_unit(u, total, heavy_units), prefix, order, offs, ngroups,
+                       args.tile_n);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_w = BN <= 64 ? l2_policy_evict_first() : l2_policy_evict_normal();
+    const uint64_t pol_t = l2_policy_evict_last();
+    // Test hook (MOE_FLAG_TEST_SKIP_SIGNAL): the first stage is never loaded,
+    // so the converters' wait on it runs out.
+    const bool skip_first = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
+    uint32_t it = skip_first ? 1u : 0u;
+    int stg = (int)it;
+    uint32_t ph = 0;
+    int kb_first = skip_first ? 1 : 0;
+    bool ok = true;
+    uint32_t lt = 0;
+    constexpr int NA = GATED ? 2 : 1;
+    constexpr int NLOADS = NA + 2;
+    for (int u = cid; u < total && ok; u += ncl, ++lt) {
+      const Tile tl = tile_of(u);
+      const bool shared = tl.g == E;
+      const int kdim = shared ? args.kdim_shared : args.kdim_routed;
+      const int sk = shared ? args.sk_shared : args.sk_routed;
+      const int a_row0 = (shared ? 0 : tl.g * args.n_out_routed) + tl.nb * C::WM;
+      // The unit's scale panel.
+      {
+        const int p = (int)(lt & 1u);
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(pempty_bar(p), ((lt >> 1) & 1u) ^ 1u, args.status, limit);
+        if (!__shfl_sync(0xffffffffu, wok, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(pfull_bar(p), (uint32_t)(C::BM * sk));
+        __syncwarp();
+        const uint32_t pdst = panels_base + (uint32_t)(p * panel_bytes);
+        if (lane < NA)
+          tma_load_2d(pdst + (uint32_t)(lane * 64 * sk), &args.tmS[(shared ? 2 : 0) + lane], 0,
+                      a_row0, pfull_bar(p), pol_w);
+      }
+      const int n_mma = (tl.n_valid + 15) / 16 * 16;
+      const int bsel = n_mma <= 16 ? 2 : (n_mma <= C::BOX1 ? 1 : 0);
+      const int box_rows = bsel == 2 ? 16 : (bsel == 1 ? C::BOX1 : BN);
+      const uint32_t tx = C::A8_BYTES + 2u * (uint32_t)box_rows * 128u;
+      const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
+      // Per-lane operands: lanes < NA weight codes (GATED: gate, up rows),
+      // then the token tile's two K halves.
+      const CUtensorMap* my_map = &args.tmA[shared ? 2 : 0];
+      int my_row = a_row0, my_dx = 0;
+      uint32_t my_off = 0;
+      uint64_t my_pol = pol_w;
+      if (GATED && lane == 1) {
+        my_map = &args.tmA[shared ? 3 : 1];
+        my_off = 64 * 128;
+      }
+      if (lane >= NA && lane < NLOADS) {
+        const int h = lane - NA;
+        my_map = &args.tmB[(shared ? 3 : 0) + bsel];
+        my_row = b_row0;
+        my_dx = 64 * h;
+        my_off = C::A8_BYTES + (uint32_t)(h * C::B_HALF);
+        my_pol = pol_t;
+      }
+      const int nkb = kdim / C::BK;
+      const int kb0 = kb_first;
+      kb_first = 0;
+      for (int kb = kb0; kb < nkb; ++kb) {
+        const int s = stg;
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(empty_bar(s), ph ^ 1u, args.status, limit);
+        if (!__shfl_sync(0xffffffffu, wok, 0)) {
+          ok = false;
+          break;
+        }
+        ++it;
+        if (++stg == STAGES) {
+          stg = 0;
+          ph ^= 1u;
+        }
+        const uint32_t dst = stages_base + (uint32_t)s * C::STAGE_BYTES;
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
+        __syncwarp();
+        // Codes: x in bytes; token halves: x in bf16 elements.
+        if (lane < NLOADS)
+          tma_load_2d(dst + my_off, my_map, kb * C::BK + my_dx, my_row, full_bar(s), my_pol);
+      }
+    }
+    // Let the last loads land before the CTA can exit (bounded, status ignored).
+    if (lane == 0) {
+      const uint32_t n_last = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+      for (uint32_t i = it - n_last; i < it; ++i)
+        mbar_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u, nullptr, 20000000ull);
+      const uint32_t p_last = lt < 2u ? lt : 2u;
+      for (uint32_t i = lt - p_last; i < lt; ++i)
+        mbar_wait(pfull_bar((int)(i & 1u)), (i >> 1) & 1u, nullptr, 20000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t lt = 0, ph = 0, cph = 0;
+      int stg = 0, cstg = 0;
+      bool ok = true;
+      for (int u = cid; u < total && ok; u += ncl, ++lt) {
+        const Tile tl = tile_of(u);
+        const int kdim = (tl.g == E) ? args.kdim_shared : args.kdim_routed;
+        const uint32_t acc = lt & 1u, around = lt >> 1;
+        if (!mbar_wait(tempty_bar((int)acc), (around & 1u) ^ 1u, args.status, limit)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        const int n_mma = (tl.n_valid + 15) / 16 * 16;
+        const uint32_t idesc = umma_idesc(1, C::BM, (uint32_t)n_mma);
+        for (int kb = 0; kb < kdim / C::BK; ++kb) {
+          const int s = stg, c = cstg;
+          if (!mbar_wait(full_bar(s), ph, args.status, limit) ||
+              !mbar_wait(cfull_bar(c), cph, args.status, limit)) {
+            ok = false;
+            break;
+          }
+          if (++stg == STAGES) {
+            stg = 0;
+            ph ^= 1u;
+          }
+          if (++cstg == C::SA) {
+            cstg = 0;
+            cph ^= 1u;
+          }
+          tc_fence_after();
+          const uint32_t a_t = tmem_base + C::ACC_COLS + (uint32_t)c * 64u;
+          const uint32_t b_addr = stages_base + (uint32_t)s * C::STAGE_BYTES + C::A8_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bd =
+                umma_desc_sw128(b_addr + (uint32_t)((kk >> 2) * C::B_HALF + (kk & 3) * 32));
+            umma_issue_tmem_a(d_tmem, a_t + (uint32_t)kk * 8u, bd, idesc,
+                              (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(s));
+          umma_commit(cempty_bar(c));
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar((int)acc));
+      }
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, nullptr, 20000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ converters
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // weight row of the unit = TMEM lane
+    const uint32_t lane_field = (uint32_t)(q * 32) << 16;
+    uint32_t lt = 0, ph = 0, cph = 0;
+    int stg = 0, cstg = 0;
+    bool ok = true;
+    for (int u = cid; u < total && ok; u += ncl, ++lt) {
+      const Tile tl = tile_of(u);
+      const bool shared = tl.g == E;
+      const int kdim = shared ? args.kdim_shared : args.kdim_routed;
+      const int sk = shared ? args.sk_shared : args.sk_routed;
+      const int p = (int)(lt & 1u);
+      if (!warp_wait(pfull_bar(p), (lt >> 1) & 1u, args.status, limit)) break;
+      const uint8_t* srow = panels + (size_t)p * panel_bytes + (size_t)r * sk;
+      for (int kb = 0; kb < kdim / C::BK; ++kb) {
+        const int s = stg, c = cstg;
+        if (!warp_wait(full_bar(s), ph, args.status, limit) ||
+            !warp_wait(cempty_bar(c), cph ^ 1u, args.status, limit)) {
+          ok = false;
+          break;
+        }
+        if (++stg == STAGES) {
+          stg = 0;
+          ph ^= 1u;
+        }
+        if (++cstg == C::SA) {
+          cstg = 0;
+          cph ^= 1u;
+        }
+        tc_fence_after();
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(srow + kb * 4);
+        const uint8_t* arow = stages + (size_t)s * C::STAGE_BYTES + (size_t)r * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o[32];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * h + jj;  // 16-byte chunk of the 128-byte row
+            const uint4 ch = *reinterpret_cast<const uint4*>(arow + ((j ^ (r & 7)) << 4));
+            const float X = mx_scale_of((sw >> (8 * (j >> 1))) & 0xFFu);
+            mx_decode4_bf16(ch.x, X, o[8 * jj + 0], o[8 * jj + 1]);
+            mx_decode4_bf16(ch.y, X, o[8 * jj + 2], o[8 * jj + 3]);
+            mx_decode4_bf16(ch.z, X, o[8 * jj + 4], o[8 * jj + 5]);
+            mx_decode4_bf16(ch.w, X, o[8 * jj + 6], o[8 * jj + 7]);
+          }
+          tmem_st32(tmem_base + lane_field + C::ACC_COLS + (uint32_t)c * 64u + (uint32_t)h * 32u,
+                    o);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cfull_bar(c));
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pempty_bar(p));
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int et = threadIdx.x - 64;  // 0..127
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t lt = 0;
+    for (int u = cid; u < total; u += ncl, ++lt) {
+      Tile tl = tile_of(u);
+      const bool shared = tl.g == E;
+      const uint32_t acc = lt & 1u, around = lt >> 1;
+      if (et == 0)
+        *epi_flag = mbar_wait(tfull_bar((int)acc), around & 1u, args.status, limit) ? 1 : 0;
+      if constexpr (!GATED) {
+        int32_t* yrow = reinterpret_cast<int32_t*>(epi);
+        float* wt = epi + BN;
+        for (int j = et; j < tl.n_valid; j += 128) {
+          int row;
+          float wv;
+          if (shared) {
+            const int t = tl.p0 - offs[E] + j;
+            row = t * args.KP + args.k;
+            wv = 1.0f;
+          } else {
+            const int s = args.gather_idx[tl.p0 + j];
+            if ((unsigned)s < (unsigned)(args.T * args.k)) {
+              const int t = s / args.k;
+              row = t * args.KP + (s - t * args.k);
+              wv = args.topk_w[s];
+            } else {  // device check: reported; the column goes to row 0 as zeros
+              set_status(args.status, MOE_ERR_DEVICE_CHECK);
+              row = 0;
+              wv = 0.f;
+            }
+          }
+          yrow[j] = row;
+          wt[j] = wv;
+        }
+      }
+      named_barrier_sync(1, 128);
+      if (!*epi_flag) break;
+      tc_fence_after();
+      const uint32_t t_acc = tmem_base + lane_base + acc * BN;
+      if constexpr (GATED) {
+        __nv_bfloat16* out =
+            reinterpret_cast<__nv_bfloat16*>(shared ? args.out_shared : args.out);
+        const int ld = shared ? args.ld_out_shared : args.ld_out_routed;
+        const int row0 = shared ? tl.p0 - offs[E] : tl.p0;
+        const int jj = et >> 2, fg = et & 3;
+        for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+          float v[32];
+          tmem_ld32(t_acc + c0, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) epi[(q * 32 + lane) * 33 + i] = v[i];
+          named_barrier_sync(1, 128);
+          float hv[16];
+          float amax = 0.0f;
+#pragma unroll
+          for (int f = 0; f < 16; ++f) {
+            const float g = epi[(fg * 16 + f) * 33 + jj];
+            const float up = epi[(64 + fg * 16 + f) * 33 + jj];
+            hv[f] = __fdividef(g, 1.0f + __expf(-g)) * up;
+            amax = fmaxf(amax, fabsf(hv[f]));
+          }
+          // Block of 32 features: this thread's 16 and its neighbour's (fg ^ 1).
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          const int e = mx_block_exponent(amax);
+          const float inv = mx_pow2(-e), X = mx_pow2(e);
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mx_decode4_bf16(mx_encode4(hv[4 * i] * inv, hv[4 * i + 1] * inv,
+                                       hv[4 * i + 2] * inv, hv[4 * i + 3] * inv),
+                            X, pk[2 * i], pk[2 * i + 1]);
+          const int j = c0 + jj;
+          if (j < tl.n_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)(row0 + j) * ld + tl.nb * 64 +
+                                                  fg * 16);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+          tc_fence_before();
+          named_barrier_sync(1, 128);
+        }
+      } else {
+        float* Y = reinterpret_cast<float*>(args.out);
+        const int4* yrow4 = reinterpret_cast<const int4*>(epi);
+        const float4* wt4 = reinterpret_cast<const float4*>(epi + BN);
+        const size_t H = (size_t)args.n_out_routed;
+        float* Yc = Y + tl.nb * 128 + q * 32 + lane;
+        for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+          float v[32];
+          tmem_ld32(t_acc + c0, v);
+          const int nj = min(32, tl.n_valid - c0);
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const int4 rr = yrow4[(c0 >> 2) + i4];
+            const float4 wv = wt4[(c0 >> 2) + i4];
+            const int i = 4 * i4;
+            if (i < nj) Yc[(size_t)rr.x * H] = wv.x * v[i];
+            if (i + 1 < nj) Yc[(size_t)rr.y * H] = wv.y * v[i + 1];
+            if (i + 2 < nj) Yc[(size_t)rr.z * H] = wv.z * v[i + 2];
+            if (i + 3 < nj) Yc[(size_t)rr.w * H] = wv.w * v[i + 3];
+          }
+        }
+        tc_fence_before();
+        named_barrier_sync(1, 128);
+      }
+      if (et == 0) mbar_arrive_relaxed(tempty_bar((int)acc));
+    }
+  }
+
+  // Teardown: every MMA has completed (drained), every tensor-memory access of
+  // the epilogue and the converters is done.
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// Opt-in shared memory of the current device, looked up once per device.
+int smem_optin() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess)
+      cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+template <bool GATED, int BN, int STAGES>
+cudaError_t launch_mx_variant(const MxGemmArgs& a, int num_sms, size_t upper_units,
+                              cudaStream_t st) {
+  using C = MxCfg<GATED, BN, STAGES>;
+  const int sk_max = a.sk_routed > a.sk_shared ? a.sk_routed : a.sk_shared;
+  const size_t smem = C::smem_bytes(a.E, sk_max);
+  const int optin = smem_optin();
+  if (smem > (size_t)optin) return cudaErrorInvalidValue;
+  auto fn = mx_gemm_kernel<GATED, BN, STAGES>;
+  cudaError_t e = ensure_smem_attr((const void*)fn, (size_t)optin);
+  if (e != cudaSuccess) return e;
+  size_t grid = (size_t)num_sms;
+  if (upper_units < grid) grid = upper_units;
+  if (grid == 0) return cudaSuccess;
+  return launch_chained(fn, dim3((unsigned)grid), dim3(C::THREADS), smem, st, 1, a);
+}
+
+// Decode-sized batches: 32-token tiles, 6 stages (4 if the scale panels of a
+// wide K or many experts leave no room); otherwise 128-token tiles, 3 stages
+// (2 likewise).
+template <bool GATED>
+cudaError_t launch_mx(const MxGemmArgs& a, bool dec, int num_sms, size_t ub, cudaStream_t st) {
+  const int sk_max = a.sk_routed > a.sk_shared ? a.sk_routed : a.sk_shared;
+  const size_t optin = (size_t)smem_optin();
+  if (dec) {
+    if (MxCfg<GATED, 32, 6>::smem_bytes(a.E, sk_max) <= optin)
+      return launch_mx_variant<GATED, 32, 6>(a, num_sms, ub, st);
+    return launch_mx_variant<GATED, 32, 4>(a, num_sms, ub, st);
+  }
+  if (MxCfg<GATED, 128, 3>::smem_bytes(a.E, sk_max) <= optin)
+    return launch_mx_variant<GATED, 128, 3>(a, num_sms, ub, st);
+  return launch_mx_variant<GATED, 128, 2>(a, num_sms, ub, st);
+}
+
+bool mx_decode_tiles(const GemmProblem& p) {
+  return p.tile == MOE_TILE_DECODE || (p.tile == MOE_TILE_AUTO && p.T <= 64);
+}
+
+void fill_mx_common(MxGemmArgs& a, const GemmProblem& p, const int32_t* offsets,
+                    const int32_t* gather_idx, int* status, int tile_n) {
+  a.offsets = offsets;
+  a.gather_idx = gather_idx;
+  a.status = status;
+  a.limit_ns = p.limit_ns;
+  a.T = p.T;
+  a.k = p.k;
+  a.E = p.E;
+  a.KP = p.k + (p.Is > 0 ? 1 : 0);
+  a.flags = p.flags;
+  a.m_lo = 1;
+  a.m_hi = 1 << 30;
+  a.tile_n = tile_n;
+}
+
+}  // namespace
+
+bool mx_problem_fits(const GemmProblem& p) {
+  const size_t optin = (size_t)smem_optin();
+  const int skH = mx_scale_cols(p.H), skI = mx_scale_cols(p.I);
+  const int skIs = p.Is > 0 ? mx_scale_cols(p.Is) : 0;
+  const int skd = skI > skIs ? skI : skIs;
+  if (mx_decode_tiles(p))
+    return MxCfg<true, 32, 4>::smem_bytes(p.E, skH) <= optin &&
+           MxCfg<false, 32, 4>::smem_bytes(p.E, skd) <= optin;
+  return MxCfg<true, 128, 2>::smem_bytes(p.E, skH) <= optin &&
+         MxCfg<false, 128, 2>::smem_bytes(p.E, skd) <= optin;
+}
+
+cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, const void* xq,
+                                  const void* xg, const int32_t* offsets,
+                                  const int32_t* gather_idx, void* h, void* hs, int* status,
+                                  cudaStream_t st) {
+  const bool has_s = p.Is > 0;
+  const bool dec = mx_decode_tiles(p);
+  const int bn = dec ? 32 : 128;
+  const uint32_t b1 = bn / 2 < 16 ? 16 : bn / 2;
+  const int skH = mx_scale_cols(p.H);
+  MxGemmArgs a;
+  memset(&a, 0, sizeof(a));
+  bool ok = make_tma_map(&a.tmA[0], w.gate, MOE_DTYPE_E4M3, (uint64_t)p.E * p.I, p.H, 64) &&
+            make_tma_map(&a.tmA[1], w.up, MOE_DTYPE_E4M3, (uint64_t)p.E * p.I, p.H, 64) &&
+            make_scale_map(&a.tmS[0], w.s_gate, (uint64_t)p.E * p.I, skH, 64) &&
+            make_scale_map(&a.tmS[1], w.s_up, (uint64_t)p.E * p.I, skH, 64) &&
+            make_b_maps(&a.tmB[0], xg, MOE_DTYPE_BF16, (uint64_t)p.T * p.k, p.H, bn, b1) &&
+            make_b_maps(&a.tmB[3], xq, MOE_DTYPE_BF16, p.T, p.H, bn, b1);
+  if (ok && has_s)
+    ok = make_tma_map(&a.tmA[2], w.sh_gate, MOE_DTYPE_E4M3, p.Is, p.H, 64) &&
+         make_tma_map(&a.tmA[3], w.sh_up, MOE_DTYPE_E4M3, p.Is, p.H, 64) &&
+         make_scale_map(&a.tmS[2], w.sh_s_gate, p.Is, skH, 64) &&
+         make_scale_map(&a.tmS[3], w.sh_s_up, p.Is, skH, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_s) {
+    a.tmA[2] = a.tmA[0];
+    a.tmA[3] = a.tmA[1];
+    a.tmS[2] = a.tmS[0];
+    a.tmS[3] = a.tmS[1];
+  }
+  fill_mx_common(a, p, offsets, gather_idx, status, bn);
+  a.topk_w = nullptr;
+  a.out = h;
+  a.out_shared = hs;
+  a.n_out_routed = p.I;
+  a.n_out_shared = has_s ? p.Is : 64;
+  a.kdim_routed = p.H;
+  a.kdim_shared = p.H;
+  a.sk_routed = skH;
+  a.sk_shared = skH;
+  a.ld_out_routed = p.I;
+  a.ld_out_shared = has_s ? p.Is : 0;
+  const size_t ub = unit_upper_bound(p.T, p.k, p.E, bn, p.I / 64, has_s ? p.Is / 64 : 0);
+  return launch_mx<true>(a, dec, p.num_sms, ub, st);
+}
+
+cudaError_t launch_mx_down_gemm(const GemmProblem& p, const MxWeights& w, const void* h,
+                                const void* hs, const int32_t* offsets, const int32_t* gather_idx,
+                                const float* topk_w, float* Y, int* status, cudaStream_t st) {
+  const bool has_s = p.Is > 0;
+  const bool dec = mx_decode_tiles(p);
+  const int bn = dec ? 32 : 128;
+  const uint32_t b1 = bn / 2 < 16 ? 16 : bn / 2;
+  const int skI = mx_scale_cols(p.I);
+  const int skIs = has_s ? mx_scale_cols(p.Is) : skI;
+  MxGemmArgs a;
+  memset(&a, 0, sizeof(a));
+  bool ok = make_tma_map(&a.tmA[0], w.down, MOE_DTYPE_E4M3, (uint64_t)p.E * p.H, p.I, 128) &&
+            make_scale_map(&a.tmS[0], w.s_down, (uint64_t)p.E * p.H, skI, 128) &&
+            make_b_maps(&a.tmB[0], h, MOE_DTYPE_BF16, (uint64_t)p.T * p.k, p.I, bn, b1);
+  if (ok && has_s)
+    ok = make_tma_map(&a.tmA[2], w.sh_down, MOE_DTYPE_E4M3, p.H, p.Is, 128) &&
+         make_scale_map(&a.tmS[2], w.sh_s_down, p.H, skIs, 128) &&
+         make_b_maps(&a.tmB[3], hs, MOE_DTYPE_BF16, p.T, p.Is, bn, b1);
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_s) {
+    a.tmA[2] = a.tmA[0];
+    a.tmS[2] = a.tmS[0];
+    for (int i = 0; i < 3; ++i) a.tmB[3 + i] = a.tmB[i];
+  }
+  a.tmA[1] = a.tmA[0];
+  a.tmA[3] = a.tmA[2];
+  a.tmS[1] = a.tmS[0];
+  a.tmS[3] = a.tmS[2];
+  fill_mx_common(a, p, offsets, gather_idx, status, bn);
+  a.topk_w = topk_w;
+  a.out = Y;
+  a.out_shared = nullptr;
+  a.n_out_routed = p.H;
+  a.n_out_shared = p.H;
+  a.kdim_routed = p.I;
+  a.kdim_shared = has_s ? p.Is : p.I;
+  a.sk_routed = skI;
+  a.sk_shared = skIs;
+  a.ld_out_routed = p.H;
+  a.ld_out_shared = p.H;
+  const size_t ub = unit_upper_bound(p.T, p.k, p.E, bn, p.H / 128, has_s ? p.H / 128 : 0);
+  return launch_mx<false>(a, dec, p.num_sms, ub, st);
+}
+
+}  // namespace moe

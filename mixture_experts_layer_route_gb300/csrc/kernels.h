@@ -16,6 +16,19 @@ namespace moe {
 // or the encoder rejects the shape.
 bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
                   uint32_t box_rows);
+// Tensor map of a uint8 [rows][cols] matrix whose box is whole rows (cols
+// bytes, a multiple of 16 and at most 256) of box_rows rows, no swizzle.
+bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t cols,
+                    uint32_t box_rows);
+// Tensor maps of a tiled token operand [rows][cols]: boxes of b_rows, box1 and
+// 16 rows.
+bool make_b_maps(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
+                 uint32_t b_rows, uint32_t box1);
+// Upper bound of the unit count of one grouped-GEMM launch (token tiles of
+// tile_n rows, routed_blocks / shared_blocks feature blocks per group).
+size_t unit_upper_bound(int T, int k, int E, int tile_n, int routed_blocks, int shared_blocks);
+// Raise a kernel's dynamic shared-memory limit to smem once per device.
+cudaError_t ensure_smem_attr(const void* fn, size_t smem);
 
 // Router (router.cu).
 // Slices S of H whose partial logits the router writes (S == 1: final logits).
@@ -87,7 +100,7 @@ bool tensor_map_encoder_available();
 int sm_count();
 // Argument checks of a moe_problem (shapes, dtype, tile, the int32 index
 // ranges the kernels rely on); MOE_OK or the error to return before any launch.
-moe_status check_problem(const moe_problem* pb, bool allow_e4m3 = false);
+moe_status check_problem(const moe_problem* pb, bool allow_quantized = false);
 // The grouped-GEMM description of a checked problem.
 GemmProblem gemm_problem(const moe_problem& p);
 
@@ -121,6 +134,34 @@ cudaError_t launch_fused_decode(const GemmProblem& p, const FusedDecodeIO& io, c
 // src [rows][cols] of MOE_DTYPE_BF16 or MOE_DTYPE_F32, cols a multiple of 16.
 cudaError_t launch_quantize_rows(int dtype, const void* src, int64_t rows, int64_t cols,
                                  uint8_t* q, float* scale, int num_sms, cudaStream_t st);
+
+// MXFP8 (quantize_mx.cu): blocks of 32 elements along each row, one E8M0
+// scale byte per block (rows of mx_scale_cols(cols) bytes, zero padded).
+// launch_quantize_mx: src [rows][cols] bf16 or fp32 -> codes + scales;
+// launch_qdq_mx: bf16 src -> the bf16 value of every element after
+// quantization (the MXFP8 layer's token rows). cols a multiple of 32.
+cudaError_t launch_quantize_mx(int dtype, const void* src, int64_t rows, int64_t cols,
+                               uint8_t* q, uint8_t* scales, int num_sms, cudaStream_t st);
+cudaError_t launch_qdq_mx(const void* src, int64_t rows, int64_t cols, void* out, int num_sms,
+                          cudaStream_t st);
+
+// MXFP8 grouped GEMMs (grouped_gemm_mx.cu). Weight codes [rows][K] with
+// their scale rows; the shared expert's (sh_*) are null without one.
+struct MxWeights {
+  const uint8_t *gate, *s_gate, *up, *s_up, *down, *s_down;
+  const uint8_t *sh_gate, *sh_s_gate, *sh_up, *sh_s_up, *sh_down, *sh_s_down;
+};
+// True when both MXFP8 GEMMs of the problem fit the device's shared memory.
+bool mx_problem_fits(const GemmProblem& p);
+// xq: the quantized token rows [T][H] (bf16 values); xg: their expert-ordered
+// copy [T*k][H]; h, hs bf16 outputs holding MXFP8 values.
+cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, const void* xq,
+                                  const void* xg, const int32_t* offsets,
+                                  const int32_t* gather_idx, void* h, void* hs, int* status,
+                                  cudaStream_t st);
+cudaError_t launch_mx_down_gemm(const GemmProblem& p, const MxWeights& w, const void* h,
+                                const void* hs, const int32_t* offsets, const int32_t* gather_idx,
+                                const float* topk_w, float* Y, int* status, cudaStream_t st);
 
 // Combine (combine.cu): y[t] = sum_j Y[t][j] for j < KP, rank order.
 cudaError_t launch_combine(int dtype, const float* Y, int T, int H, int KP, void* y,

@@ -38,6 +38,7 @@ struct Layout {
   // E4M3 layers only: quantized token rows and scales, quantized h rows and
   // scales (routed and shared); 0 otherwise.
   size_t xq, sx, hq, sh, hsq, shs;
+  size_t xm;  // MXFP8 layers only: quantized token rows (bf16 values); 0 otherwise
   int S;  // router split count
 };
 
@@ -54,11 +55,15 @@ bool needs_copy(const moe_problem& p) {
 }
 
 // Bytes of one element of the expert GEMM operands (E4M3 codes: 1).
+// MXFP8 layers: 2 (their token operands are bf16 rows holding MXFP8 values).
 size_t elem_bytes(int dtype) {
-  return dtype == MOE_DTYPE_BF16 ? 2 : (dtype == MOE_DTYPE_E4M3 ? 1 : 4);
+  return (dtype == MOE_DTYPE_BF16 || dtype == MOE_DTYPE_MXFP8) ? 2
+                                                               : (dtype == MOE_DTYPE_E4M3 ? 1 : 4);
 }
-// Dtype of the activations (x, W_router, h, y): bf16 for E4M3 layers.
-int act_dtype(int dtype) { return dtype == MOE_DTYPE_E4M3 ? MOE_DTYPE_BF16 : dtype; }
+// Dtype of the activations (x, W_router, h, y): bf16 for E4M3 and MXFP8 layers.
+int act_dtype(int dtype) {
+  return (dtype == MOE_DTYPE_E4M3 || dtype == MOE_DTYPE_MXFP8) ? MOE_DTYPE_BF16 : dtype;
+}
 
 Layout layout_of(const moe_problem& p) {
   Layout L;
@@ -66,6 +71,7 @@ Layout layout_of(const moe_problem& p) {
   const size_t T = (size_t)p.T, E = (size_t)p.E, k = (size_t)p.k;
   const size_t KP = k + (p.I_shared > 0 ? 1 : 0);
   const bool f8 = p.dtype == MOE_DTYPE_E4M3;
+  const bool mx = p.dtype == MOE_DTYPE_MXFP8;
   const size_t as = elem_bytes(act_dtype(p.dtype));
   L.S = router_split_count(act_dtype(p.dtype), p.T, p.H, p.E, kRouterSplitSms);
   size_t off = kHeader;
@@ -87,7 +93,10 @@ Layout layout_of(const moe_problem& p) {
   // Prefill-sized tiles read the routed token rows from an expert-ordered copy.
   L.xq = f8 ? take(T * (size_t)p.H) : 0;
   L.sx = f8 ? take(T * 4) : 0;
-  L.xg = needs_copy(p) ? take(T * k * (size_t)p.H * es) : 0;
+  // MXFP8 layers: the quantized token rows (bf16 values), and always their
+  // expert-ordered copy (both MXFP8 GEMMs read tiled token rows).
+  L.xm = mx ? take(T * (size_t)p.H * 2) : 0;
+  L.xg = (needs_copy(p) || mx) ? take(T * k * (size_t)p.H * es) : 0;
   L.h = take(T * k * (size_t)p.I * as);
   L.hs = p.I_shared > 0 ? take(T * (size_t)p.I_shared * as) : 0;
   L.hq = f8 ? take(T * k * (size_t)p.I) : 0;
@@ -149,22 +158,26 @@ int sm_count() {
   return g_sm_count[dev];
 }
 
-// Host-side validation of a problem, before any launch. allow_e4m3: the entry
-// points that take E4M3 weights (workspace queries and moe_forward_fp8); the
-// bf16/fp32 sub-calls reject that dtype.
-moe_status check_problem(const moe_problem* pb, bool allow_e4m3) {
+// Host-side validation of a problem, before any launch. allow_quantized: the
+// entry points that take quantized weights (workspace queries,
+// moe_forward_fp8 and moe_forward_mx); the bf16/fp32 sub-calls reject those
+// dtypes.
+moe_status check_problem(const moe_problem* pb, bool allow_quantized) {
   if (!pb) return MOE_ERR_INVALID_ARG;
   const moe_problem& p = *pb;
   if (p.T < 0 || p.H <= 0 || p.E <= 0 || p.k <= 0 || p.I <= 0 || p.I_shared < 0)
     return MOE_ERR_INVALID_ARG;
   if (p.k > p.E || p.k > 32 || p.E > 1024) return MOE_ERR_INVALID_ARG;
   if (p.H % 128 != 0 || p.I % 64 != 0 || p.I_shared % 64 != 0) return MOE_ERR_INVALID_ARG;
-  if (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32 &&
-      !(allow_e4m3 && p.dtype == MOE_DTYPE_E4M3))
+  const bool quantized = p.dtype == MOE_DTYPE_E4M3 || p.dtype == MOE_DTYPE_MXFP8;
+  if (p.dtype != MOE_DTYPE_BF16 && p.dtype != MOE_DTYPE_F32 && !(allow_quantized && quantized))
     return MOE_ERR_INVALID_ARG;
-  // E4M3 GEMMs take 128 codes of K per stage.
-  if (p.dtype == MOE_DTYPE_E4M3 && (p.I % 128 != 0 || p.I_shared % 128 != 0))
-    return MOE_ERR_INVALID_ARG;
+  // E4M3 and MXFP8 GEMMs take 128 elements of K per stage.
+  if (quantized && (p.I % 128 != 0 || p.I_shared % 128 != 0)) return MOE_ERR_INVALID_ARG;
+  // An MXFP8 weight row's scales (one byte per 32 elements) are loaded as one
+  // box of at most 256 bytes.
+  if (p.dtype == MOE_DTYPE_MXFP8 && (p.H > 8192 || p.I > 8192 || p.I_shared > 8192))
+    return MOE_ERR_UNSUPPORTED;
   if (p.tile < MOE_TILE_AUTO || p.tile > MOE_TILE_MEDIUM) return MOE_ERR_INVALID_ARG;
   if (p.renorm != 0 && p.renorm != 1) return MOE_ERR_INVALID_ARG;
   if (p.out_f32 != 0 && p.out_f32 != 1) return MOE_ERR_INVALID_ARG;
@@ -616,6 +629,110 @@ moe_status moe_forward_fp8(const moe_problem* pb, const void* x, const void* W_r
   if (e == cudaSuccess)
     e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : MOE_DTYPE_BF16, Y, g.T, g.H,
                        g.k + (has_s ? 1 : 0), y, g.num_sms, st);
+  return cuda_status(e);
+}
+
+int64_t moe_mx_scale_cols(int64_t cols) { return cols < 0 ? 0 : 16 * ((cols / 32 + 15) / 16); }
+
+moe_status moe_quantize_mx(const void* src, int32_t src_dtype, int64_t rows, int64_t cols,
+                           uint8_t* q, uint8_t* scales, void* stream) {
+  NvtxRange range("moe_quantize_mx");
+  if (src_dtype != MOE_DTYPE_BF16 && src_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (cols >= ((int64_t)1 << 30) || rows * moe_mx_scale_cols(cols) >= ((int64_t)1 << 40))
+    return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (!src || !q || !scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(q) || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_mx(src_dtype, src, rows, cols, q, scales, sm_count(),
+                                        (cudaStream_t)stream));
+}
+
+moe_status moe_forward_mx(const moe_problem* pb, const void* x, const void* W_router,
+                          const float* router_bias, const uint8_t* Wq_gate, const uint8_t* s_gate,
+                          const uint8_t* Wq_up, const uint8_t* s_up, const uint8_t* Wq_down,
+                          const uint8_t* s_down, const uint8_t* Wsq_gate, const uint8_t* ss_gate,
+                          const uint8_t* Wsq_up, const uint8_t* ss_up, const uint8_t* Wsq_down,
+                          const uint8_t* ss_down, void* y, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  NvtxRange range("moe_forward_mx");
+  if (!pb || pb->dtype != MOE_DTYPE_MXFP8) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_problem(pb, true);
+  if (s != MOE_OK) return s;
+  if (pb->T == 0) return MOE_OK;
+  const bool has_s = pb->I_shared > 0;
+  const void* ptrs[] = {x, W_router, Wq_gate, s_gate, Wq_up, s_up, Wq_down, s_down, y};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (router_bias && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
+  const void* sptrs[] = {Wsq_gate, ss_gate, Wsq_up, ss_up, Wsq_down, ss_down};
+  for (const void* p : sptrs) {
+    if (has_s != (p != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  const Layout L = layout_of(*pb);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return s;
+  if (!tensor_map_encoder_available()) return MOE_ERR_UNSUPPORTED;
+  const GemmProblem g = gemm_problem(*pb);
+  if (!mx_problem_fits(g)) return MOE_ERR_UNSUPPORTED;
+
+  cudaStream_t st = (cudaStream_t)stream;
+  int* status = status_ptr(workspace);
+  float* logits = at<float>(workspace, L.logits);
+  float* part = at<float>(workspace, L.partials);
+  int32_t* ids = at<int32_t>(workspace, L.ids);
+  float* w = at<float>(workspace, L.w);
+  int32_t* offs = at<int32_t>(workspace, L.offsets);
+  int32_t* gidx = at<int32_t>(workspace, L.gather);
+  int32_t* spos = at<int32_t>(workspace, L.slotpos);
+  void* xm = at<void>(workspace, L.xm);
+  void* xg = at<void>(workspace, L.xg);
+  void* h = at<void>(workspace, L.h);
+  void* hs = has_s ? at<void>(workspace, L.hs) : nullptr;
+  float* Y = at<float>(workspace, L.Y);
+  const MxWeights mw = {Wq_gate, s_gate, Wq_up, s_up, Wq_down, s_down,
+                        Wsq_gate, ss_gate, Wsq_up, ss_up, Wsq_down, ss_down};
+
+  cudaError_t e = cudaMemsetAsync(status, 0, kHeaderClear, st);
+  // Router, routing and permutation exactly as the bf16 layer (on x itself).
+  if (e == cudaSuccess) {
+    NvtxRange r("router_logits");
+    e = launch_router_logits(MOE_DTYPE_BF16, x, W_router, router_bias, g.T, g.H, g.E, L.S, part,
+                             status, g.limit_ns, st);
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("route");
+    e = launch_route(part, L.S, router_bias, g.T, g.E, g.k, pb->renorm,
+                     pb->n_group > 1 ? pb->n_group : 1, pb->topk_group,
+                     L.S > 1 ? logits : nullptr, ids, w, st);
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("permute");
+    e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status,
+                       at<int32_t>(workspace, L.pscratch), st);
+  }
+  // Token rows to their MXFP8 values (bf16), then their expert-ordered copy.
+  if (e == cudaSuccess) {
+    NvtxRange r("quantize_x");
+    e = launch_qdq_mx(x, g.T, g.H, xm, g.num_sms, st);
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("dispatch_copy");
+    e = launch_gather_rows(xm, spos, g.T * g.k, g.k, (size_t)g.H * 2, xg, status, g.num_sms, st);
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("gate_up_gemm");
+    e = launch_mx_swiglu_gemm(g, mw, xm, xg, offs, gidx, h, hs, status, st);
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("down_gemm");
+    e = launch_mx_down_gemm(g, mw, h, hs, offs, gidx, w, Y, status, st);
+  }
+  if (e == cudaSuccess) {
+    NvtxRange r("combine");
+    e = launch_combine(pb->out_f32 ? MOE_DTYPE_F32 : MOE_DTYPE_BF16, Y, g.T, g.H,
+                       g.k + (has_s ? 1 : 0), y, g.num_sms, st);
+  }
   return cuda_status(e);
 }
 

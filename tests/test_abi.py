@@ -121,6 +121,8 @@ LAYOUT_CASES = [dict(T=c.T, H=c.H, E=c.E, k=c.k, I=c.I, I_shared=c.I_shared, dty
                 for c in CONFIGS.values()] + [
     dict(T=64, H=4096, E=128, k=8, I=1536, I_shared=0, dtype="e4m3"),
     dict(T=4096, H=7168, E=256, k=8, I=2048, I_shared=2048, dtype="e4m3"),
+    dict(T=64, H=4096, E=128, k=8, I=1536, I_shared=0, dtype="mxfp8"),
+    dict(T=4096, H=7168, E=256, k=8, I=2048, I_shared=2048, dtype="mxfp8"),
     dict(T=1, H=128, E=4, k=4, I=64, I_shared=64, dtype="bf16"),
     dict(T=513, H=256, E=1024, k=32, I=128, I_shared=0, dtype="f32"),
 ]
@@ -182,3 +184,52 @@ def test_noalloc_rejects_bad_problems_like_the_workspace_call(lib):
     pb = m.make_problem(64, 256, 8, 2, 128, dtype="e4m3")
     assert lib.moe_down_combine_noalloc(ctypes.byref(pb), 0x1000, None, 0x2000, 0x3000, 0x4000,
                                         0x5000, None, 0x6000, None, None) == 1
+
+
+# ------------------------------------------------------------------ MXFP8 calls
+
+def test_mx_scale_cols(lib):
+    assert [lib.moe_mx_scale_cols(c) for c in (32, 512, 544, 4096, 7168)] == [16, 16, 32, 128,
+                                                                              224]
+
+
+def test_quantize_mx_rejects_bad_arguments_on_host(lib):
+    q = lib.moe_quantize_mx
+    assert q(0x1000, 1, 4, 48, 0x2000, 0x3000, None) == 1   # cols not a multiple of 32
+    assert q(0x1000, 2, 4, 64, 0x2000, 0x3000, None) == 1   # E4M3 is not a source dtype
+    assert q(0x1000, 1, 4, 64, 0x2008, 0x3000, None) == 1   # misaligned codes
+    assert q(0x1000, 1, 4, 64, None, 0x3000, None) == 1
+    assert q(None, 1, 0, 64, None, None, None) == 0         # no rows: nothing to do
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(I=192), 1),               # the MXFP8 GEMMs take K in steps of 128
+    (dict(I_shared=64), 1),
+    (dict(H=8320), 2),              # a scale row of more than 256 bytes
+    (dict(I=8320), 2),
+])
+def test_mx_problem_rejected_on_host(lib, kw, code):
+    base = dict(T=64, H=256, E=8, k=2, I=128, I_shared=0, dtype="mxfp8")
+    base.update(kw)
+    with pytest.raises(m.MoEError) as ei:
+        m.workspace_size(m.make_problem(**base))
+    assert ei.value.code == code
+
+
+def test_forward_mx_checks_dtype_and_pointers_on_host(lib):
+    def call(pb, shared, ws_bytes):
+        x, wr, bias = 0x1000, 0x2000, None
+        routed = [0x3000 + 0x1000 * i for i in range(6)]     # codes, scales x gate/up/down
+        sh = [0x20000 + 0x1000 * i for i in range(6)] if shared else [None] * 6
+        return lib.moe_forward_mx(ctypes.byref(pb), x, wr, bias, *routed, *sh, 0x40000, 0x50000,
+                                  ws_bytes, None)
+
+    assert call(m.make_problem(64, 256, 8, 2, 128, dtype="bf16"), False, 1 << 30) == 1
+    pb = m.make_problem(64, 256, 8, 2, 128, dtype="mxfp8")
+    assert call(pb, True, 1 << 30) == 1    # shared-expert pointers without a shared expert
+    assert call(pb, False, 1024) == 3      # workspace too small
+    pbs = m.make_problem(64, 256, 8, 2, 128, I_shared=128, dtype="mxfp8")
+    assert call(pbs, False, 1 << 30) == 1  # a shared expert without its pointers
+    # the bf16 entry points refuse the MXFP8 dtype
+    assert lib.moe_forward(ctypes.byref(pb), 0x1000, 0x2000, None, 0x3000, 0x4000, 0x5000, None,
+                           None, None, 0x6000, 0x7000, 1 << 30, None) == 1

@@ -129,7 +129,7 @@ def covering_tokens(cfg, offs, gidx, n_even=64, per_expert=6):
     return np.array(sorted(toks), np.int64)
 
 
-def oracle_rows(oracle, cfg, d, toks, fp8=False):
+def oracle_rows(oracle, cfg, d, toks, fp8=False, mx=False):
     """The oracle's y rows of `toks`: routing from each token's own logits, then
     every (token, rank) slot through the oracle's experts + combine with k = 1
     and the slot's gate weight, CHUNK experts' weights on the host at a time;
@@ -138,7 +138,7 @@ def oracle_rows(oracle, cfg, d, toks, fp8=False):
     x = to_np(d["x"][torch.from_numpy(toks).to(DEV)])
     lg = oracle.router_logits(x, to_np(d["W_router"]), to_np(d["router_bias"]))
     ids, w = oracle.route(lg, cfg.k, cfg.renorm)
-    fn = oracle.ffn_combine_fp8 if fp8 else oracle.ffn_combine
+    fn = oracle.ffn_combine_mx if mx else (oracle.ffn_combine_fp8 if fp8 else oracle.ffn_combine)
     parts = np.zeros((len(toks), cfg.k, cfg.H))
     experts = np.unique(ids)
     for c0 in range(0, len(experts), CHUNK):
@@ -217,3 +217,24 @@ def test_fp8_output_sample(run, oracle):
     toks = covering_tokens(cfg, run["offs"], run["gidx"], n_even=8, per_expert=1)
     ref, _ = oracle_rows(oracle, cfg, d, toks, fp8=True)
     assert_close(y32[toks], ref, f"{cfg.name} fp8 y on {len(toks)} covering tokens")
+
+
+def test_mx_output_sample(run, oracle):
+    """The MXFP8-weight layer (moe_forward_mx) at full size: a covering sample
+    of tokens recomputed by the oracle's MXFP8 experts and combine, slot by
+    slot, with only the sampled tokens' experts' weights, quantized by the
+    oracle."""
+    cfg, d = run["cfg"], run["d"]
+    if cfg.dtype != "bf16":
+        pytest.skip("MXFP8 weights come with bf16 activations")
+    layer = m.MoELayerMX(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k,
+                         router_bias=d["router_bias"], Ws_gate=d["Ws_gate"], Ws_up=d["Ws_up"],
+                         Ws_down=d["Ws_down"], renorm=cfg.renorm)
+    y32 = layer(d["x"], out_f32=True).cpu().numpy()
+    torch.cuda.synchronize()
+    assert m.get_device_status(layer.workspace(cfg.T)) == m.MOE_OK
+    del layer
+    torch.cuda.empty_cache()
+    toks = covering_tokens(cfg, run["offs"], run["gidx"], n_even=8, per_expert=1)
+    ref, _ = oracle_rows(oracle, cfg, d, toks, mx=True)
+    assert_close(y32[toks], ref, f"{cfg.name} mx y on {len(toks)} covering tokens")
