@@ -22,7 +22,9 @@ fraction against the sustained figure is given beside it);
 e2e = the same metric through MoELayer.forward with the tokens copied from
 pinned host memory and the output copied back inside the timed region (on
 copy streams, double-buffered, overlapping the next step's compute);
-cpu_baseline = the CPU oracle on a bounded sample of the same workload.
+cpu_baseline = the CPU oracle on a bounded sample of the same workload;
+fp8 / mxfp8 = the same workloads with the expert weights quantized (E4M3 with
+a scale per row, or MXFP8 with a scale per block of 32 elements).
 
 Multi-GPU (torchrun): each rank runs an independent replica of the layer on its
 own batch (the layer has no exchange step on one GPU); the time is the max over
@@ -531,20 +533,25 @@ def measure_config(cfg, args, world, local, with_clocks, parity_tokens=8):
     return out
 
 
-def measure_fp8(cfg, args, world, peaks):
-    """The same workload with E4M3 expert weights (moe_forward_fp8): weights
-    quantized once, K timed steps of the layer. Roofline: weight bytes are one
-    per element plus a 4-byte scale per row; the FP8 tensor peak is the
-    measured bf16 burst peak times the nominal fp8/bf16 ratio (4.5 / 2.25 = 2),
-    the fraction against the sustained figure beside it."""
+def measure_quantized(cfg, args, world, peaks, mx=False):
+    """The same workload with quantized expert weights: E4M3 with one
+    power-of-two scale per row (moe_forward_fp8), or MXFP8, E4M3 with one E8M0
+    scale per block of 32 (moe_forward_mx, mx=True). Weights are quantized
+    once, then K timed steps of the layer. Roofline: weight bytes are one per
+    element plus the scales (4 bytes per row; or the MX scale rows); the
+    tensor peak is the measured bf16 burst peak, times the nominal fp8/bf16
+    ratio (4.5 / 2.25 = 2) for the E4M3 MMAs (the MXFP8 GEMMs multiply bf16
+    values of the codes on the bf16 MMA); the fraction against the sustained
+    figure is given beside it."""
     import mixture_experts_layer_route_gb300 as m
     stream = torch.cuda.Stream()
     d = generate(cfg, seed=args.seed, device="cuda")
-    layer = m.MoELayerFP8(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k,
-                          router_bias=d["router_bias"], Ws_gate=d["Ws_gate"], Ws_up=d["Ws_up"],
-                          Ws_down=d["Ws_down"], renorm=cfg.renorm)
+    cls = m.MoELayerMX if mx else m.MoELayerFP8
+    layer = cls(d["W_router"], d["W_gate"], d["W_up"], d["W_down"], cfg.k,
+                router_bias=d["router_bias"], Ws_gate=d["Ws_gate"], Ws_up=d["Ws_up"],
+                Ws_down=d["Ws_down"], renorm=cfg.renorm)
     for n in ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down"):
-        d[n] = None  # only the E4M3 copies stay resident
+        d[n] = None  # only the quantized copies stay resident
     torch.cuda.empty_cache()
     ws = layer.workspace(cfg.T)
     steps = args.steps if cfg.T <= 1024 else max(3, args.steps // 8)
@@ -560,25 +567,43 @@ def measure_fp8(cfg, args, world, peaks):
     counts = torch.diff(offs[:cfg.E + 1]).cpu().numpy()
     T, H, E, k, I, Is = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.I_shared
     touched = int((counts > 0).sum())
-    wbytes = touched * (3 * H * I + 4 * (2 * I + H)) + ((3 * H * Is + 4 * (2 * Is + H)) if Is else 0)
+
+    def expert_bytes(i):  # one expert's gate, up and down matrices
+        if mx:
+            return 2 * i * (H + m.mx_scale_cols(H)) + H * (i + m.mx_scale_cols(i))
+        return 3 * H * i + 4 * (2 * i + H)
+
+    wbytes = touched * expert_bytes(I) + (expert_bytes(Is) if Is else 0)
     bytes_layer = wbytes + 2 * T * H * 2 + E * H * 2
     flop_layer = 2.0 * T * k * 3 * H * I + 2.0 * T * 3 * H * Is
     ms_step = ms_total / steps
     t_mem = bytes_layer / (peaks["hbm_gbs"] * 1e9) * 1e3
-    p8 = 2.0 * peaks["bf16_tflops"]
-    t_tc = flop_layer / (p8 * 1e12) * 1e3
+    ratio = 1.0 if mx else 2.0
+    pk = ratio * peaks["bf16_tflops"]
+    t_tc = flop_layer / (pk * 1e12) * 1e3
     t_roof = max(t_mem, t_tc)
-    t_roof_sus = max(t_mem, flop_layer / (2e12 * peaks["bf16_tflops_sustained"]) * 1e3)
+    t_roof_sus = max(t_mem, flop_layer / (ratio * 1e12 * peaks["bf16_tflops_sustained"]) * 1e3)
+    weights = ("MXFP8: E4M3 codes, one E8M0 scale per 32 elements (moe_forward_mx)" if mx else
+               "E4M3, one power-of-two scale per row (moe_forward_fp8)")
+    peak_src = ("measured bf16_tflops (burst): the MXFP8 GEMMs run the bf16 MMA" if mx else
+                "2 x measured bf16_tflops (burst; nominal fp8/bf16 ratio)")
     return {"value": world * T * steps / (ms_total / 1e3), "unit": "tokens/s",
             "ms_per_step": ms_step, "median_ms": statistics.median(per),
-            "weights": "E4M3, one power-of-two scale per row (moe_forward_fp8)",
+            "weights": weights,
             "layer_roofline": {"t_roof_ms": t_roof, "bound": "hbm" if t_mem >= t_tc else "tensor",
                                "frac": t_roof / ms_step, "frac_vs_sustained": t_roof_sus / ms_step,
                                "bytes_touched": bytes_layer,
-                               "flop_routed": flop_layer, "fp8_peak_tflops": p8,
-                               "fp8_peak_source": "2 x measured bf16_tflops (burst; nominal "
-                                                  "fp8/bf16 ratio)"},
+                               "flop_routed": flop_layer, "tensor_peak_tflops": pk,
+                               "tensor_peak_source": peak_src},
             "experts_touched": touched}
+
+
+def measure_fp8(cfg, args, world, peaks):
+    return measure_quantized(cfg, args, world, peaks, mx=False)
+
+
+def measure_mx(cfg, args, world, peaks):
+    return measure_quantized(cfg, args, world, peaks, mx=True)
 
 
 def summarize(r, peaks, world, prefix_src):
@@ -643,14 +668,14 @@ def summarize(r, peaks, world, prefix_src):
 WORKLOAD_ORDER = ["qwen3_235b_prefill", "qwen35_397b_zipf", "deepseek_v3", "tiny_f32"]
 
 
-def workload_entry(cfg, s, fp8):
+def workload_entry(cfg, s, fp8, mxfp8=None):
     return {"config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
                        "I": cfg.I, "I_shared": cfg.I_shared, "dtype": cfg.dtype,
                        "zipf_s": cfg.zipf_s, "l2": s["l2"]},
             **{k: s[k] for k in ("value", "ms_per_step", "median_ms", "roofline",
                                  "layer_roofline", "stages_ms", "expert_load", "graph", "e2e",
                                  "parity")},
-            "unit": "tokens/s", "steps": s["steps"], "fp8": fp8}
+            "unit": "tokens/s", "steps": s["steps"], "fp8": fp8, "mxfp8": mxfp8}
 
 
 def run_native(args):
@@ -667,10 +692,12 @@ def run_native(args):
     s = summarize(r, peaks, world, src)
     clocks = r["clocks"]
     del r
-    fp8 = None
+    fp8 = mxfp8 = None
     if args.fp8 and cfg.dtype == "bf16" and cfg.I % 128 == 0 and cfg.I_shared % 128 == 0:
         torch.cuda.empty_cache()
         fp8 = measure_fp8(cfg, args, world, peaks)
+        torch.cuda.empty_cache()
+        mxfp8 = measure_mx(cfg, args, world, peaks)
     # The other layer shapes, each measured the same way (one at a time: the
     # DeepSeek-V3-shaped layer alone holds ~23 GB of weights).
     others = {}
@@ -685,11 +712,13 @@ def run_native(args):
                             parity_tokens=args.parity_tokens if rank == 0 else 0)
         sp = summarize(rp, peaks, world, src)
         del rp
-        f8 = None
+        f8 = fmx = None
         if args.fp8 and c.dtype == "bf16" and c.I % 128 == 0 and c.I_shared % 128 == 0:
             torch.cuda.empty_cache()
             f8 = measure_fp8(c, args, world, peaks)
-        others[name] = workload_entry(c, sp, f8)
+            torch.cuda.empty_cache()
+            fmx = measure_mx(c, args, world, peaks)
+        others[name] = workload_entry(c, sp, f8, fmx)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         torch.cuda.empty_cache()
@@ -711,7 +740,7 @@ def run_native(args):
         "median_ms": s["median_ms"], "p10_ms": s["p10_ms"], "p90_ms": s["p90_ms"],
         "roofline": s["roofline"], "layer_roofline": s["layer_roofline"],
         "stages_ms": s["stages_ms"], "expert_load": s["expert_load"],
-        "e2e": s["e2e"], "graph": s["graph"], "fp8": fp8, "parity": s["parity"],
+        "e2e": s["e2e"], "graph": s["graph"], "fp8": fp8, "mxfp8": mxfp8, "parity": s["parity"],
         "gpu_launches": n_launch,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -774,7 +803,8 @@ def main():
                     help="tokens per workload checked against the CPU oracle (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", dest="fp8", action="store_false",
-                    help="skip the E4M3-weight measurement of the same workload")
+                    help="skip the quantized-weight measurements (E4M3 rows, MXFP8) of the "
+                         "same workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:
