@@ -265,9 +265,14 @@ moe_status moe_down_combine_noalloc(const moe_problem* pb, const void* h, const 
 
 /* Byte offsets of moe_forward's intermediates inside the workspace (for
  * inspection by tests): logits, topk_ids, topk_w, expert_offsets, gather_idx,
- * slot_pos, h, h_shared. Each is -1 when absent. */
+ * slot_pos, h, h_shared. Each is -1 when absent. MXFP8 problems that run the
+ * decode-sized kernels (moe_forward_mx) store h and h_shared as E4M3 codes
+ * with E8M0 scale rows (moe_mx_scale_cols(I) and (I_shared) bytes per row) at
+ * h_scales and h_shared_scales; otherwise those two are -1 and h holds the
+ * layer's activation values (bf16 or fp32). */
 typedef struct {
   int64_t logits, topk_ids, topk_w, expert_offsets, gather_idx, slot_pos, h, h_shared;
+  int64_t h_scales, h_shared_scales;
 } moe_workspace_layout;
 moe_status moe_get_workspace_layout(const moe_problem* pb, moe_workspace_layout* out);
 

@@ -49,7 +49,8 @@ class MoEProblem(ctypes.Structure):
 
 class MoEWorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("logits", "topk_ids", "topk_w", "expert_offsets",
-                                               "gather_idx", "slot_pos", "h", "h_shared")]
+                                               "gather_idx", "slot_pos", "h", "h_shared",
+                                               "h_scales", "h_shared_scales")]
 
 
 _lib = None

@@ -58,15 +58,18 @@ bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
-// 2-D uint8 matrix [rows][cols] (cols a multiple of 16, at most 256) whose
-// box is whole rows: cols bytes x box_rows rows, no swizzle. The MX scale rows.
+// 2-D uint8 matrix [rows][cols] (cols a multiple of 16) whose box is box_cols
+// bytes (whole rows when 0; a multiple of 16, at most 256) x box_rows rows, no
+// swizzle. The MX scale rows.
 bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t cols,
-                    uint32_t box_rows) {
+                    uint32_t box_rows, uint32_t box_cols) {
   auto enc = encoder();
-  if (!enc || cols % 16 != 0 || cols > 256) return false;
+  if (box_cols == 0) box_cols = cols;
+  if (!enc || cols % 16 != 0 || box_cols % 16 != 0 || box_cols > 256 || box_cols > cols)
+    return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {cols, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

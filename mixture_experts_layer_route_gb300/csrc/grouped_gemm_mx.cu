@@ -65,6 +65,18 @@ struct MxGemmArgs {
   int ld_out_routed, ld_out_shared;
   unsigned flags;
   int m_lo, m_hi, tile_n;
+  // Decode kernel only (mx_dec_kernel; unused by mx_gemm_kernel):
+  // tmAS: the weights' scale rows again, boxes of 16 bytes (four stages) of
+  // 64 (GATED) or 128 rows, indexed like tmA; tmB then holds E4M3 token codes
+  // (128-byte boxes, 128-byte swizzle) and tmSB their scale rows, whole rows of
+  // 32 tokens: [0] routed rows by position, [1] the shared expert's by token.
+  CUtensorMap tmAS[4];
+  CUtensorMap tmSB[2];
+  int skb_routed, skb_shared;       // scale bytes per token row of the B operand
+  // GATED: scale rows of h / h_shared (the MXFP8 codes go to out / out_shared).
+  uint8_t* out_scales;
+  uint8_t* out_shared_scales;
+  int sko_routed, sko_shared;       // their bytes per row
 };
 
 namespace {
@@ -123,6 +135,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+// Each thread reads 64 consecutive fp32 columns of its own TMEM lane (the
+// warp's lane quarter is in taddr's lane field); the wait is in the same
+// statement, so no use of the registers precedes it.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+      "%62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
+        "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
+        "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_wait_st() {
@@ -541,6 +582,425 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decode-sized MXFP8 GEMMs (32-token tiles): E4M3 x E4M3 on the tensor cores
+// (kind::f8f6f4), with the block scales applied by the CUDA cores. The MMA's
+// K = 32 is exactly one MXFP8 block, so every MMA writes one block's partial
+// product P_b (fp32, exact sums of exact code products) into its own slot of
+// tensor memory; scaler warps read the partials and accumulate
+//   acc[m][n] += P_b[m][n] * s_B[n][b] * s_A[m][b]
+// in registers (both scales are powers of two: the products are exact and the
+// one rounding per block is the fp32 accumulation, as in the MMA itself). At
+// decode sizes an MMA's time is set by its A bytes, so E4M3 operands run twice
+// as fast as their bf16 values would.
+//
+// Warp roles: warp 0 producer (per stage: the weight codes, their 16-byte
+// scale boxes (four stages each) and the token codes; per unit: the token
+// tile's scale rows), warp 1 MMA issuer (four MMAs per stage into one of four
+// slot groups of tensor memory), warps 2-9 scalers and epilogue (warp w: TMEM
+// lane quarter w % 4, blocks 2 bh and 2 bh + 1 of every stage for
+// bh = (w - 2) / 4, all token columns; the two halves' sums are added in
+// shared memory).
+// GATED epilogue: silu(gate) * up, quantized per 32 features (MXFP8 codes and
+// scale bytes of h); DOWN: the gate-weighted fp32 slot rows, as mx_gemm_kernel.
+
+template <bool GATED, int STAGES>
+struct MxDecCfg {
+  static constexpr int BN = 32;
+  static constexpr int BM = 128;
+  static constexpr int WM = GATED ? 64 : 128;
+  static constexpr int BK = 128;
+  static constexpr int A_BYTES = BM * 128;   // codes
+  static constexpr int B_BYTES = BN * 128;   // token codes
+  static constexpr int AS_BYTES = BM * 16;   // scale box of the weight rows
+  static constexpr int B_OFF = A_BYTES;
+  static constexpr int AS_OFF = A_BYTES + B_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + AS_BYTES;  // 22 KB
+  static constexpr int NG = 4;               // partial slot groups (4 blocks x 32 columns)
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int SCALER_WARPS = 8;
+  static constexpr int THREADS = 64 + 32 * SCALER_WARPS;
+  // Partial sums of the two scaler halves meet here (128 rows x 32 columns,
+  // padded), then DOWN's per-column destination rows and gate weights.
+  static constexpr int EPI_FLOATS = 128 * 33 + 2 * BN;
+  // full, empty [STAGES]; pfull, pempty [NG]; bfull, bempty [2]; drain
+  static constexpr int NBARS = 2 * STAGES + 2 * NG + 5;
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(NG * 4 * BN <= TMEM_COLS, "tensor memory");
+
+  // skb_max: token scale bytes per row; nblk_max: 32-element blocks of K.
+  static size_t smem_bytes(int E, int skb_max, int nblk_max) {
+    return 1024 + (size_t)STAGES * STAGE_BYTES + 2 * (size_t)BN * skb_max +
+           (size_t)nblk_max * BN * 4 + EPI_FLOATS * 4 + NBARS * 8 + 16 +
+           3 * (size_t)(E + 2) * 4;
+  }
+};
+
+template <bool GATED, int STAGES>
+__global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
+    mx_dec_kernel(const __grid_constant__ MxGemmArgs args) {
+  pdl_trigger();
+  using C = MxDecCfg<GATED, STAGES>;
+  constexpr int BN = C::BN;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int E = args.E;
+  const int skb_max = args.skb_routed > args.skb_shared ? args.skb_routed : args.skb_shared;
+  const int kmax = args.kdim_routed > args.kdim_shared ? args.kdim_routed : args.kdim_shared;
+  const int nblk_max = kmax / 32;
+  uint8_t* stages = smem;
+  uint8_t* bpanels = stages + (size_t)STAGES * C::STAGE_BYTES;  // token scale bytes [2][BN][skb]
+  float* fpanel = reinterpret_cast<float*>(bpanels + 2 * (size_t)BN * skb_max);  // [blk][BN]
+  float* epi = fpanel + (size_t)nblk_max * BN;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_FLOATS);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* n_sched = reinterpret_cast<int*>(tmem_holder + 2);
+  int* n_heavy = reinterpret_cast<int*>(tmem_holder + 3);
+  int32_t* prefix = reinterpret_cast<int32_t*>(tmem_holder + 4);
+  int32_t* offs = prefix + (E + 2);
+  int32_t* order = offs + (E + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bars_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bars_base + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bars_base + 8u * (uint32_t)(STAGES + s); };
+  auto pfull_bar = [&](int g) { return bars_base + 8u * (uint32_t)(2 * STAGES + g); };
+  auto pempty_bar = [&](int g) { return bars_base + 8u * (uint32_t)(2 * STAGES + C::NG + g); };
+  constexpr int B0 = 2 * STAGES + 2 * C::NG;
+  auto bfull_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + p); };
+  auto bempty_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + 2 + p); };
+  const uint32_t drain_bar = bars_base + 8u * (uint32_t)(B0 + 4);
+  const uint32_t stages_base = smem_u32(stages);
+  const uint32_t bpanels_base = smem_u32(bpanels);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      // The MMAs' commit, and every scaler warp once it has read the stage's
+      // weight scales.
+      mbar_init(empty_bar(s), 1 + C::SCALER_WARPS);
+    }
+    for (int g = 0; g < C::NG; ++g) {
+      mbar_init(pfull_bar(g), 1);
+      mbar_init(pempty_bar(g), C::SCALER_WARPS);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bfull_bar(i), 1);
+      mbar_init(bempty_bar(i), C::SCALER_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    *abort_flag = 0;
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmA[i]);
+    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmAS[i]);
+    for (int i = 0; i < 6; ++i) tma_prefetch_desc(&args.tmB[i]);
+    for (int i = 0; i < 2; ++i) tma_prefetch_desc(&args.tmSB[i]);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+  pdl_wait();  // global memory from here on
+  if (warp == 2)
+    build_schedule<C::WM>(args.offsets, E, args.T, args.k, args.KP, args.m_lo, args.m_hi,
+                          args.tile_n, args.n_out_routed, args.n_out_shared, args.status, offs,
+                          order, prefix, n_sched, n_heavy, lane);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int ngroups = *n_sched;
+  const int heavy_units = *n_heavy;
+  const int total = prefix[ngroups];
+  const uint64_t limit = args.limit_ns;
+  const int cid = blockIdx.x, ncl = gridDim.x;
+  auto tile_of = [&](int u) {
+    return decode_tile(remap_unit(u, total, heavy_units), prefix, order, offs, ngroups,
+                       args.tile_n);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_t = l2_policy_evict_last();
+    const bool skip_first = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
+    uint32_t it = skip_first ? 1u : 0u;
+    int stg = (int)it;
+    uint32_t ph = 0;
+    int kb_first = skip_first ? 1 : 0;
+    bool ok = true;
+    uint32_t lt = 0;
+    constexpr int NA = GATED ? 2 : 1;
+    constexpr int NLOADS = 2 * NA + 1;  // codes and scale boxes of the weight rows, token codes
+    for (int u = cid; u < total && ok; u += ncl, ++lt) {
+      const Tile tl = tile_of(u);
+      const bool shared = tl.g == E;
+      const int kdim = shared ? args.kdim_shared : args.kdim_routed;
+      const int skb = shared ? args.skb_shared : args.skb_routed;
+      const int a_row0 = (shared ? 0 : tl.g * args.n_out_routed) + tl.nb * C::WM;
+      const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
+      {  // the token tile's scale rows
+        const int p = (int)(lt & 1u);
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(bempty_bar(p), ((lt >> 1) & 1u) ^ 1u, args.status, limit);
+        if (!__shfl_sync(0xffffffffu, wok, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bfull_bar(p), (uint32_t)(BN * skb));
+          tma_load_2d(bpanels_base + (uint32_t)(p * BN * skb_max), &args.tmSB[shared ? 1 : 0], 0,
+                      b_row0, bfull_bar(p), pol_t);
+        }
+        __syncwarp();
+      }
+      const int n_mma = (tl.n_valid + 15) / 16 * 16;
+      const int bsel = n_mma <= 16 ? 2 : 0;
+      const int box_rows = n_mma <= 16 ? 16 : BN;
+      const uint32_t tx = C::A_BYTES + C::AS_BYTES + (uint32_t)box_rows * 128u;
+      // Per-lane operands: lanes < NA weight codes, NA..2NA-1 their scale
+      // boxes (x in 16-byte steps), 2NA the token codes.
+      const CUtensorMap* my_map = &args.tmA[(shared ? 2 : 0) + (lane % NA)];
+      int my_row = a_row0;
+      uint32_t my_off = (uint32_t)((lane % NA) * 64 * 128);
+      uint64_t my_pol = pol_w;
+      bool scale_box = false;
+      if (lane >= NA && lane < 2 * NA) {
+        my_map = &args.tmAS[(shared ? 2 : 0) + (lane - NA)];
+        my_off = C::AS_OFF + (uint32_t)((lane - NA) * 64 * 16);
+        scale_box = true;
+      } else if (lane == 2 * NA) {
+        my_map = &args.tmB[(shared ? 3 : 0) + bsel];
+        my_row = b_row0;
+        my_off = C::B_OFF;
+        my_pol = pol_t;
+      }
+      const int nkb = kdim / C::BK;
+      const int kb0 = kb_first;
+      kb_first = 0;
+      for (int kb = kb0; kb < nkb; ++kb) {
+        const int s = stg;
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(empty_bar(s), ph ^ 1u, args.status, limit);
+        if (!__shfl_sync(0xffffffffu, wok, 0)) {
+          ok = false;
+          break;
+        }
+        ++it;
+        if (++stg == STAGES) {
+          stg = 0;
+          ph ^= 1u;
+        }
+        const uint32_t dst = stages_base + (uint32_t)s * C::STAGE_BYTES;
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
+        __syncwarp();
+        if (lane < NLOADS)
+          tma_load_2d(dst + my_off, my_map, scale_box ? (kb >> 2) * 16 : kb * C::BK, my_row,
+                      full_bar(s), my_pol);
+      }
+    }
+    if (lane == 0) {
+      const uint32_t n_last = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+      for (uint32_t i = it - n_last; i < it; ++i)
+        mbar_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u, nullptr, 20000000ull);
+      const uint32_t p_last = lt < 2u ? lt : 2u;
+      for (uint32_t i = lt - p_last; i < lt; ++i)
+        mbar_wait(bfull_bar((int)(i & 1u)), (i >> 1) & 1u, nullptr, 20000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t i = 0;  // global stage index
+      bool ok = true;
+      for (int u = cid; u < total && ok; u += ncl) {
+        const Tile tl = tile_of(u);
+        const int kdim = (tl.g == E) ? args.kdim_shared : args.kdim_routed;
+        const int n_mma = (tl.n_valid + 15) / 16 * 16;
+        const uint32_t idesc = umma_idesc(UmmaOf<uint8_t>::fmt, C::BM, (uint32_t)n_mma);
+        for (int kb = 0; kb < kdim / C::BK; ++kb, ++i) {
+          const int s = (int)(i % STAGES), g = (int)(i % C::NG);
+          if (!mbar_wait(full_bar(s), (i / STAGES) & 1u, args.status, limit) ||
+              !mbar_wait(pempty_bar(g), ((i / C::NG) & 1u) ^ 1u, args.status, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = stages_base + (uint32_t)s * C::STAGE_BYTES;
+          const uint32_t b_addr = a_addr + C::B_OFF;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            umma_issue<kKindF8>(tmem_base + (uint32_t)((g * 4 + b) * BN),
+                                umma_desc_sw128(a_addr + b * 32), umma_desc_sw128(b_addr + b * 32),
+                                idesc, 0u);
+          umma_commit(empty_bar(s));
+          umma_commit(pfull_bar(g));
+        }
+      }
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, nullptr, 20000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ scalers + epilogue
+    // Warp w: TMEM lane quarter w % 4 (thread = weight row), blocks 2 bh and
+    // 2 bh + 1 of every stage (bh = (w - 2) / 4), all 32 token columns. Every
+    // decision to stop is taken from the shared abort flag after a barrier, so
+    // that all scaler warps pass the same barriers.
+    const int q = warp & 3;
+    const int bh = (warp - 2) >> 2;
+    const int r = q * 32 + lane;  // weight row of the unit = TMEM lane
+    const int et = threadIdx.x - 64;  // 0..255
+    constexpr int NT = 32 * C::SCALER_WARPS;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(bh * 2 * BN);
+    uint32_t lt = 0, i = 0;
+    for (int u = cid; u < total; u += ncl, ++lt) {
+      const Tile tl = tile_of(u);
+      const bool shared = tl.g == E;
+      const int kdim = shared ? args.kdim_shared : args.kdim_routed;
+      const int skb = shared ? args.skb_shared : args.skb_routed;
+      const int nblk = kdim / 32;
+      // Token scales of the tile as floats, block-major: fpanel[b][n].
+      const int p = (int)(lt & 1u);
+      if (et == 0 && !mbar_wait(bfull_bar(p), (lt >> 1) & 1u, args.status, limit))
+        *abort_flag = 1;
+      named_barrier_sync(1, NT);
+      if (*abort_flag) break;
+      mbar_wait(bfull_bar(p), (lt >> 1) & 1u, nullptr, limit);  // completed: this thread's acquire
+      {
+        const uint8_t* bp = bpanels + (size_t)p * BN * skb_max;
+        for (int e = et; e < nblk * BN; e += NT) {
+          const int b = e / BN, n = e - b * BN;
+          fpanel[e] = mx_scale_of(bp[n * skb + b]);
+        }
+      }
+      named_barrier_sync(1, NT);
+      if (lane == 0) mbar_arrive(bempty_bar(p));
+      float acc[BN];
+#pragma unroll
+      for (int n = 0; n < BN; ++n) acc[n] = 0.0f;
+      for (int kb = 0; kb < kdim / C::BK; ++kb, ++i) {
+        const int s = (int)(i % STAGES), g = (int)(i % C::NG);
+        if (!warp_wait(pfull_bar(g), (i / C::NG) & 1u, args.status, limit)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        float P[2 * BN];
+        tmem_ld64(t_lane + (uint32_t)(g * 4 * BN), P);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pempty_bar(g));
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(
+            stages + (size_t)s * C::STAGE_BYTES + C::AS_OFF + r * 16 + (kb & 3) * 4);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = 2 * bh + bb;
+          const float sa = mx_scale_of((sw >> (8 * b)) & 0xFFu);
+          const float4* fb = reinterpret_cast<const float4*>(fpanel + (size_t)(kb * 4 + b) * BN);
+#pragma unroll
+          for (int n4 = 0; n4 < BN / 4; ++n4) {
+            const float4 sb = fb[n4];
+            acc[4 * n4 + 0] = fmaf(P[bb * BN + 4 * n4 + 0] * sb.x, sa, acc[4 * n4 + 0]);
+            acc[4 * n4 + 1] = fmaf(P[bb * BN + 4 * n4 + 1] * sb.y, sa, acc[4 * n4 + 1]);
+            acc[4 * n4 + 2] = fmaf(P[bb * BN + 4 * n4 + 2] * sb.z, sa, acc[4 * n4 + 2]);
+            acc[4 * n4 + 3] = fmaf(P[bb * BN + 4 * n4 + 3] * sb.w, sa, acc[4 * n4 + 3]);
+          }
+        }
+      }
+      named_barrier_sync(1, NT);
+      if (*abort_flag) break;
+      // The two halves' partial sums, added in smem: epi[row][n].
+      if (bh == 0) {
+#pragma unroll
+        for (int n = 0; n < BN; ++n) epi[r * 33 + n] = acc[n];
+      }
+      named_barrier_sync(1, NT);
+      if (bh == 1) {
+#pragma unroll
+        for (int n = 0; n < BN; ++n) epi[r * 33 + n] += acc[n];
+      }
+      named_barrier_sync(1, NT);
+      if constexpr (GATED) {
+        // Thread: token column jj, features 8 fg .. 8 fg + 7 of the unit's 64;
+        // a block of 32 features is four neighbouring threads (fg & 3).
+        const int jj = et >> 3, fg = et & 7;
+        float hv[8];
+        float amax = 0.0f;
+#pragma unroll
+        for (int f = 0; f < 8; ++f) {
+          const float gt = epi[(fg * 8 + f) * 33 + jj];
+          const float up = epi[(64 + fg * 8 + f) * 33 + jj];
+          hv[f] = __fdividef(gt, 1.0f + __expf(-gt)) * up;
+          amax = fmaxf(amax, fabsf(hv[f]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int e = mx_block_exponent(amax);
+        const float inv = mx_pow2(-e);
+        const uint32_t lo = mx_encode4(hv[0] * inv, hv[1] * inv, hv[2] * inv, hv[3] * inv);
+        const uint32_t hi = mx_encode4(hv[4] * inv, hv[5] * inv, hv[6] * inv, hv[7] * inv);
+        if (jj < tl.n_valid) {
+          uint8_t* out = reinterpret_cast<uint8_t*>(shared ? args.out_shared : args.out);
+          uint8_t* osc = shared ? args.out_shared_scales : args.out_scales;
+          const int ld = shared ? args.ld_out_shared : args.ld_out_routed;
+          const int sko = shared ? args.sko_shared : args.sko_routed;
+          const size_t row = (size_t)(shared ? tl.p0 - offs[E] : tl.p0) + jj;
+          const int f0 = tl.nb * 64 + fg * 8;
+          *reinterpret_cast<uint2*>(out + row * ld + f0) = make_uint2(lo, hi);
+          if ((fg & 3) == 0) osc[row * sko + f0 / 32] = (uint8_t)(e + 127);
+        }
+      } else {
+        // Per-token destination rows and gate weights; then thread = output
+        // feature r, token columns 16 bh .. 16 bh + 15.
+        int32_t* yrow = reinterpret_cast<int32_t*>(epi + 128 * 33);
+        float* wt = epi + 128 * 33 + BN;
+        for (int j = et; j < tl.n_valid; j += NT) {
+          int row;
+          float wv;
+          if (shared) {
+            const int t = tl.p0 - offs[E] + j;
+            row = t * args.KP + args.k;
+            wv = 1.0f;
+          } else {
+            const int s = args.gather_idx[tl.p0 + j];
+            if ((unsigned)s < (unsigned)(args.T * args.k)) {
+              const int t = s / args.k;
+              row = t * args.KP + (s - t * args.k);
+              wv = args.topk_w[s];
+            } else {  // device check: reported; the column goes to row 0 as zeros
+              set_status(args.status, MOE_ERR_DEVICE_CHECK);
+              row = 0;
+              wv = 0.f;
+            }
+          }
+          yrow[j] = row;
+          wt[j] = wv;
+        }
+        named_barrier_sync(1, NT);
+        float* Yc = reinterpret_cast<float*>(args.out) + tl.nb * 128 + r;
+        const size_t H = (size_t)args.n_out_routed;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          const int j = bh * 16 + n;
+          if (j < tl.n_valid) Yc[(size_t)yrow[j] * H] = wt[j] * epi[r * 33 + j];
+        }
+      }
+      named_barrier_sync(1, NT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
 // Opt-in shared memory of the current device, looked up once per device.
 int smem_optin() {
   static int cache[64] = {0};
@@ -610,14 +1070,146 @@ void fill_mx_common(MxGemmArgs& a, const GemmProblem& p, const int32_t* offsets,
 
 }  // namespace
 
+namespace {
+
+template <bool GATED, int STAGES>
+cudaError_t launch_mx_dec_variant(const MxGemmArgs& a, int num_sms, size_t upper_units,
+                                  cudaStream_t st) {
+  using C = MxDecCfg<GATED, STAGES>;
+  const int skb_max = a.skb_routed > a.skb_shared ? a.skb_routed : a.skb_shared;
+  const int kmax = a.kdim_routed > a.kdim_shared ? a.kdim_routed : a.kdim_shared;
+  const size_t smem = C::smem_bytes(a.E, skb_max, kmax / 32);
+  const int optin = smem_optin();
+  if (smem > (size_t)optin) return cudaErrorInvalidValue;
+  auto fn = mx_dec_kernel<GATED, STAGES>;
+  cudaError_t e = ensure_smem_attr((const void*)fn, (size_t)optin);
+  if (e != cudaSuccess) return e;
+  size_t grid = (size_t)num_sms;
+  if (upper_units < grid) grid = upper_units;
+  if (grid == 0) return cudaSuccess;
+  return launch_chained(fn, dim3((unsigned)grid), dim3(C::THREADS), smem, st, 1, a);
+}
+
+// The deepest ring of 22 KB stages (8, 6 or 4) that fits next to the token
+// scale panels of the problem.
+template <bool GATED>
+cudaError_t launch_mx_dec(const MxGemmArgs& a, int num_sms, size_t ub, cudaStream_t st) {
+  const int skb_max = a.skb_routed > a.skb_shared ? a.skb_routed : a.skb_shared;
+  const int kmax = a.kdim_routed > a.kdim_shared ? a.kdim_routed : a.kdim_shared;
+  const size_t optin = (size_t)smem_optin();
+  if (MxDecCfg<GATED, 8>::smem_bytes(a.E, skb_max, kmax / 32) <= optin)
+    return launch_mx_dec_variant<GATED, 8>(a, num_sms, ub, st);
+  if (MxDecCfg<GATED, 6>::smem_bytes(a.E, skb_max, kmax / 32) <= optin)
+    return launch_mx_dec_variant<GATED, 6>(a, num_sms, ub, st);
+  return launch_mx_dec_variant<GATED, 4>(a, num_sms, ub, st);
+}
+
+}  // namespace
+
+bool mx_uses_decode_kernels(const GemmProblem& p) { return mx_decode_tiles(p); }
+
+cudaError_t launch_mx_dec_swiglu_gemm(const GemmProblem& p, const MxWeights& w,
+                                      const MxDecTokens& x, const int32_t* offsets,
+                                      const int32_t* gather_idx, const MxDecOut& h, int* status,
+                                      cudaStream_t st) {
+  const bool has_s = p.Is > 0;
+  const int skH = mx_scale_cols(p.H), skI = mx_scale_cols(p.I);
+  const int skIs = has_s ? mx_scale_cols(p.Is) : skI;
+  MxGemmArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t R = (uint64_t)p.E * p.I;
+  bool ok = make_tma_map(&a.tmA[0], w.gate, MOE_DTYPE_E4M3, R, p.H, 64) &&
+            make_tma_map(&a.tmA[1], w.up, MOE_DTYPE_E4M3, R, p.H, 64) &&
+            make_scale_map(&a.tmAS[0], w.s_gate, R, skH, 64, 16) &&
+            make_scale_map(&a.tmAS[1], w.s_up, R, skH, 64, 16) &&
+            make_b_maps(&a.tmB[0], x.routed, MOE_DTYPE_E4M3, (uint64_t)p.T * p.k, p.H, 32, 16) &&
+            make_b_maps(&a.tmB[3], x.shared, MOE_DTYPE_E4M3, p.T, p.H, 32, 16) &&
+            make_scale_map(&a.tmSB[0], x.routed_scales, (uint64_t)p.T * p.k, skH, 32) &&
+            make_scale_map(&a.tmSB[1], x.shared_scales, p.T, skH, 32);
+  if (ok && has_s)
+    ok = make_tma_map(&a.tmA[2], w.sh_gate, MOE_DTYPE_E4M3, p.Is, p.H, 64) &&
+         make_tma_map(&a.tmA[3], w.sh_up, MOE_DTYPE_E4M3, p.Is, p.H, 64) &&
+         make_scale_map(&a.tmAS[2], w.sh_s_gate, p.Is, skH, 64, 16) &&
+         make_scale_map(&a.tmAS[3], w.sh_s_up, p.Is, skH, 64, 16);
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_s) {
+    a.tmA[2] = a.tmA[0];
+    a.tmA[3] = a.tmA[1];
+    a.tmAS[2] = a.tmAS[0];
+    a.tmAS[3] = a.tmAS[1];
+  }
+  fill_mx_common(a, p, offsets, gather_idx, status, 32);
+  a.out = h.routed;
+  a.out_shared = h.shared;
+  a.out_scales = h.routed_scales;
+  a.out_shared_scales = h.shared_scales;
+  a.sko_routed = skI;
+  a.sko_shared = skIs;
+  a.n_out_routed = p.I;
+  a.n_out_shared = has_s ? p.Is : 64;
+  a.kdim_routed = p.H;
+  a.kdim_shared = p.H;
+  a.skb_routed = skH;
+  a.skb_shared = skH;
+  a.ld_out_routed = p.I;
+  a.ld_out_shared = has_s ? p.Is : 0;
+  const size_t ub = unit_upper_bound(p.T, p.k, p.E, 32, p.I / 64, has_s ? p.Is / 64 : 0);
+  return launch_mx_dec<true>(a, p.num_sms, ub, st);
+}
+
+cudaError_t launch_mx_dec_down_gemm(const GemmProblem& p, const MxWeights& w,
+                                    const MxDecTokens& h, const int32_t* offsets,
+                                    const int32_t* gather_idx, const float* topk_w, float* Y,
+                                    int* status, cudaStream_t st) {
+  const bool has_s = p.Is > 0;
+  const int skI = mx_scale_cols(p.I);
+  const int skIs = has_s ? mx_scale_cols(p.Is) : skI;
+  MxGemmArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t R = (uint64_t)p.E * p.H;
+  bool ok = make_tma_map(&a.tmA[0], w.down, MOE_DTYPE_E4M3, R, p.I, 128) &&
+            make_scale_map(&a.tmAS[0], w.s_down, R, skI, 128, 16) &&
+            make_b_maps(&a.tmB[0], h.routed, MOE_DTYPE_E4M3, (uint64_t)p.T * p.k, p.I, 32, 16) &&
+            make_scale_map(&a.tmSB[0], h.routed_scales, (uint64_t)p.T * p.k, skI, 32);
+  if (ok && has_s)
+    ok = make_tma_map(&a.tmA[2], w.sh_down, MOE_DTYPE_E4M3, p.H, p.Is, 128) &&
+         make_scale_map(&a.tmAS[2], w.sh_s_down, p.H, skIs, 128, 16) &&
+         make_b_maps(&a.tmB[3], h.shared, MOE_DTYPE_E4M3, p.T, p.Is, 32, 16) &&
+         make_scale_map(&a.tmSB[1], h.shared_scales, p.T, skIs, 32);
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_s) {
+    a.tmA[2] = a.tmA[0];
+    a.tmAS[2] = a.tmAS[0];
+    for (int i = 0; i < 3; ++i) a.tmB[3 + i] = a.tmB[i];
+    a.tmSB[1] = a.tmSB[0];
+  }
+  a.tmA[1] = a.tmA[0];
+  a.tmA[3] = a.tmA[2];
+  a.tmAS[1] = a.tmAS[0];
+  a.tmAS[3] = a.tmAS[2];
+  fill_mx_common(a, p, offsets, gather_idx, status, 32);
+  a.topk_w = topk_w;
+  a.out = Y;
+  a.n_out_routed = p.H;
+  a.n_out_shared = p.H;
+  a.kdim_routed = p.I;
+  a.kdim_shared = has_s ? p.Is : p.I;
+  a.skb_routed = skI;
+  a.skb_shared = skIs;
+  const size_t ub = unit_upper_bound(p.T, p.k, p.E, 32, p.H / 128, has_s ? p.H / 128 : 0);
+  return launch_mx_dec<false>(a, p.num_sms, ub, st);
+}
+
 bool mx_problem_fits(const GemmProblem& p) {
   const size_t optin = (size_t)smem_optin();
   const int skH = mx_scale_cols(p.H), skI = mx_scale_cols(p.I);
   const int skIs = p.Is > 0 ? mx_scale_cols(p.Is) : 0;
   const int skd = skI > skIs ? skI : skIs;
-  if (mx_decode_tiles(p))
-    return MxCfg<true, 32, 4>::smem_bytes(p.E, skH) <= optin &&
-           MxCfg<false, 32, 4>::smem_bytes(p.E, skd) <= optin;
+  if (mx_decode_tiles(p)) {
+    const int kd = p.I > p.Is ? p.I : p.Is;
+    return MxDecCfg<true, 4>::smem_bytes(p.E, skH, p.H / 32) <= optin &&
+           MxDecCfg<false, 4>::smem_bytes(p.E, skd, kd / 32) <= optin;
+  }
   return MxCfg<true, 128, 2>::smem_bytes(p.E, skH) <= optin &&
          MxCfg<false, 128, 2>::smem_bytes(p.E, skd) <= optin;
 }

@@ -16,10 +16,11 @@ namespace moe {
 // or the encoder rejects the shape.
 bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
                   uint32_t box_rows);
-// Tensor map of a uint8 [rows][cols] matrix whose box is whole rows (cols
-// bytes, a multiple of 16 and at most 256) of box_rows rows, no swizzle.
+// Tensor map of a uint8 [rows][cols] matrix (cols a multiple of 16) whose box
+// is box_cols bytes (0: whole rows; a multiple of 16, at most 256) of box_rows
+// rows, no swizzle.
 bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t cols,
-                    uint32_t box_rows);
+                    uint32_t box_rows, uint32_t box_cols = 0);
 // Tensor maps of a tiled token operand [rows][cols]: boxes of b_rows, box1 and
 // 16 rows.
 bool make_b_maps(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
@@ -162,6 +163,25 @@ cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, cons
 cudaError_t launch_mx_down_gemm(const GemmProblem& p, const MxWeights& w, const void* h,
                                 const void* hs, const int32_t* offsets, const int32_t* gather_idx,
                                 const float* topk_w, float* Y, int* status, cudaStream_t st);
+// Decode-sized problems (32-token tiles) run the E4M3-MMA kernels instead:
+// token operands are MXFP8 codes with scale rows; the gate/up GEMM writes h
+// and h_shared the same way.
+bool mx_uses_decode_kernels(const GemmProblem& p);
+struct MxDecTokens {
+  const uint8_t *routed, *routed_scales;  // rows by position [T*k]
+  const uint8_t *shared, *shared_scales;  // rows by token [T] (x, or h_shared)
+};
+struct MxDecOut {
+  uint8_t *routed, *routed_scales, *shared, *shared_scales;
+};
+cudaError_t launch_mx_dec_swiglu_gemm(const GemmProblem& p, const MxWeights& w,
+                                      const MxDecTokens& x, const int32_t* offsets,
+                                      const int32_t* gather_idx, const MxDecOut& h, int* status,
+                                      cudaStream_t st);
+cudaError_t launch_mx_dec_down_gemm(const GemmProblem& p, const MxWeights& w,
+                                    const MxDecTokens& h, const int32_t* offsets,
+                                    const int32_t* gather_idx, const float* topk_w, float* Y,
+                                    int* status, cudaStream_t st);
 
 // Combine (combine.cu): y[t] = sum_j Y[t][j] for j < KP, rank order.
 cudaError_t launch_combine(int dtype, const float* Y, int T, int H, int KP, void* y,

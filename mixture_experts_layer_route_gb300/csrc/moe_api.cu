@@ -39,6 +39,11 @@ struct Layout {
   // scales (routed and shared); 0 otherwise.
   size_t xq, sx, hq, sh, hsq, shs;
   size_t xm;  // MXFP8 layers only: quantized token rows (bf16 values); 0 otherwise
+  // MXFP8 layers on the decode-sized kernels: token codes and scale rows
+  // (xq above holds the codes), their expert-ordered copies (xg holds the
+  // codes), and the scale rows of h and h_shared (h, hs hold the codes).
+  size_t xs, xgs, hsc, hss;
+  bool mx_dec;
   int S;  // router split count
 };
 
@@ -63,6 +68,12 @@ size_t elem_bytes(int dtype) {
 // Dtype of the activations (x, W_router, h, y): bf16 for E4M3 and MXFP8 layers.
 int act_dtype(int dtype) {
   return (dtype == MOE_DTYPE_E4M3 || dtype == MOE_DTYPE_MXFP8) ? MOE_DTYPE_BF16 : dtype;
+}
+
+// MXFP8 problems with decode-sized token tiles run the E4M3-MMA kernels
+// (grouped_gemm_mx.cu), whose token operands are codes with scale rows.
+bool mx_decode_kernels(const moe_problem& p) {
+  return p.tile == MOE_TILE_DECODE || (p.tile == MOE_TILE_AUTO && p.T <= 64);
 }
 
 Layout layout_of(const moe_problem& p) {
@@ -93,9 +104,21 @@ Layout layout_of(const moe_problem& p) {
   // Prefill-sized tiles read the routed token rows from an expert-ordered copy.
   L.xq = f8 ? take(T * (size_t)p.H) : 0;
   L.sx = f8 ? take(T * 4) : 0;
-  // MXFP8 layers: the quantized token rows (bf16 values), and always their
-  // expert-ordered copy (both MXFP8 GEMMs read tiled token rows).
-  L.xm = mx ? take(T * (size_t)p.H * 2) : 0;
+  // MXFP8 layers: the quantized token rows (bf16 values, or E4M3 codes and
+  // scale rows for the decode-sized kernels), and always their expert-ordered
+  // copy (both MXFP8 GEMMs read tiled token rows).
+  L.mx_dec = mx && mx_decode_kernels(p);
+  L.xm = mx && !L.mx_dec ? take(T * (size_t)p.H * 2) : 0;
+  if (L.mx_dec) {
+    const size_t skH = (size_t)moe_mx_scale_cols(p.H);
+    L.xq = take(T * (size_t)p.H);
+    L.xs = take(T * skH);
+    L.xgs = take(T * k * skH);
+    L.hsc = take(T * k * (size_t)moe_mx_scale_cols(p.I));
+    L.hss = p.I_shared > 0 ? take(T * (size_t)moe_mx_scale_cols(p.I_shared)) : 0;
+  } else {
+    L.xs = L.xgs = L.hsc = L.hss = 0;
+  }
   L.xg = (needs_copy(p) || mx) ? take(T * k * (size_t)p.H * es) : 0;
   L.h = take(T * k * (size_t)p.I * as);
   L.hs = p.I_shared > 0 ? take(T * (size_t)p.I_shared * as) : 0;
@@ -245,6 +268,8 @@ moe_status moe_get_workspace_layout(const moe_problem* pb, moe_workspace_layout*
   out->slot_pos = (int64_t)L.slotpos;
   out->h = (int64_t)L.h;
   out->h_shared = pb->I_shared > 0 ? (int64_t)L.hs : -1;
+  out->h_scales = L.mx_dec ? (int64_t)L.hsc : -1;
+  out->h_shared_scales = L.mx_dec && pb->I_shared > 0 ? (int64_t)L.hss : -1;
   return MOE_OK;
 }
 
@@ -685,7 +710,7 @@ moe_status moe_forward_mx(const moe_problem* pb, const void* x, const void* W_ro
   int32_t* offs = at<int32_t>(workspace, L.offsets);
   int32_t* gidx = at<int32_t>(workspace, L.gather);
   int32_t* spos = at<int32_t>(workspace, L.slotpos);
-  void* xm = at<void>(workspace, L.xm);
+  void* xm = L.xm ? at<void>(workspace, L.xm) : nullptr;
   void* xg = at<void>(workspace, L.xg);
   void* h = at<void>(workspace, L.h);
   void* hs = has_s ? at<void>(workspace, L.hs) : nullptr;
@@ -711,22 +736,56 @@ moe_status moe_forward_mx(const moe_problem* pb, const void* x, const void* W_ro
     e = launch_permute(ids, g.T, g.E, g.k, has_s ? 1 : 0, offs, gidx, spos, status,
                        at<int32_t>(workspace, L.pscratch), st);
   }
-  // Token rows to their MXFP8 values (bf16), then their expert-ordered copy.
-  if (e == cudaSuccess) {
-    NvtxRange r("quantize_x");
-    e = launch_qdq_mx(x, g.T, g.H, xm, g.num_sms, st);
-  }
-  if (e == cudaSuccess) {
-    NvtxRange r("dispatch_copy");
-    e = launch_gather_rows(xm, spos, g.T * g.k, g.k, (size_t)g.H * 2, xg, status, g.num_sms, st);
-  }
-  if (e == cudaSuccess) {
-    NvtxRange r("gate_up_gemm");
-    e = launch_mx_swiglu_gemm(g, mw, xm, xg, offs, gidx, h, hs, status, st);
-  }
-  if (e == cudaSuccess) {
-    NvtxRange r("down_gemm");
-    e = launch_mx_down_gemm(g, mw, h, hs, offs, gidx, w, Y, status, st);
+  if (L.mx_dec) {
+    // Decode-sized batches: token rows to MXFP8 codes and scale rows, their
+    // expert-ordered copies, then the E4M3-MMA GEMMs (h as codes and scales).
+    const size_t skH = (size_t)moe_mx_scale_cols(g.H);
+    uint8_t* xq = at<uint8_t>(workspace, L.xq);
+    uint8_t* xs = at<uint8_t>(workspace, L.xs);
+    uint8_t* xgq = at<uint8_t>(workspace, L.xg);
+    uint8_t* xgs = at<uint8_t>(workspace, L.xgs);
+    const MxDecTokens xt = {xgq, xgs, xq, xs};
+    const MxDecOut ho = {at<uint8_t>(workspace, L.h), at<uint8_t>(workspace, L.hsc),
+                         has_s ? at<uint8_t>(workspace, L.hs) : nullptr,
+                         has_s ? at<uint8_t>(workspace, L.hss) : nullptr};
+    const MxDecTokens ht = {ho.routed, ho.routed_scales, ho.shared, ho.shared_scales};
+    if (e == cudaSuccess) {
+      NvtxRange r("quantize_x");
+      e = launch_quantize_mx(MOE_DTYPE_BF16, x, g.T, g.H, xq, xs, g.num_sms, st);
+    }
+    if (e == cudaSuccess) {
+      NvtxRange r("dispatch_copy");
+      e = launch_gather_rows(xq, spos, g.T * g.k, g.k, (size_t)g.H, xgq, status, g.num_sms, st);
+      if (e == cudaSuccess)
+        e = launch_gather_rows(xs, spos, g.T * g.k, g.k, skH, xgs, status, g.num_sms, st);
+    }
+    if (e == cudaSuccess) {
+      NvtxRange r("gate_up_gemm");
+      e = launch_mx_dec_swiglu_gemm(g, mw, xt, offs, gidx, ho, status, st);
+    }
+    if (e == cudaSuccess) {
+      NvtxRange r("down_gemm");
+      e = launch_mx_dec_down_gemm(g, mw, ht, offs, gidx, w, Y, status, st);
+    }
+  } else {
+    // Token rows to their MXFP8 values (bf16), then their expert-ordered copy.
+    if (e == cudaSuccess) {
+      NvtxRange r("quantize_x");
+      e = launch_qdq_mx(x, g.T, g.H, xm, g.num_sms, st);
+    }
+    if (e == cudaSuccess) {
+      NvtxRange r("dispatch_copy");
+      e = launch_gather_rows(xm, spos, g.T * g.k, g.k, (size_t)g.H * 2, xg, status, g.num_sms,
+                             st);
+    }
+    if (e == cudaSuccess) {
+      NvtxRange r("gate_up_gemm");
+      e = launch_mx_swiglu_gemm(g, mw, xm, xg, offs, gidx, h, hs, status, st);
+    }
+    if (e == cudaSuccess) {
+      NvtxRange r("down_gemm");
+      e = launch_mx_down_gemm(g, mw, h, hs, offs, gidx, w, Y, status, st);
+    }
   }
   if (e == cudaSuccess) {
     NvtxRange r("combine");

@@ -8,7 +8,8 @@ stored h (bf16 values of MXFP8 codes) is decided from the GPU's own fp32 h,
 whose sums run in another order than the oracle's: it equals the oracle's at
 all but a few positions (a code or a block scale on the other side of a
 rounding boundary), and there by at most one E4M3 step (a quarter of the
-value). y is held to the layer's bound max|gpu - oracle| <= 2e-2 rms and
+value). Decode-sized batches run the E4M3-MMA kernels, which store h as MXFP8
+codes with scale rows; the check reads their values. y is held to the layer's bound max|gpu - oracle| <= 2e-2 rms and
 rel-L2 <= 5e-3 (fp32 output); the bf16 y is that fp32 y rounded to nearest.
 """
 import numpy as np
@@ -77,6 +78,17 @@ def _layer_and_ref(oracle, cfg, tile=m.MOE_TILE_AUTO, n_group=1, topk_group=1, s
     return d, n, layer, ref, inter
 
 
+def stored_h(oracle, ws, off, scales_off, rows, cols):
+    """The layer's stored h as values: MXFP8 codes with scale rows (decode-sized
+    kernels), else bf16 values."""
+    if scales_off >= 0:
+        sk = m.mx_scale_cols(cols)
+        q = ws[off:off + rows * cols].view(rows, cols).cpu().numpy()
+        sc = ws[scales_off:scales_off + rows * sk].view(rows, sk).cpu().numpy()
+        return oracle.dequantize_mx(q, sc)
+    return ws[off:off + rows * cols * 2].view(torch.bfloat16).view(rows, cols).float().cpu().numpy()
+
+
 def assert_mx_h(h_gpu, h_ref, what):
     """Equal but at a few positions, and there within one E4M3 step."""
     h_gpu = np.asarray(h_gpu, np.float64)
@@ -107,12 +119,10 @@ def test_forward_mx_vs_oracle(oracle, cfg):
     np.testing.assert_array_equal(gids.cpu().numpy(), inter["ids"])
     gw = ws[lay["topk_w"]:lay["topk_w"] + T * k * 4].view(torch.float32).view(T, k)
     np.testing.assert_allclose(gw.cpu().numpy(), inter["w"], rtol=0, atol=1e-6)
-    h = ws[lay["h"]:lay["h"] + T * k * I * 2].view(torch.bfloat16).view(T * k, I)
-    assert_mx_h(h.float().cpu().numpy(), inter["h"], "h")
+    assert_mx_h(stored_h(oracle, ws, lay["h"], lay["h_scales"], T * k, I), inter["h"], "h")
     if cfg.I_shared:
-        o = lay["h_shared"]
-        hs = ws[o:o + T * cfg.I_shared * 2].view(torch.bfloat16).view(T, cfg.I_shared)
-        assert_mx_h(hs.float().cpu().numpy(), inter["hs"], "h_shared")
+        hs = stored_h(oracle, ws, lay["h_shared"], lay["h_shared_scales"], T, cfg.I_shared)
+        assert_mx_h(hs, inter["hs"], "h_shared")
     assert_close(y32.cpu().numpy(), ref, "y")
     assert_bf16_is_rounded(y, y32)
     # a second call repeats the result bit for bit
