@@ -65,12 +65,10 @@ struct MxGemmArgs {
   int ld_out_routed, ld_out_shared;
   unsigned flags;
   int m_lo, m_hi, tile_n;
-  // Decode kernel only (mx_dec_kernel; unused by mx_gemm_kernel):
-  // tmAS: the weights' scale rows again, boxes of 16 bytes (four stages) of
-  // 64 (GATED) or 128 rows, indexed like tmA; tmB then holds E4M3 token codes
-  // (128-byte boxes, 128-byte swizzle) and tmSB their scale rows, whole rows of
-  // 32 tokens: [0] routed rows by position, [1] the shared expert's by token.
-  CUtensorMap tmAS[4];
+  // Decode kernel only (mx_dec_kernel; unused by mx_gemm_kernel): tmB then
+  // holds E4M3 token codes (128-byte boxes, 128-byte swizzle) and tmSB their
+  // scale rows, whole rows of 32 tokens: [0] routed rows by position, [1] the
+  // shared expert's by token.
   CUtensorMap tmSB[2];
   int skb_routed, skb_shared;       // scale bytes per token row of the B operand
   // GATED: scale rows of h / h_shared (the MXFP8 codes go to out / out_shared).
@@ -168,6 +166,23 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// (a0, a1) += (p0 * s0, p1 * s1) * sa with packed fp32 pair instructions (one
+// multiply and one fused multiply-add for the two lanes of the pair; each
+// element is rounded exactly as fmaf(p * s, sa, a)).
+__device__ __forceinline__ void mul_fma2(float& a0, float& a1, float p0, float p1, float s0,
+                                         float s1, float sa) {
+  asm("{\n\t.reg .b64 pp, ps, pt, pa, pc;\n\t"
+      "mov.b64 pp, {%2, %3};\n\t"
+      "mov.b64 ps, {%4, %5};\n\t"
+      "mul.rn.f32x2 pt, pp, ps;\n\t"
+      "mov.b64 pa, {%6, %6};\n\t"
+      "mov.b64 pc, {%0, %1};\n\t"
+      "fma.rn.f32x2 pc, pt, pa, pc;\n\t"
+      "mov.b64 {%0, %1}, pc;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(p0), "f"(p1), "f"(s0), "f"(s1), "f"(sa));
 }
 
 // All lanes wait (each thread's own acquire of the phase); the warp agrees on
@@ -594,9 +609,9 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
 // decode sizes an MMA's time is set by its A bytes, so E4M3 operands run twice
 // as fast as their bf16 values would.
 //
-// Warp roles: warp 0 producer (per stage: the weight codes, their 16-byte
-// scale boxes (four stages each) and the token codes; per unit: the token
-// tile's scale rows), warp 1 MMA issuer (four MMAs per stage into one of four
+// Warp roles: warp 0 producer (per stage: the weight codes and the token
+// codes; per unit: the scale rows of the unit's weight rows and of its token
+// tile, into one of two panel buffers), warp 1 MMA issuer (four MMAs per stage into one of four
 // slot groups of tensor memory), warps 2-9 scalers and epilogue (warp w: TMEM
 // lane quarter w % 4, blocks 2 bh and 2 bh + 1 of every stage for
 // bh = (w - 2) / 4, all token columns; the two halves' sums are added in
@@ -612,26 +627,28 @@ struct MxDecCfg {
   static constexpr int BK = 128;
   static constexpr int A_BYTES = BM * 128;   // codes
   static constexpr int B_BYTES = BN * 128;   // token codes
-  static constexpr int AS_BYTES = BM * 16;   // scale box of the weight rows
   static constexpr int B_OFF = A_BYTES;
-  static constexpr int AS_OFF = A_BYTES + B_BYTES;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + AS_BYTES;  // 22 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 20 KB
   static constexpr int NG = 4;               // partial slot groups (4 blocks x 32 columns)
   static constexpr int TMEM_COLS = 512;
   static constexpr int SCALER_WARPS = 8;
   static constexpr int THREADS = 64 + 32 * SCALER_WARPS;
   // Partial sums of the two scaler halves meet here (128 rows x 32 columns,
-  // padded), then DOWN's per-column destination rows and gate weights.
+  // padded), then DOWN's per-column destination rows and gate weights. The
+  // space is shared with the token scales as floats (fpanel), which are dead
+  // by then.
   static constexpr int EPI_FLOATS = 128 * 33 + 2 * BN;
-  // full, empty [STAGES]; pfull, pempty [NG]; bfull, bempty [2]; drain
+  // full, empty [STAGES]; pfull, pempty [NG]; scale panels full, empty [2]; drain
   static constexpr int NBARS = 2 * STAGES + 2 * NG + 5;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(NG * 4 * BN <= TMEM_COLS, "tensor memory");
 
-  // skb_max: token scale bytes per row; nblk_max: 32-element blocks of K.
+  // skb_max: scale bytes per row of the weights and of the tokens (the same
+  // contraction axis); nblk_max: 32-element blocks of K.
   static size_t smem_bytes(int E, int skb_max, int nblk_max) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + 2 * (size_t)BN * skb_max +
-           (size_t)nblk_max * BN * 4 + EPI_FLOATS * 4 + NBARS * 8 + 16 +
+    const size_t fp = (size_t)nblk_max * BN;
+    return 1024 + (size_t)STAGES * STAGE_BYTES + 2 * (size_t)(BM + BN) * skb_max +
+           4 * (fp > (size_t)EPI_FLOATS ? fp : (size_t)EPI_FLOATS) + NBARS * 8 + 16 +
            3 * (size_t)(E + 2) * 4;
   }
 };
@@ -649,11 +666,16 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
   const int skb_max = args.skb_routed > args.skb_shared ? args.skb_routed : args.skb_shared;
   const int kmax = args.kdim_routed > args.kdim_shared ? args.kdim_routed : args.kdim_shared;
   const int nblk_max = kmax / 32;
+  // Per unit, in one of two panel buffers: the weight rows' scale rows
+  // [BM][skb] followed by the token tile's [BN][skb].
+  const int panel_bytes = (C::BM + BN) * skb_max;
   uint8_t* stages = smem;
-  uint8_t* bpanels = stages + (size_t)STAGES * C::STAGE_BYTES;  // token scale bytes [2][BN][skb]
-  float* fpanel = reinterpret_cast<float*>(bpanels + 2 * (size_t)BN * skb_max);  // [blk][BN]
-  float* epi = fpanel + (size_t)nblk_max * BN;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_FLOATS);
+  uint8_t* panels = stages + (size_t)STAGES * C::STAGE_BYTES;
+  float* fpanel = reinterpret_cast<float*>(panels + 2 * (size_t)panel_bytes);  // [blk][BN]
+  float* epi = fpanel;  // used only after the unit's last stage
+  const size_t fp_floats = (size_t)nblk_max * BN;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      fpanel + (fp_floats > (size_t)C::EPI_FLOATS ? fp_floats : (size_t)C::EPI_FLOATS));
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* n_sched = reinterpret_cast<int*>(tmem_holder + 2);
@@ -673,14 +695,12 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
   auto bempty_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + 2 + p); };
   const uint32_t drain_bar = bars_base + 8u * (uint32_t)(B0 + 4);
   const uint32_t stages_base = smem_u32(stages);
-  const uint32_t bpanels_base = smem_u32(bpanels);
+  const uint32_t panels_base = smem_u32(panels);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      // The MMAs' commit, and every scaler warp once it has read the stage's
-      // weight scales.
-      mbar_init(empty_bar(s), 1 + C::SCALER_WARPS);
+      mbar_init(empty_bar(s), 1);
     }
     for (int g = 0; g < C::NG; ++g) {
       mbar_init(pfull_bar(g), 1);
@@ -696,7 +716,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmA[i]);
-    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmAS[i]);
+    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&args.tmS[i]);
     for (int i = 0; i < 6; ++i) tma_prefetch_desc(&args.tmB[i]);
     for (int i = 0; i < 2; ++i) tma_prefetch_desc(&args.tmSB[i]);
   }
@@ -732,7 +752,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
     bool ok = true;
     uint32_t lt = 0;
     constexpr int NA = GATED ? 2 : 1;
-    constexpr int NLOADS = 2 * NA + 1;  // codes and scale boxes of the weight rows, token codes
+    constexpr int NLOADS = NA + 1;  // weight codes, token codes
     for (int u = cid; u < total && ok; u += ncl, ++lt) {
       const Tile tl = tile_of(u);
       const bool shared = tl.g == E;
@@ -740,7 +760,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
       const int skb = shared ? args.skb_shared : args.skb_routed;
       const int a_row0 = (shared ? 0 : tl.g * args.n_out_routed) + tl.nb * C::WM;
       const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
-      {  // the token tile's scale rows
+      {  // the unit's scale panels: weight rows (one box per 64 / 128 rows), token rows
         const int p = (int)(lt & 1u);
         int wok = 1;
         if (lane == 0) wok = mbar_wait(bempty_bar(p), ((lt >> 1) & 1u) ^ 1u, args.status, limit);
@@ -748,29 +768,27 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
           ok = false;
           break;
         }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bfull_bar(p), (uint32_t)(BN * skb));
-          tma_load_2d(bpanels_base + (uint32_t)(p * BN * skb_max), &args.tmSB[shared ? 1 : 0], 0,
-                      b_row0, bfull_bar(p), pol_t);
-        }
+        const uint32_t pdst = panels_base + (uint32_t)(p * panel_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(bfull_bar(p), (uint32_t)((C::BM + BN) * skb));
         __syncwarp();
+        if (lane < NA)
+          tma_load_2d(pdst + (uint32_t)(lane * 64 * skb), &args.tmS[(shared ? 2 : 0) + lane], 0,
+                      a_row0, bfull_bar(p), pol_w);
+        else if (lane == NA)
+          tma_load_2d(pdst + (uint32_t)(C::BM * skb), &args.tmSB[shared ? 1 : 0], 0, b_row0,
+                      bfull_bar(p), pol_t);
       }
       const int n_mma = (tl.n_valid + 15) / 16 * 16;
       const int bsel = n_mma <= 16 ? 2 : 0;
       const int box_rows = n_mma <= 16 ? 16 : BN;
-      const uint32_t tx = C::A_BYTES + C::AS_BYTES + (uint32_t)box_rows * 128u;
-      // Per-lane operands: lanes < NA weight codes, NA..2NA-1 their scale
-      // boxes (x in 16-byte steps), 2NA the token codes.
+      const uint32_t tx = C::A_BYTES + (uint32_t)box_rows * 128u;
+      // Per-lane operands: lanes < NA weight codes (GATED: gate, up rows),
+      // lane NA the token codes.
       const CUtensorMap* my_map = &args.tmA[(shared ? 2 : 0) + (lane % NA)];
       int my_row = a_row0;
       uint32_t my_off = (uint32_t)((lane % NA) * 64 * 128);
       uint64_t my_pol = pol_w;
-      bool scale_box = false;
-      if (lane >= NA && lane < 2 * NA) {
-        my_map = &args.tmAS[(shared ? 2 : 0) + (lane - NA)];
-        my_off = C::AS_OFF + (uint32_t)((lane - NA) * 64 * 16);
-        scale_box = true;
-      } else if (lane == 2 * NA) {
+      if (lane == NA) {
         my_map = &args.tmB[(shared ? 3 : 0) + bsel];
         my_row = b_row0;
         my_off = C::B_OFF;
@@ -795,9 +813,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
         const uint32_t dst = stages_base + (uint32_t)s * C::STAGE_BYTES;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
         __syncwarp();
-        if (lane < NLOADS)
-          tma_load_2d(dst + my_off, my_map, scale_box ? (kb >> 2) * 16 : kb * C::BK, my_row,
-                      full_bar(s), my_pol);
+        if (lane < NLOADS) tma_load_2d(dst + my_off, my_map, kb * C::BK, my_row, full_bar(s), my_pol);
       }
     }
     if (lane == 0) {
@@ -845,9 +861,10 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ scalers + epilogue
     // Warp w: TMEM lane quarter w % 4 (thread = weight row), blocks 2 bh and
-    // 2 bh + 1 of every stage (bh = (w - 2) / 4), all 32 token columns. Every
-    // decision to stop is taken from the shared abort flag after a barrier, so
-    // that all scaler warps pass the same barriers.
+    // 2 bh + 1 of every stage (bh = (w - 2) / 4), all token columns; the two
+    // halves' sums are added in shared memory. Every decision to stop is taken
+    // from the shared abort flag after a barrier, so that all scaler warps
+    // pass the same barriers.
     const int q = warp & 3;
     const int bh = (warp - 2) >> 2;
     const int r = q * 32 + lane;  // weight row of the unit = TMEM lane
@@ -868,20 +885,22 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
       named_barrier_sync(1, NT);
       if (*abort_flag) break;
       mbar_wait(bfull_bar(p), (lt >> 1) & 1u, nullptr, limit);  // completed: this thread's acquire
+      const uint8_t* apanel = panels + (size_t)p * panel_bytes;  // [BM][skb]
       {
-        const uint8_t* bp = bpanels + (size_t)p * BN * skb_max;
+        const uint8_t* bp = apanel + (size_t)C::BM * skb;       // [BN][skb]
         for (int e = et; e < nblk * BN; e += NT) {
           const int b = e / BN, n = e - b * BN;
           fpanel[e] = mx_scale_of(bp[n * skb + b]);
         }
       }
       named_barrier_sync(1, NT);
-      if (lane == 0) mbar_arrive(bempty_bar(p));
+      const uint8_t* srow = apanel + (size_t)r * skb;
+      uint4 sc4 = make_uint4(0, 0, 0, 0);
       float acc[BN];
 #pragma unroll
       for (int n = 0; n < BN; ++n) acc[n] = 0.0f;
       for (int kb = 0; kb < kdim / C::BK; ++kb, ++i) {
-        const int s = (int)(i % STAGES), g = (int)(i % C::NG);
+        const int g = (int)(i % C::NG);
         if (!warp_wait(pfull_bar(g), (i / C::NG) & 1u, args.status, limit)) {
           *abort_flag = 1;
           break;
@@ -892,10 +911,10 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(pempty_bar(g));
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(
-            stages + (size_t)s * C::STAGE_BYTES + C::AS_OFF + r * 16 + (kb & 3) * 4);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(s));
+        // The weight row's scale bytes of four stages per 16-byte read.
+        if ((kb & 3) == 0) sc4 = *reinterpret_cast<const uint4*>(srow + kb * 4);
+        const uint32_t sw = (kb & 3) == 0 ? sc4.x : (kb & 3) == 1 ? sc4.y : (kb & 3) == 2 ? sc4.z
+                                                                                       : sc4.w;
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int b = 2 * bh + bb;
@@ -904,15 +923,16 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
 #pragma unroll
           for (int n4 = 0; n4 < BN / 4; ++n4) {
             const float4 sb = fb[n4];
-            acc[4 * n4 + 0] = fmaf(P[bb * BN + 4 * n4 + 0] * sb.x, sa, acc[4 * n4 + 0]);
-            acc[4 * n4 + 1] = fmaf(P[bb * BN + 4 * n4 + 1] * sb.y, sa, acc[4 * n4 + 1]);
-            acc[4 * n4 + 2] = fmaf(P[bb * BN + 4 * n4 + 2] * sb.z, sa, acc[4 * n4 + 2]);
-            acc[4 * n4 + 3] = fmaf(P[bb * BN + 4 * n4 + 3] * sb.w, sa, acc[4 * n4 + 3]);
+            mul_fma2(acc[4 * n4 + 0], acc[4 * n4 + 1], P[bb * BN + 4 * n4 + 0],
+                     P[bb * BN + 4 * n4 + 1], sb.x, sb.y, sa);
+            mul_fma2(acc[4 * n4 + 2], acc[4 * n4 + 3], P[bb * BN + 4 * n4 + 2],
+                     P[bb * BN + 4 * n4 + 3], sb.z, sb.w, sa);
           }
         }
       }
       named_barrier_sync(1, NT);
       if (*abort_flag) break;
+      if (lane == 0) mbar_arrive(bempty_bar(p));  // this unit's scale panels are read
       // The two halves' partial sums, added in smem: epi[row][n].
       if (bh == 0) {
 #pragma unroll
@@ -1090,8 +1110,8 @@ cudaError_t launch_mx_dec_variant(const MxGemmArgs& a, int num_sms, size_t upper
   return launch_chained(fn, dim3((unsigned)grid), dim3(C::THREADS), smem, st, 1, a);
 }
 
-// The deepest ring of 22 KB stages (8, 6 or 4) that fits next to the token
-// scale panels of the problem.
+// The deepest ring of 20 KB stages (8, 6 or 4) that fits next to the scale
+// panels of the problem.
 template <bool GATED>
 cudaError_t launch_mx_dec(const MxGemmArgs& a, int num_sms, size_t ub, cudaStream_t st) {
   const int skb_max = a.skb_routed > a.skb_shared ? a.skb_routed : a.skb_shared;
@@ -1120,8 +1140,8 @@ cudaError_t launch_mx_dec_swiglu_gemm(const GemmProblem& p, const MxWeights& w,
   const uint64_t R = (uint64_t)p.E * p.I;
   bool ok = make_tma_map(&a.tmA[0], w.gate, MOE_DTYPE_E4M3, R, p.H, 64) &&
             make_tma_map(&a.tmA[1], w.up, MOE_DTYPE_E4M3, R, p.H, 64) &&
-            make_scale_map(&a.tmAS[0], w.s_gate, R, skH, 64, 16) &&
-            make_scale_map(&a.tmAS[1], w.s_up, R, skH, 64, 16) &&
+            make_scale_map(&a.tmS[0], w.s_gate, R, skH, 64) &&
+            make_scale_map(&a.tmS[1], w.s_up, R, skH, 64) &&
             make_b_maps(&a.tmB[0], x.routed, MOE_DTYPE_E4M3, (uint64_t)p.T * p.k, p.H, 32, 16) &&
             make_b_maps(&a.tmB[3], x.shared, MOE_DTYPE_E4M3, p.T, p.H, 32, 16) &&
             make_scale_map(&a.tmSB[0], x.routed_scales, (uint64_t)p.T * p.k, skH, 32) &&
@@ -1129,14 +1149,14 @@ cudaError_t launch_mx_dec_swiglu_gemm(const GemmProblem& p, const MxWeights& w,
   if (ok && has_s)
     ok = make_tma_map(&a.tmA[2], w.sh_gate, MOE_DTYPE_E4M3, p.Is, p.H, 64) &&
          make_tma_map(&a.tmA[3], w.sh_up, MOE_DTYPE_E4M3, p.Is, p.H, 64) &&
-         make_scale_map(&a.tmAS[2], w.sh_s_gate, p.Is, skH, 64, 16) &&
-         make_scale_map(&a.tmAS[3], w.sh_s_up, p.Is, skH, 64, 16);
+         make_scale_map(&a.tmS[2], w.sh_s_gate, p.Is, skH, 64) &&
+         make_scale_map(&a.tmS[3], w.sh_s_up, p.Is, skH, 64);
   if (!ok) return cudaErrorInvalidValue;
   if (!has_s) {
     a.tmA[2] = a.tmA[0];
     a.tmA[3] = a.tmA[1];
-    a.tmAS[2] = a.tmAS[0];
-    a.tmAS[3] = a.tmAS[1];
+    a.tmS[2] = a.tmS[0];
+    a.tmS[3] = a.tmS[1];
   }
   fill_mx_common(a, p, offsets, gather_idx, status, 32);
   a.out = h.routed;
@@ -1168,25 +1188,25 @@ cudaError_t launch_mx_dec_down_gemm(const GemmProblem& p, const MxWeights& w,
   memset(&a, 0, sizeof(a));
   const uint64_t R = (uint64_t)p.E * p.H;
   bool ok = make_tma_map(&a.tmA[0], w.down, MOE_DTYPE_E4M3, R, p.I, 128) &&
-            make_scale_map(&a.tmAS[0], w.s_down, R, skI, 128, 16) &&
+            make_scale_map(&a.tmS[0], w.s_down, R, skI, 128) &&
             make_b_maps(&a.tmB[0], h.routed, MOE_DTYPE_E4M3, (uint64_t)p.T * p.k, p.I, 32, 16) &&
             make_scale_map(&a.tmSB[0], h.routed_scales, (uint64_t)p.T * p.k, skI, 32);
   if (ok && has_s)
     ok = make_tma_map(&a.tmA[2], w.sh_down, MOE_DTYPE_E4M3, p.H, p.Is, 128) &&
-         make_scale_map(&a.tmAS[2], w.sh_s_down, p.H, skIs, 128, 16) &&
+         make_scale_map(&a.tmS[2], w.sh_s_down, p.H, skIs, 128) &&
          make_b_maps(&a.tmB[3], h.shared, MOE_DTYPE_E4M3, p.T, p.Is, 32, 16) &&
          make_scale_map(&a.tmSB[1], h.shared_scales, p.T, skIs, 32);
   if (!ok) return cudaErrorInvalidValue;
   if (!has_s) {
     a.tmA[2] = a.tmA[0];
-    a.tmAS[2] = a.tmAS[0];
+    a.tmS[2] = a.tmS[0];
     for (int i = 0; i < 3; ++i) a.tmB[3 + i] = a.tmB[i];
     a.tmSB[1] = a.tmSB[0];
   }
   a.tmA[1] = a.tmA[0];
   a.tmA[3] = a.tmA[2];
-  a.tmAS[1] = a.tmAS[0];
-  a.tmAS[3] = a.tmAS[2];
+  a.tmS[1] = a.tmS[0];
+  a.tmS[3] = a.tmS[2];
   fill_mx_common(a, p, offsets, gather_idx, status, 32);
   a.topk_w = topk_w;
   a.out = Y;
