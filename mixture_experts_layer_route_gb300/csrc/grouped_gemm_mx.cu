@@ -185,6 +185,29 @@ __device__ __forceinline__ void mul_fma2(float& a0, float& a1, float p0, float p
       : "f"(p0), "f"(p1), "f"(s0), "f"(s1), "f"(sa));
 }
 
+// acc[n] += P_b[n] * s_B[n][b] * s_A[b] over this warp's two blocks b = 2 bh,
+// 2 bh + 1 and the tile's NC columns (P: the two partials, NC columns each;
+// fkb: the stage's token scales as floats, [4 blocks][32]; sw: the weight
+// row's four scale bytes of the stage).
+template <int NC>
+__device__ __forceinline__ void scale_blocks(const float (&P)[2 * NC], float (&acc)[32],
+                                             uint32_t sw, int bh, const float* fkb) {
+#pragma unroll
+  for (int bb = 0; bb < 2; ++bb) {
+    const int b = 2 * bh + bb;
+    const float sa = mx_scale_of((sw >> (8 * b)) & 0xFFu);
+    const float4* fb = reinterpret_cast<const float4*>(fkb + b * 32);
+#pragma unroll
+    for (int n4 = 0; n4 < NC / 4; ++n4) {
+      const float4 sb = fb[n4];
+      mul_fma2(acc[4 * n4 + 0], acc[4 * n4 + 1], P[bb * NC + 4 * n4 + 0], P[bb * NC + 4 * n4 + 1],
+               sb.x, sb.y, sa);
+      mul_fma2(acc[4 * n4 + 2], acc[4 * n4 + 3], P[bb * NC + 4 * n4 + 2], P[bb * NC + 4 * n4 + 3],
+               sb.z, sb.w, sa);
+    }
+  }
+}
+
 // All lanes wait (each thread's own acquire of the phase); the warp agrees on
 // the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status,
@@ -835,6 +858,8 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
         const int kdim = (tl.g == E) ? args.kdim_shared : args.kdim_routed;
         const int n_mma = (tl.n_valid + 15) / 16 * 16;
         const uint32_t idesc = umma_idesc(UmmaOf<uint8_t>::fmt, C::BM, (uint32_t)n_mma);
+        // Partial slot of block b in group g: column g * 4 BN + b * n_mma (a
+        // 16-column tile packs its four partials into half of the group).
         for (int kb = 0; kb < kdim / C::BK; ++kb, ++i) {
           const int s = (int)(i % STAGES), g = (int)(i % C::NG);
           if (!mbar_wait(full_bar(s), (i / STAGES) & 1u, args.status, limit) ||
@@ -847,7 +872,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
           const uint32_t b_addr = a_addr + C::B_OFF;
 #pragma unroll
           for (int b = 0; b < 4; ++b)
-            umma_issue<kKindF8>(tmem_base + (uint32_t)((g * 4 + b) * BN),
+            umma_issue<kKindF8>(tmem_base + (uint32_t)(g * 4 * BN + b * n_mma),
                                 umma_desc_sw128(a_addr + b * 32), umma_desc_sw128(b_addr + b * 32),
                                 idesc, 0u);
           umma_commit(empty_bar(s));
@@ -870,7 +895,7 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
     const int r = q * 32 + lane;  // weight row of the unit = TMEM lane
     const int et = threadIdx.x - 64;  // 0..255
     constexpr int NT = 32 * C::SCALER_WARPS;
-    const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(bh * 2 * BN);
+    const uint32_t t_quarter = tmem_base + ((uint32_t)(q * 32) << 16);
     uint32_t lt = 0, i = 0;
     for (int u = cid; u < total; u += ncl, ++lt) {
       const Tile tl = tile_of(u);
@@ -896,6 +921,10 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
       named_barrier_sync(1, NT);
       const uint8_t* srow = apanel + (size_t)r * skb;
       uint4 sc4 = make_uint4(0, 0, 0, 0);
+      // Tiles of at most 16 tokens (the usual decode tile) have 16-column
+      // partials: half the tensor-memory reads and multiply-adds.
+      const bool n16 = tl.n_valid <= 16;
+      const uint32_t t_lane = t_quarter + (uint32_t)(bh * 2 * (n16 ? 16 : BN));
       float acc[BN];
 #pragma unroll
       for (int n = 0; n < BN; ++n) acc[n] = 0.0f;
@@ -906,28 +935,25 @@ __global__ void __launch_bounds__(MxDecCfg<GATED, STAGES>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        float P[2 * BN];
-        tmem_ld64(t_lane + (uint32_t)(g * 4 * BN), P);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pempty_bar(g));
         // The weight row's scale bytes of four stages per 16-byte read.
         if ((kb & 3) == 0) sc4 = *reinterpret_cast<const uint4*>(srow + kb * 4);
         const uint32_t sw = (kb & 3) == 0 ? sc4.x : (kb & 3) == 1 ? sc4.y : (kb & 3) == 2 ? sc4.z
                                                                                        : sc4.w;
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = 2 * bh + bb;
-          const float sa = mx_scale_of((sw >> (8 * b)) & 0xFFu);
-          const float4* fb = reinterpret_cast<const float4*>(fpanel + (size_t)(kb * 4 + b) * BN);
-#pragma unroll
-          for (int n4 = 0; n4 < BN / 4; ++n4) {
-            const float4 sb = fb[n4];
-            mul_fma2(acc[4 * n4 + 0], acc[4 * n4 + 1], P[bb * BN + 4 * n4 + 0],
-                     P[bb * BN + 4 * n4 + 1], sb.x, sb.y, sa);
-            mul_fma2(acc[4 * n4 + 2], acc[4 * n4 + 3], P[bb * BN + 4 * n4 + 2],
-                     P[bb * BN + 4 * n4 + 3], sb.z, sb.w, sa);
-          }
+        const uint32_t ta = t_lane + (uint32_t)(g * 4 * BN);
+        if (n16) {
+          float P[32];
+          tmem_ld32(ta, P);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pempty_bar(g));
+          scale_blocks<16>(P, acc, sw, bh, fpanel + (size_t)kb * 4 * BN);
+        } else {
+          float P[64];
+          tmem_ld64(ta, P);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pempty_bar(g));
+          scale_blocks<32>(P, acc, sw, bh, fpanel + (size_t)kb * 4 * BN);
         }
       }
       named_barrier_sync(1, NT);
