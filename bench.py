@@ -585,8 +585,9 @@ def measure_quantized(cfg, args, world, peaks, mx=False):
     t_roof_sus = max(t_mem, flop_layer / (ratio * 1e12 * peaks["bf16_tflops_sustained"]) * 1e3)
     weights = ("MXFP8: E4M3 codes, one E8M0 scale per 32 elements (moe_forward_mx)" if mx else
                "E4M3, one power-of-two scale per row (moe_forward_fp8)")
-    peak_src = ("measured bf16_tflops (burst): the MXFP8 GEMMs run the bf16 MMA" if mx else
-                "2 x measured bf16_tflops (burst; nominal fp8/bf16 ratio)")
+    peak_src = ("measured bf16_tflops (burst): the MXFP8 GEMMs of batches over 64 tokens run "
+                "the bf16 MMA on converted tiles (decode-sized ones the E4M3 MMA, HBM-bound)"
+                if mx else "2 x measured bf16_tflops (burst; nominal fp8/bf16 ratio)")
     return {"value": world * T * steps / (ms_total / 1e3), "unit": "tokens/s",
             "ms_per_step": ms_step, "median_ms": statistics.median(per),
             "weights": weights,
