@@ -1077,18 +1077,12 @@ cudaError_t launch_mx_variant(const MxGemmArgs& a, int num_sms, size_t upper_uni
   return launch_chained(fn, dim3((unsigned)grid), dim3(C::THREADS), smem, st, 1, a);
 }
 
-// Decode-sized batches: 32-token tiles, 6 stages (4 if the scale panels of a
-// wide K or many experts leave no room); otherwise 128-token tiles, 3 stages
-// (2 likewise).
+// 128-token tiles, 3 stages (2 if the scale panels of a wide K or many
+// experts leave no room). Decode-sized batches run mx_dec_kernel instead.
 template <bool GATED>
-cudaError_t launch_mx(const MxGemmArgs& a, bool dec, int num_sms, size_t ub, cudaStream_t st) {
+cudaError_t launch_mx(const MxGemmArgs& a, int num_sms, size_t ub, cudaStream_t st) {
   const int sk_max = a.sk_routed > a.sk_shared ? a.sk_routed : a.sk_shared;
   const size_t optin = (size_t)smem_optin();
-  if (dec) {
-    if (MxCfg<GATED, 32, 6>::smem_bytes(a.E, sk_max) <= optin)
-      return launch_mx_variant<GATED, 32, 6>(a, num_sms, ub, st);
-    return launch_mx_variant<GATED, 32, 4>(a, num_sms, ub, st);
-  }
   if (MxCfg<GATED, 128, 3>::smem_bytes(a.E, sk_max) <= optin)
     return launch_mx_variant<GATED, 128, 3>(a, num_sms, ub, st);
   return launch_mx_variant<GATED, 128, 2>(a, num_sms, ub, st);
@@ -1265,8 +1259,8 @@ cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, cons
                                   const int32_t* gather_idx, void* h, void* hs, int* status,
                                   cudaStream_t st) {
   const bool has_s = p.Is > 0;
-  const bool dec = mx_decode_tiles(p);
-  const int bn = dec ? 32 : 128;
+  if (mx_decode_tiles(p)) return cudaErrorInvalidValue;  // the decode kernels' problems
+  const int bn = 128;
   const uint32_t b1 = bn / 2 < 16 ? 16 : bn / 2;
   const int skH = mx_scale_cols(p.H);
   MxGemmArgs a;
@@ -1302,15 +1296,15 @@ cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, cons
   a.ld_out_routed = p.I;
   a.ld_out_shared = has_s ? p.Is : 0;
   const size_t ub = unit_upper_bound(p.T, p.k, p.E, bn, p.I / 64, has_s ? p.Is / 64 : 0);
-  return launch_mx<true>(a, dec, p.num_sms, ub, st);
+  return launch_mx<true>(a, p.num_sms, ub, st);
 }
 
 cudaError_t launch_mx_down_gemm(const GemmProblem& p, const MxWeights& w, const void* h,
                                 const void* hs, const int32_t* offsets, const int32_t* gather_idx,
                                 const float* topk_w, float* Y, int* status, cudaStream_t st) {
   const bool has_s = p.Is > 0;
-  const bool dec = mx_decode_tiles(p);
-  const int bn = dec ? 32 : 128;
+  if (mx_decode_tiles(p)) return cudaErrorInvalidValue;  // the decode kernels' problems
+  const int bn = 128;
   const uint32_t b1 = bn / 2 < 16 ? 16 : bn / 2;
   const int skI = mx_scale_cols(p.I);
   const int skIs = has_s ? mx_scale_cols(p.Is) : skI;
@@ -1346,7 +1340,7 @@ cudaError_t launch_mx_down_gemm(const GemmProblem& p, const MxWeights& w, const 
   a.ld_out_routed = p.H;
   a.ld_out_shared = p.H;
   const size_t ub = unit_upper_bound(p.T, p.k, p.E, bn, p.H / 128, has_s ? p.H / 128 : 0);
-  return launch_mx<false>(a, dec, p.num_sms, ub, st);
+  return launch_mx<false>(a, p.num_sms, ub, st);
 }
 
 }  // namespace moe

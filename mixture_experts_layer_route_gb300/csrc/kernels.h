@@ -154,8 +154,10 @@ struct MxWeights {
 };
 // True when both MXFP8 GEMMs of the problem fit the device's shared memory.
 bool mx_problem_fits(const GemmProblem& p);
-// xq: the quantized token rows [T][H] (bf16 values); xg: their expert-ordered
-// copy [T*k][H]; h, hs bf16 outputs holding MXFP8 values.
+// Batches beyond the decode size (128-token tiles; decode-sized problems are
+// refused here and run launch_mx_dec_*): xq: the quantized token rows [T][H]
+// (bf16 values); xg: their expert-ordered copy [T*k][H]; h, hs bf16 outputs
+// holding MXFP8 values.
 cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, const void* xq,
                                   const void* xg, const int32_t* offsets,
                                   const int32_t* gather_idx, void* h, void* hs, int* status,
