@@ -145,6 +145,13 @@ cudaError_t launch_quantize_mx(int dtype, const void* src, int64_t rows, int64_t
                                uint8_t* q, uint8_t* scales, int num_sms, cudaStream_t st);
 cudaError_t launch_qdq_mx(const void* src, int64_t rows, int64_t cols, void* out, int num_sms,
                           cudaStream_t st);
+// The decode-sized MXFP8 layer's token operand: bf16 x [T][H] -> codes and scale
+// rows of every routed slot at its position (xgq [T*k][H], xgs [T*k][sk]), and
+// in token order (xq, xs; skipped when null). A position beyond T*k sets
+// MOE_ERR_DEVICE_CHECK in *status and is skipped.
+cudaError_t launch_quantize_dispatch_mx(const void* x, const int32_t* slot_pos, int T, int k,
+                                       int H, uint8_t* xgq, uint8_t* xgs, uint8_t* xq, uint8_t* xs,
+                                       int* status, int num_sms, cudaStream_t st);
 
 // MXFP8 grouped GEMMs (grouped_gemm_mx.cu). Weight codes [rows][K] with
 // their scale rows; the shared expert's (sh_*) are null without one.

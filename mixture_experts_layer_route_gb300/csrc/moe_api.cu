@@ -737,9 +737,9 @@ moe_status moe_forward_mx(const moe_problem* pb, const void* x, const void* W_ro
                        at<int32_t>(workspace, L.pscratch), st);
   }
   if (L.mx_dec) {
-    // Decode-sized batches: token rows to MXFP8 codes and scale rows, their
-    // expert-ordered copies, then the E4M3-MMA GEMMs (h as codes and scales).
-    const size_t skH = (size_t)moe_mx_scale_cols(g.H);
+    // Decode-sized batches: token rows to MXFP8 codes and scale rows, written
+    // in expert order (and token order for a shared expert), then the E4M3-MMA
+    // GEMMs (h as codes and scales).
     uint8_t* xq = at<uint8_t>(workspace, L.xq);
     uint8_t* xs = at<uint8_t>(workspace, L.xs);
     uint8_t* xgq = at<uint8_t>(workspace, L.xg);
@@ -750,14 +750,9 @@ moe_status moe_forward_mx(const moe_problem* pb, const void* x, const void* W_ro
                          has_s ? at<uint8_t>(workspace, L.hss) : nullptr};
     const MxDecTokens ht = {ho.routed, ho.routed_scales, ho.shared, ho.shared_scales};
     if (e == cudaSuccess) {
-      NvtxRange r("quantize_x");
-      e = launch_quantize_mx(MOE_DTYPE_BF16, x, g.T, g.H, xq, xs, g.num_sms, st);
-    }
-    if (e == cudaSuccess) {
-      NvtxRange r("dispatch_copy");
-      e = launch_gather_rows(xq, spos, g.T * g.k, g.k, (size_t)g.H, xgq, status, g.num_sms, st);
-      if (e == cudaSuccess)
-        e = launch_gather_rows(xs, spos, g.T * g.k, g.k, skH, xgs, status, g.num_sms, st);
+      NvtxRange r("quantize_dispatch_x");
+      e = launch_quantize_dispatch_mx(x, spos, g.T, g.k, g.H, xgq, xgs, has_s ? xq : nullptr,
+                                      has_s ? xs : nullptr, status, g.num_sms, st);
     }
     if (e == cudaSuccess) {
       NvtxRange r("gate_up_gemm");

@@ -99,6 +99,61 @@ __global__ void __launch_bounds__(256) quantize_mx_kernel(const TIn* __restrict_
   }
 }
 
+// The MXFP8 decode-sized layer's token operand in one pass: warp = routed
+// slot s (token s / k), lane = one block of 32 elements per step. The slot's
+// codes and scale row go to row slot_pos[s] of xgq / xgs (the expert-ordered
+// copy the GEMMs read as tiles); the token's first slot also writes row t of
+// xq / xs (token order, for the shared expert) when those are given. A
+// position beyond T*k sets MOE_ERR_DEVICE_CHECK and the slot is skipped.
+__global__ void __launch_bounds__(256) quantize_dispatch_mx_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ slot_pos, int T, int k,
+    int H, int sk, uint8_t* __restrict__ xgq, uint8_t* __restrict__ xgs, uint8_t* __restrict__ xq,
+    uint8_t* __restrict__ xs, int* status) {
+  pdl_entry();
+  const int lane = threadIdx.x & 31;
+  const int P = T * k;
+  const int nb = H / 32;
+  const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t s = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < P; s += warps) {
+    const int p = slot_pos[s];
+    if ((unsigned)p >= (unsigned)P) {
+      if (lane == 0) set_status(status, MOE_ERR_DEVICE_CHECK);
+      continue;
+    }
+    const int t = (int)(s / k);
+    const bool token_row = xq != nullptr && s - (int64_t)t * k == 0;
+    for (int b = lane; b < sk; b += 32) {
+      if (b >= nb) {  // the scale row's padding
+        xgs[(size_t)p * sk + b] = 0;
+        if (token_row) xs[(size_t)t * sk + b] = 0;
+        continue;
+      }
+      float v[32];
+      load32(x + (size_t)t * H + (size_t)b * 32, v);
+      float amax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      const int e = mx_block_exponent(amax);
+      const float inv = mx_pow2(-e);
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        w[j] = mx_encode4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv,
+                          v[4 * j + 3] * inv);
+      uint4* dst = reinterpret_cast<uint4*>(xgq + (size_t)p * H + (size_t)b * 32);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      xgs[(size_t)p * sk + b] = (uint8_t)(e + 127);
+      if (token_row) {
+        uint4* dt = reinterpret_cast<uint4*>(xq + (size_t)t * H + (size_t)b * 32);
+        dt[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dt[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        xs[(size_t)t * sk + b] = (uint8_t)(e + 127);
+      }
+    }
+  }
+}
+
 unsigned grid_for(int64_t n, int num_sms) {
   int64_t blocks = (n + 255) / 256;
   if (blocks > 16 * (int64_t)num_sms) blocks = 16 * (int64_t)num_sms;
@@ -119,6 +174,18 @@ cudaError_t launch_quantize_mx(int dtype, const void* src, int64_t rows, int64_t
   return launch_chained(quantize_mx_kernel<float, false>, dim3(g), dim3(256), 0, st, 1,
                         (const float*)src, rows, (int)cols, sk, q, scales,
                         (__nv_bfloat16*)nullptr);
+}
+
+cudaError_t launch_quantize_dispatch_mx(const void* x, const int32_t* slot_pos, int T, int k,
+                                       int H, uint8_t* xgq, uint8_t* xgs, uint8_t* xq, uint8_t* xs,
+                                       int* status, int num_sms, cudaStream_t st) {
+  const int P = T * k;
+  if (P == 0) return cudaSuccess;
+  int64_t blocks = ((int64_t)P + 7) / 8;
+  if (blocks > 16 * (int64_t)num_sms) blocks = 16 * (int64_t)num_sms;
+  return launch_chained(quantize_dispatch_mx_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                        (const __nv_bfloat16*)x, slot_pos, T, k, H, mx_scale_cols(H), xgq, xgs,
+                        xq, xs, status);
 }
 
 cudaError_t launch_qdq_mx(const void* src, int64_t rows, int64_t cols, void* out, int num_sms,
