@@ -58,6 +58,24 @@ bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
+// 2-D uint8 matrix [rows][cols] (E4M3 codes) with boxes of 64 bytes of columns
+// x box_rows rows, 64-byte swizzle (16-byte chunk c of a box row r lands at
+// chunk position c ^ ((r >> 1) & 3)).
+bool make_code_map64(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows) {
+  auto enc = encoder();
+  if (!enc || cols % 16 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D uint8 matrix [rows][cols] (cols a multiple of 16) whose box is box_cols
 // bytes (whole rows when 0; a multiple of 16, at most 256) x box_rows rows, no
 // swizzle. The MX scale rows.

@@ -14,20 +14,24 @@
 // order of the fp32 sums.
 //
 // Problem and schedule as grouped_gemm.cuh (the same unit list and deal); the
-// differences are in the pipeline of one CTA (no CTA pairs):
-//   warp 0, producer: per stage (K = 128) the 128 weight rows' codes (one
-//     128-byte box per 64 rows, 128-byte swizzle) and the token tile's two
-//     64-element halves (bf16, one box each); per unit the scale panel of its
-//     weight rows (all K / 32 scale bytes of each row, one box per 64 or 128
-//     rows) into one of two panel buffers.
+// differences are in the pipeline of one CTA (no CTA pairs). Two tile shapes,
+// chosen per problem: when the experts average 256 routed rows or more,
+// 256-token tiles with K = 64 per stage (each converted weight tile serves
+// twice the tokens); otherwise 128-token tiles with K = 128 per stage.
+//   warp 0, producer: per stage the 128 weight rows' codes (one BK-byte box
+//     per 64 or 128 rows; 64-byte swizzle for K = 64, 128-byte for K = 128)
+//     and the token tile (boxes of BN tokens x 64 bf16 elements); per unit
+//     the scale panel of its weight rows (all K / 32 scale bytes of each row,
+//     one box per 64 or 128 rows) into one of two panel buffers.
 //   warps 6-9, converters (one per TMEM lane quarter, thread = weight row):
-//     per stage, the row's 128 codes times their block scales -> 64 bf16
-//     pairs, stored into one of four 64-column slots of tensor memory (the
-//     MMA reads operand A from there: row m in lane m, column c holding
-//     elements 2c and 2c + 1); each slot is handed back by the MMA's commit.
-//   warp 1, MMA issuer: 8 MMAs of K = 16 per stage, A from tensor memory, B
-//     from the stage's token halves (K-major, 128-byte swizzle), into one of
-//     two accumulators.
+//     per stage, the row's codes times their block scales -> bf16 pairs,
+//     stored into a ring of converted slots of tensor memory (256 columns:
+//     eight of 32 or four of 64; the MMA reads operand A from there: row m in
+//     lane m, column c holding elements 2c and 2c + 1); each slot is handed
+//     back by the MMA's commit.
+//   warp 1, MMA issuer: BK / 16 MMAs of K = 16 per stage, A from tensor
+//     memory, B from the stage's token tile (K-major, 128-byte swizzle), into
+//     the accumulator (two of 128 columns, or one of 256 beside the slots).
 //   warps 2-5, epilogue: GATED, silu(gate) * up, then each h row quantized per
 //     block of 32 features (the two threads holding a block's 16 + 16 values
 //     share their maximum) and stored as its bf16 values; DOWN, as the bf16
@@ -42,7 +46,8 @@ namespace moe {
 struct MxGemmArgs {
   // E4M3 weight codes, rows of K bytes. GATED: [0] routed gate, [1] routed up,
   // [2] shared gate, [3] shared up (64-row boxes); DOWN: [0] routed down, [2]
-  // shared down (128-row boxes). 128-byte boxes, 128-byte swizzle.
+  // shared down (128-row boxes). Boxes of BK bytes: 64 (64-byte swizzle) or
+  // 128 (128-byte swizzle).
   CUtensorMap tmA[4];
   // The E8M0 scale rows of the same weights (sk bytes per row), indexed like
   // tmA; a box holds whole rows (sk bytes) of 64 or 128 rows, no swizzle.
@@ -79,24 +84,32 @@ struct MxGemmArgs {
 
 namespace {
 
-template <bool GATED, int BN, int STAGES>
+template <bool GATED, int BN, int STAGES, int BK_ = 128>
 struct MxCfg {
   static constexpr int BM = 128;                 // weight rows per unit (MMA M)
   static constexpr int WM = GATED ? 64 : 128;    // output features per unit
-  static constexpr int BK = 128;                 // K per stage
-  static constexpr int A8_BYTES = BM * 128;      // codes of one stage
-  static constexpr int B_HALF = BN * 128;        // one 64-element half of the token tile
-  static constexpr int STAGE_BYTES = A8_BYTES + 2 * B_HALF;
-  static constexpr int SA = 4;                   // converted-A slots in tensor memory
-  static constexpr int ACC_COLS = 2 * BN;        // two fp32 accumulators
+  static constexpr int BK = BK_;                 // K per stage: 128 or 64
+  static constexpr int A8_BYTES = BM * BK;       // codes of one stage (BK-byte rows)
+  static constexpr int NBH = BK / 64;            // token boxes per stage (64 bf16 elements each)
+  static constexpr int B_HALF = BN * 128;
+  static constexpr int STAGE_BYTES = A8_BYTES + NBH * B_HALF;
+  static constexpr int SLOT_COLS = BK / 2;       // a converted stage in tensor memory
+  static constexpr int SA = 256 / SLOT_COLS;     // converted-A slots (256 columns in all)
+  // Two fp32 accumulators when they fit beside the converted slots, else one
+  // (256-token tiles: the epilogue then overlaps only the next unit's loads
+  // and conversion, not its MMAs).
+  static constexpr int NACC = 2 * BN + SA * SLOT_COLS <= 512 ? 2 : 1;
+  static constexpr int ACC_COLS = NACC * BN;
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
   static constexpr int THREADS = 320;            // producer, MMA, 4 epilogue, 4 converter warps
   static constexpr int BOX1 = BN / 2 < 16 ? 16 : BN / 2;
   // full, empty [STAGES]; cfull, cempty [SA]; pfull, pempty, tfull, tempty [2]; drain
   static constexpr int NBARS = 2 * STAGES + 2 * SA + 9;
-  static_assert(ACC_COLS + SA * 64 <= TMEM_COLS, "tensor memory");
-  static_assert(BN % 32 == 0 && BN <= 128, "token tile");
+  static_assert(ACC_COLS + SA * SLOT_COLS <= TMEM_COLS, "tensor memory");
+  static_assert(BK == 64 || BK == 128, "stage depth");
+  static_assert(BN % 32 == 0 && BN <= 256, "token tile");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 
   static size_t smem_bytes(int E, int sk_max) {
     return 1024 + (size_t)STAGES * STAGE_BYTES + 2 * (size_t)BM * sk_max + EPI_FLOATS * 4 +
@@ -216,10 +229,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* st
   return __all_sync(0xffffffffu, ok);
 }
 
-template <bool GATED, int BN, int STAGES>
-__global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__ MxGemmArgs args) {
+template <bool GATED, int BN, int STAGES, int BK>
+__global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
+    mx_gemm_kernel(const __grid_constant__ MxGemmArgs args) {
   pdl_trigger();
-  using C = MxCfg<GATED, BN, STAGES>;
+  using C = MxCfg<GATED, BN, STAGES, BK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -310,7 +324,7 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
     bool ok = true;
     uint32_t lt = 0;
     constexpr int NA = GATED ? 2 : 1;
-    constexpr int NLOADS = NA + 2;
+    constexpr int NLOADS = NA + C::NBH;
     for (int u = cid; u < total && ok; u += ncl, ++lt) {
       const Tile tl = tile_of(u);
       const bool shared = tl.g == E;
@@ -336,17 +350,18 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
       const int n_mma = (tl.n_valid + 15) / 16 * 16;
       const int bsel = n_mma <= 16 ? 2 : (n_mma <= C::BOX1 ? 1 : 0);
       const int box_rows = bsel == 2 ? 16 : (bsel == 1 ? C::BOX1 : BN);
-      const uint32_t tx = C::A8_BYTES + 2u * (uint32_t)box_rows * 128u;
+      const uint32_t tx = C::A8_BYTES + (uint32_t)(C::NBH * box_rows * 128);
       const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
-      // Per-lane operands: lanes < NA weight codes (GATED: gate, up rows),
-      // then the token tile's two K halves.
+      // Per-lane operands: lanes < NA weight codes (GATED: gate, up rows; one
+      // BK-byte box of 64 or 128 rows each), then the token tile's NBH boxes
+      // of 64 elements.
       const CUtensorMap* my_map = &args.tmA[shared ? 2 : 0];
       int my_row = a_row0, my_dx = 0;
       uint32_t my_off = 0;
       uint64_t my_pol = pol_w;
       if (GATED && lane == 1) {
         my_map = &args.tmA[shared ? 3 : 1];
-        my_off = 64 * 128;
+        my_off = 64 * C::BK;
       }
       if (lane >= NA && lane < NLOADS) {
         const int h = lane - NA;
@@ -375,7 +390,7 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
         const uint32_t dst = stages_base + (uint32_t)s * C::STAGE_BYTES;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
         __syncwarp();
-        // Codes: x in bytes; token halves: x in bf16 elements.
+        // Codes: x in bytes; tokens: x in bf16 elements.
         if (lane < NLOADS)
           tma_load_2d(dst + my_off, my_map, kb * C::BK + my_dx, my_row, full_bar(s), my_pol);
       }
@@ -399,7 +414,7 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
       for (int u = cid; u < total && ok; u += ncl, ++lt) {
         const Tile tl = tile_of(u);
         const int kdim = (tl.g == E) ? args.kdim_shared : args.kdim_routed;
-        const uint32_t acc = lt & 1u, around = lt >> 1;
+        const uint32_t acc = lt % C::NACC, around = lt / C::NACC;
         if (!mbar_wait(tempty_bar((int)acc), (around & 1u) ^ 1u, args.status, limit)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -421,15 +436,13 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
             cph ^= 1u;
           }
           tc_fence_after();
-          const uint32_t a_t = tmem_base + C::ACC_COLS + (uint32_t)c * 64u;
+          const uint32_t a_t = tmem_base + C::ACC_COLS + (uint32_t)(c * C::SLOT_COLS);
           const uint32_t b_addr = stages_base + (uint32_t)s * C::STAGE_BYTES + C::A8_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bd =
-                umma_desc_sw128(b_addr + (uint32_t)((kk >> 2) * C::B_HALF + (kk & 3) * 32));
-            umma_issue_tmem_a(d_tmem, a_t + (uint32_t)kk * 8u, bd, idesc,
-                              (kb | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < C::BK / 16; ++kk)
+            umma_issue_tmem_a(d_tmem, a_t + (uint32_t)kk * 8u,
+                              umma_desc_sw128(b_addr + (kk >> 2) * C::B_HALF + (kk & 3) * 32),
+                              idesc, (kb | kk) != 0 ? 1u : 0u);
           umma_commit(empty_bar(s));
           umma_commit(cempty_bar(c));
         }
@@ -472,22 +485,27 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
           cph ^= 1u;
         }
         tc_fence_after();
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(srow + kb * 4);
-        const uint8_t* arow = stages + (size_t)s * C::STAGE_BYTES + (size_t)r * 128;
+        // BK / 32 scale bytes per stage (blocks BK / 32 * kb ..).
+        const uint32_t sw = C::BK == 128 ? *reinterpret_cast<const uint32_t*>(srow + kb * 4)
+                                         : *reinterpret_cast<const uint16_t*>(srow + kb * 2);
+        // BK-byte rows: 128-byte swizzle (chunk j of row r at j ^ (r & 7)) or
+        // 64-byte swizzle (at j ^ ((r >> 1) & 3)).
+        const uint8_t* arow = stages + (size_t)s * C::STAGE_BYTES + (size_t)r * C::BK;
+        const int rsw = C::BK == 128 ? (r & 7) : ((r >> 1) & 3);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < C::NBH; ++h) {
           uint32_t o[32];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
-            const int j = 4 * h + jj;  // 16-byte chunk of the 128-byte row
-            const uint4 ch = *reinterpret_cast<const uint4*>(arow + ((j ^ (r & 7)) << 4));
+            const int j = 4 * h + jj;  // 16-byte chunk of the row
+            const uint4 ch = *reinterpret_cast<const uint4*>(arow + ((j ^ rsw) << 4));
             const float X = mx_scale_of((sw >> (8 * (j >> 1))) & 0xFFu);
             mx_decode4_bf16(ch.x, X, o[8 * jj + 0], o[8 * jj + 1]);
             mx_decode4_bf16(ch.y, X, o[8 * jj + 2], o[8 * jj + 3]);
             mx_decode4_bf16(ch.z, X, o[8 * jj + 4], o[8 * jj + 5]);
             mx_decode4_bf16(ch.w, X, o[8 * jj + 6], o[8 * jj + 7]);
           }
-          tmem_st32(tmem_base + lane_field + C::ACC_COLS + (uint32_t)c * 64u + (uint32_t)h * 32u,
+          tmem_st32(tmem_base + lane_field + C::ACC_COLS + (uint32_t)(c * C::SLOT_COLS + h * 32),
                     o);
         }
         tmem_wait_st();
@@ -508,7 +526,7 @@ __global__ void __launch_bounds__(320, 1) mx_gemm_kernel(const __grid_constant__
     for (int u = cid; u < total; u += ncl, ++lt) {
       Tile tl = tile_of(u);
       const bool shared = tl.g == E;
-      const uint32_t acc = lt & 1u, around = lt >> 1;
+      const uint32_t acc = lt % C::NACC, around = lt / C::NACC;
       if (et == 0)
         *epi_flag = mbar_wait(tfull_bar((int)acc), around & 1u, args.status, limit) ? 1 : 0;
       if constexpr (!GATED) {
@@ -1060,15 +1078,15 @@ int smem_optin() {
   return cache[dev];
 }
 
-template <bool GATED, int BN, int STAGES>
+template <bool GATED, int BN, int STAGES, int BK>
 cudaError_t launch_mx_variant(const MxGemmArgs& a, int num_sms, size_t upper_units,
                               cudaStream_t st) {
-  using C = MxCfg<GATED, BN, STAGES>;
+  using C = MxCfg<GATED, BN, STAGES, BK>;
   const int sk_max = a.sk_routed > a.sk_shared ? a.sk_routed : a.sk_shared;
   const size_t smem = C::smem_bytes(a.E, sk_max);
   const int optin = smem_optin();
   if (smem > (size_t)optin) return cudaErrorInvalidValue;
-  auto fn = mx_gemm_kernel<GATED, BN, STAGES>;
+  auto fn = mx_gemm_kernel<GATED, BN, STAGES, BK>;
   cudaError_t e = ensure_smem_attr((const void*)fn, (size_t)optin);
   if (e != cudaSuccess) return e;
   size_t grid = (size_t)num_sms;
@@ -1077,15 +1095,37 @@ cudaError_t launch_mx_variant(const MxGemmArgs& a, int num_sms, size_t upper_uni
   return launch_chained(fn, dim3((unsigned)grid), dim3(C::THREADS), smem, st, 1, a);
 }
 
-// 128-token tiles, 3 stages (2 if the scale panels of a wide K or many
-// experts leave no room). Decode-sized batches run mx_dec_kernel instead.
+// wide: 256-token tiles with K = 64 stages (4 of 40 KB; 3 or 2 if the scale
+// panels of a wide K or many experts leave no room); otherwise 128-token
+// tiles with K = 128 stages (3 of 48 KB, or 2). Decode-sized batches run
+// mx_dec_kernel.
 template <bool GATED>
-cudaError_t launch_mx(const MxGemmArgs& a, int num_sms, size_t ub, cudaStream_t st) {
+cudaError_t launch_mx(const MxGemmArgs& a, bool wide, int num_sms, size_t ub, cudaStream_t st) {
   const int sk_max = a.sk_routed > a.sk_shared ? a.sk_routed : a.sk_shared;
   const size_t optin = (size_t)smem_optin();
-  if (MxCfg<GATED, 128, 3>::smem_bytes(a.E, sk_max) <= optin)
-    return launch_mx_variant<GATED, 128, 3>(a, num_sms, ub, st);
-  return launch_mx_variant<GATED, 128, 2>(a, num_sms, ub, st);
+  if (wide) {
+    if (MxCfg<GATED, 256, 4, 64>::smem_bytes(a.E, sk_max) <= optin)
+      return launch_mx_variant<GATED, 256, 4, 64>(a, num_sms, ub, st);
+    if (MxCfg<GATED, 256, 3, 64>::smem_bytes(a.E, sk_max) <= optin)
+      return launch_mx_variant<GATED, 256, 3, 64>(a, num_sms, ub, st);
+    return launch_mx_variant<GATED, 256, 2, 64>(a, num_sms, ub, st);
+  }
+  if (MxCfg<GATED, 128, 3, 128>::smem_bytes(a.E, sk_max) <= optin)
+    return launch_mx_variant<GATED, 128, 3, 128>(a, num_sms, ub, st);
+  return launch_mx_variant<GATED, 128, 2, 128>(a, num_sms, ub, st);
+}
+
+// 256-token tiles when the experts average at least 256 routed rows (each
+// converted weight tile then serves twice the tokens); below that a 256-token
+// tile would run half empty and its K = 64 stages cost more per weight byte.
+bool mx_wide_tiles(const GemmProblem& p) { return (int64_t)p.T * p.k >= 256 * (int64_t)p.E; }
+
+// The converter kernel's weight-code maps: 64-byte boxes with the 64-byte
+// swizzle for K = 64 stages (wide), else 128-byte boxes with the 128-byte one.
+bool make_code_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows, bool wide) {
+  return wide ? make_code_map64(m, base, rows, cols, box_rows)
+              : make_tma_map(m, base, MOE_DTYPE_E4M3, rows, cols, box_rows);
 }
 
 bool mx_decode_tiles(const GemmProblem& p) {
@@ -1250,8 +1290,10 @@ bool mx_problem_fits(const GemmProblem& p) {
     return MxDecCfg<true, 4>::smem_bytes(p.E, skH, p.H / 32) <= optin &&
            MxDecCfg<false, 4>::smem_bytes(p.E, skd, kd / 32) <= optin;
   }
-  return MxCfg<true, 128, 2>::smem_bytes(p.E, skH) <= optin &&
-         MxCfg<false, 128, 2>::smem_bytes(p.E, skd) <= optin;
+  return MxCfg<true, 256, 2, 64>::smem_bytes(p.E, skH) <= optin &&
+         MxCfg<false, 256, 2, 64>::smem_bytes(p.E, skd) <= optin &&
+         MxCfg<true, 128, 2, 128>::smem_bytes(p.E, skH) <= optin &&
+         MxCfg<false, 128, 2, 128>::smem_bytes(p.E, skd) <= optin;
 }
 
 cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, const void* xq,
@@ -1260,20 +1302,21 @@ cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, cons
                                   cudaStream_t st) {
   const bool has_s = p.Is > 0;
   if (mx_decode_tiles(p)) return cudaErrorInvalidValue;  // the decode kernels' problems
-  const int bn = 128;
+  const bool wide = mx_wide_tiles(p);
+  const int bn = wide ? 256 : 128;
   const uint32_t b1 = bn / 2 < 16 ? 16 : bn / 2;
   const int skH = mx_scale_cols(p.H);
   MxGemmArgs a;
   memset(&a, 0, sizeof(a));
-  bool ok = make_tma_map(&a.tmA[0], w.gate, MOE_DTYPE_E4M3, (uint64_t)p.E * p.I, p.H, 64) &&
-            make_tma_map(&a.tmA[1], w.up, MOE_DTYPE_E4M3, (uint64_t)p.E * p.I, p.H, 64) &&
+  bool ok = make_code_map(&a.tmA[0], w.gate, (uint64_t)p.E * p.I, p.H, 64, wide) &&
+            make_code_map(&a.tmA[1], w.up, (uint64_t)p.E * p.I, p.H, 64, wide) &&
             make_scale_map(&a.tmS[0], w.s_gate, (uint64_t)p.E * p.I, skH, 64) &&
             make_scale_map(&a.tmS[1], w.s_up, (uint64_t)p.E * p.I, skH, 64) &&
             make_b_maps(&a.tmB[0], xg, MOE_DTYPE_BF16, (uint64_t)p.T * p.k, p.H, bn, b1) &&
             make_b_maps(&a.tmB[3], xq, MOE_DTYPE_BF16, p.T, p.H, bn, b1);
   if (ok && has_s)
-    ok = make_tma_map(&a.tmA[2], w.sh_gate, MOE_DTYPE_E4M3, p.Is, p.H, 64) &&
-         make_tma_map(&a.tmA[3], w.sh_up, MOE_DTYPE_E4M3, p.Is, p.H, 64) &&
+    ok = make_code_map(&a.tmA[2], w.sh_gate, p.Is, p.H, 64, wide) &&
+         make_code_map(&a.tmA[3], w.sh_up, p.Is, p.H, 64, wide) &&
          make_scale_map(&a.tmS[2], w.sh_s_gate, p.Is, skH, 64) &&
          make_scale_map(&a.tmS[3], w.sh_s_up, p.Is, skH, 64);
   if (!ok) return cudaErrorInvalidValue;
@@ -1296,7 +1339,7 @@ cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, cons
   a.ld_out_routed = p.I;
   a.ld_out_shared = has_s ? p.Is : 0;
   const size_t ub = unit_upper_bound(p.T, p.k, p.E, bn, p.I / 64, has_s ? p.Is / 64 : 0);
-  return launch_mx<true>(a, p.num_sms, ub, st);
+  return launch_mx<true>(a, wide, p.num_sms, ub, st);
 }
 
 cudaError_t launch_mx_down_gemm(const GemmProblem& p, const MxWeights& w, const void* h,
@@ -1304,17 +1347,18 @@ cudaError_t launch_mx_down_gemm(const GemmProblem& p, const MxWeights& w, const 
                                 const float* topk_w, float* Y, int* status, cudaStream_t st) {
   const bool has_s = p.Is > 0;
   if (mx_decode_tiles(p)) return cudaErrorInvalidValue;  // the decode kernels' problems
-  const int bn = 128;
+  const bool wide = mx_wide_tiles(p);
+  const int bn = wide ? 256 : 128;
   const uint32_t b1 = bn / 2 < 16 ? 16 : bn / 2;
   const int skI = mx_scale_cols(p.I);
   const int skIs = has_s ? mx_scale_cols(p.Is) : skI;
   MxGemmArgs a;
   memset(&a, 0, sizeof(a));
-  bool ok = make_tma_map(&a.tmA[0], w.down, MOE_DTYPE_E4M3, (uint64_t)p.E * p.H, p.I, 128) &&
+  bool ok = make_code_map(&a.tmA[0], w.down, (uint64_t)p.E * p.H, p.I, 128, wide) &&
             make_scale_map(&a.tmS[0], w.s_down, (uint64_t)p.E * p.H, skI, 128) &&
             make_b_maps(&a.tmB[0], h, MOE_DTYPE_BF16, (uint64_t)p.T * p.k, p.I, bn, b1);
   if (ok && has_s)
-    ok = make_tma_map(&a.tmA[2], w.sh_down, MOE_DTYPE_E4M3, p.H, p.Is, 128) &&
+    ok = make_code_map(&a.tmA[2], w.sh_down, p.H, p.Is, 128, wide) &&
          make_scale_map(&a.tmS[2], w.sh_s_down, p.H, skIs, 128) &&
          make_b_maps(&a.tmB[3], hs, MOE_DTYPE_BF16, p.T, p.Is, bn, b1);
   if (!ok) return cudaErrorInvalidValue;
@@ -1340,7 +1384,7 @@ cudaError_t launch_mx_down_gemm(const GemmProblem& p, const MxWeights& w, const 
   a.ld_out_routed = p.H;
   a.ld_out_shared = p.H;
   const size_t ub = unit_upper_bound(p.T, p.k, p.E, bn, p.H / 128, has_s ? p.H / 128 : 0);
-  return launch_mx<false>(a, p.num_sms, ub, st);
+  return launch_mx<false>(a, wide, p.num_sms, ub, st);
 }
 
 }  // namespace moe

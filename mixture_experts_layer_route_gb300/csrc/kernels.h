@@ -16,6 +16,10 @@ namespace moe {
 // or the encoder rejects the shape.
 bool make_tma_map(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols,
                   uint32_t box_rows);
+// Tensor map of E4M3 codes [rows][cols]: boxes of 64 bytes x box_rows rows,
+// 64-byte swizzle.
+bool make_code_map64(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows);
 // Tensor map of a uint8 [rows][cols] matrix (cols a multiple of 16) whose box
 // is box_cols bytes (0: whole rows; a multiple of 16, at most 256) of box_rows
 // rows, no swizzle.

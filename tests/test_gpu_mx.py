@@ -61,6 +61,10 @@ CASES = [
     MoEConfig("mx_t1", T=1, H=128, E=4, k=4, I=128, renorm=0),
     MoEConfig("mx_wide_shared", T=48, H=1024, E=16, k=4, I=640, I_shared=256),
     MoEConfig("mx_e256", T=64, H=256, E=256, k=8, I=128),
+    # experts averaging 256 rows or more: 256-token tiles with K = 64 stages,
+    # ragged tails, a shared expert, and a skewed routing
+    MoEConfig("mx_wide_tiles_shared", T=1100, H=384, E=8, k=2, I=384, I_shared=256),
+    MoEConfig("mx_wide_tiles_zipf", T=1500, H=256, E=8, k=3, I=256, zipf_s=1.2),
 ]
 
 
