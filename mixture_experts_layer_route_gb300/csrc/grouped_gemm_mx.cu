@@ -24,14 +24,16 @@
 //     the scale panel of its weight rows (all K / 32 scale bytes of each row,
 //     one box per 64 or 128 rows) into one of two panel buffers.
 //   warps 6-9, converters (one per TMEM lane quarter, thread = weight row):
-//     per stage, the row's codes times their block scales -> bf16 pairs,
-//     stored into a ring of converted slots of tensor memory (256 columns:
-//     eight of 32 or four of 64; the MMA reads operand A from there: row m in
-//     lane m, column c holding elements 2c and 2c + 1); each slot is handed
-//     back by the MMA's commit.
-//   warp 1, MMA issuer: BK / 16 MMAs of K = 16 per stage, A from tensor
-//     memory, B from the stage's token tile (K-major, 128-byte swizzle), into
-//     the accumulator (two of 128 columns, or one of 256 beside the slots).
+//     once a stage's loads complete, the row's codes times their block
+//     scales -> bf16 pairs, stored into the stage's slot of tensor memory (the
+//     MMA reads operand A from there: row m in lane m, column c holding
+//     elements 2c and 2c + 1), then one arrive per warp on the stage's
+//     "converted" barrier.
+//   warp 1, MMA issuer: per stage one wait (the converted barrier, which
+//     implies the loads), BK / 16 MMAs of K = 16 (A from the slot, B from the
+//     stage's token tile, K-major, 128-byte swizzle) into the accumulator (two
+//     of 128 columns, or one of 256 beside the slots), and one commit that
+//     frees the stage and its slot together.
 //   warps 2-5, epilogue: GATED, silu(gate) * up, then each h row quantized per
 //     block of 32 features (the two threads holding a block's 16 + 16 values
 //     share their maximum) and stored as its bf16 values; DOWN, as the bf16
@@ -93,20 +95,21 @@ struct MxCfg {
   static constexpr int NBH = BK / 64;            // token boxes per stage (64 bf16 elements each)
   static constexpr int B_HALF = BN * 128;
   static constexpr int STAGE_BYTES = A8_BYTES + NBH * B_HALF;
-  static constexpr int SLOT_COLS = BK / 2;       // a converted stage in tensor memory
-  static constexpr int SA = 256 / SLOT_COLS;     // converted-A slots (256 columns in all)
+  // A converted stage in tensor memory: one slot per shared-memory stage, so
+  // a slot is free again exactly when its stage is (the same MMAs read both).
+  static constexpr int SLOT_COLS = BK / 2;
   // Two fp32 accumulators when they fit beside the converted slots, else one
   // (256-token tiles: the epilogue then overlaps only the next unit's loads
   // and conversion, not its MMAs).
-  static constexpr int NACC = 2 * BN + SA * SLOT_COLS <= 512 ? 2 : 1;
+  static constexpr int NACC = 2 * BN + STAGES * SLOT_COLS <= 512 ? 2 : 1;
   static constexpr int ACC_COLS = NACC * BN;
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
   static constexpr int THREADS = 320;            // producer, MMA, 4 epilogue, 4 converter warps
   static constexpr int BOX1 = BN / 2 < 16 ? 16 : BN / 2;
-  // full, empty [STAGES]; cfull, cempty [SA]; pfull, pempty, tfull, tempty [2]; drain
-  static constexpr int NBARS = 2 * STAGES + 2 * SA + 9;
-  static_assert(ACC_COLS + SA * SLOT_COLS <= TMEM_COLS, "tensor memory");
+  // full, empty, cfull [STAGES]; pfull, pempty, tfull, tempty [2]; drain
+  static constexpr int NBARS = 3 * STAGES + 9;
+  static_assert(ACC_COLS + STAGES * SLOT_COLS <= TMEM_COLS, "tensor memory");
   static_assert(BK == 64 || BK == 128, "stage depth");
   static_assert(BN % 32 == 0 && BN <= 256, "token tile");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -256,9 +259,8 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
   const uint32_t bars_base = smem_u32(bars);
   auto full_bar = [&](int s) { return bars_base + 8u * (uint32_t)s; };
   auto empty_bar = [&](int s) { return bars_base + 8u * (uint32_t)(STAGES + s); };
-  auto cfull_bar = [&](int c) { return bars_base + 8u * (uint32_t)(2 * STAGES + c); };
-  auto cempty_bar = [&](int c) { return bars_base + 8u * (uint32_t)(2 * STAGES + C::SA + c); };
-  constexpr int B0 = 2 * STAGES + 2 * C::SA;
+  auto cfull_bar = [&](int s) { return bars_base + 8u * (uint32_t)(2 * STAGES + s); };
+  constexpr int B0 = 3 * STAGES;
   auto pfull_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + p); };
   auto pempty_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + 2 + p); };
   auto tfull_bar = [&](int a) { return bars_base + 8u * (uint32_t)(B0 + 4 + a); };
@@ -271,10 +273,7 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-    }
-    for (int c = 0; c < C::SA; ++c) {
-      mbar_init(cfull_bar(c), 4);  // one arrive per converter warp
-      mbar_init(cempty_bar(c), 1);
+      mbar_init(cfull_bar(s), 4);  // one arrive per converter warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(pfull_bar(i), 1);
@@ -408,8 +407,8 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t lt = 0, ph = 0, cph = 0;
-      int stg = 0, cstg = 0;
+      uint32_t lt = 0, ph = 0;
+      int stg = 0;
       bool ok = true;
       for (int u = cid; u < total && ok; u += ncl, ++lt) {
         const Tile tl = tile_of(u);
@@ -421,9 +420,10 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
         const int n_mma = (tl.n_valid + 15) / 16 * 16;
         const uint32_t idesc = umma_idesc(1, C::BM, (uint32_t)n_mma);
         for (int kb = 0; kb < kdim / C::BK; ++kb) {
-          const int s = stg, c = cstg;
-          if (!mbar_wait(full_bar(s), ph, args.status, limit) ||
-              !mbar_wait(cfull_bar(c), cph, args.status, limit)) {
+          // One wait per stage: the converters arrive on cfull only after
+          // they saw the stage's loads (codes and token tile) complete.
+          const int s = stg;
+          if (!mbar_wait(cfull_bar(s), ph, args.status, limit)) {
             ok = false;
             break;
           }
@@ -431,20 +431,18 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
             stg = 0;
             ph ^= 1u;
           }
-          if (++cstg == C::SA) {
-            cstg = 0;
-            cph ^= 1u;
-          }
           tc_fence_after();
-          const uint32_t a_t = tmem_base + C::ACC_COLS + (uint32_t)(c * C::SLOT_COLS);
+          const uint32_t a_t = tmem_base + C::ACC_COLS + (uint32_t)(s * C::SLOT_COLS);
           const uint32_t b_addr = stages_base + (uint32_t)s * C::STAGE_BYTES + C::A8_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
             umma_issue_tmem_a(d_tmem, a_t + (uint32_t)kk * 8u,
                               umma_desc_sw128(b_addr + (kk >> 2) * C::B_HALF + (kk & 3) * 32),
                               idesc, (kb | kk) != 0 ? 1u : 0u);
+          // Frees the stage and its slot: the producer refills the stage only
+          // after this, and the converters write the slot only after the
+          // refill's loads completed.
           umma_commit(empty_bar(s));
-          umma_commit(cempty_bar(c));
         }
         if (!ok) break;
         umma_commit(tfull_bar((int)acc));
@@ -458,8 +456,8 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;  // weight row of the unit = TMEM lane
     const uint32_t lane_field = (uint32_t)(q * 32) << 16;
-    uint32_t lt = 0, ph = 0, cph = 0;
-    int stg = 0, cstg = 0;
+    uint32_t lt = 0, ph = 0;
+    int stg = 0;
     bool ok = true;
     for (int u = cid; u < total && ok; u += ncl, ++lt) {
       const Tile tl = tile_of(u);
@@ -470,19 +468,16 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
       if (!warp_wait(pfull_bar(p), (lt >> 1) & 1u, args.status, limit)) break;
       const uint8_t* srow = panels + (size_t)p * panel_bytes + (size_t)r * sk;
       for (int kb = 0; kb < kdim / C::BK; ++kb) {
-        const int s = stg, c = cstg;
-        if (!warp_wait(full_bar(s), ph, args.status, limit) ||
-            !warp_wait(cempty_bar(c), cph ^ 1u, args.status, limit)) {
+        // The stage's slot is free: the stage was refilled only after the
+        // MMAs that read its previous contents (and the slot) completed.
+        const int s = stg;
+        if (!warp_wait(full_bar(s), ph, args.status, limit)) {
           ok = false;
           break;
         }
         if (++stg == STAGES) {
           stg = 0;
           ph ^= 1u;
-        }
-        if (++cstg == C::SA) {
-          cstg = 0;
-          cph ^= 1u;
         }
         tc_fence_after();
         // BK / 32 scale bytes per stage (blocks BK / 32 * kb ..).
@@ -505,13 +500,13 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
             mx_decode4_bf16(ch.z, X, o[8 * jj + 4], o[8 * jj + 5]);
             mx_decode4_bf16(ch.w, X, o[8 * jj + 6], o[8 * jj + 7]);
           }
-          tmem_st32(tmem_base + lane_field + C::ACC_COLS + (uint32_t)(c * C::SLOT_COLS + h * 32),
+          tmem_st32(tmem_base + lane_field + C::ACC_COLS + (uint32_t)(s * C::SLOT_COLS + h * 32),
                     o);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(cfull_bar(c));
+        if (lane == 0) mbar_arrive(cfull_bar(s));
       }
       if (!ok) break;
       __syncwarp();
