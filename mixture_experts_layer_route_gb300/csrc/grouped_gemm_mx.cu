@@ -18,22 +18,27 @@
 // chosen per problem: when the experts average 256 routed rows or more,
 // 256-token tiles with K = 64 per stage (each converted weight tile serves
 // twice the tokens); otherwise 128-token tiles with K = 128 per stage.
-//   warp 0, producer: per stage the 128 weight rows' codes (one BK-byte box
-//     per 64 or 128 rows; 64-byte swizzle for K = 64, 128-byte for K = 128)
-//     and the token tile (boxes of BN tokens x 64 bf16 elements); per unit
-//     the scale panel of its weight rows (all K / 32 scale bytes of each row,
-//     one box per 64 or 128 rows) into one of two panel buffers.
+//   warp 0, token producer: per stage the token tile (boxes of BN tokens x
+//     64 bf16 elements) into a ring of STAGES stages.
+//   warp 10, code producer: per stage the 128 weight rows' codes (one BK-byte
+//     box per 64 or 128 rows; 64-byte swizzle for K = 64, 128-byte for K =
+//     128) into a ring of CST stages of its own, and per unit the scale panel
+//     of its weight rows (all K / 32 scale bytes of each row, one box per 64
+//     or 128 rows) into one of two panel buffers. The codes run ahead of the
+//     token tiles, so their conversion is off the loop a token stage goes
+//     through (MMA done -> refill -> MMA).
 //   warps 6-9, converters (one per TMEM lane quarter, thread = weight row):
-//     once a stage's loads complete, the row's codes times their block
-//     scales -> bf16 pairs, stored into the stage's slot of tensor memory (the
-//     MMA reads operand A from there: row m in lane m, column c holding
-//     elements 2c and 2c + 1), then one arrive per warp on the stage's
-//     "converted" barrier.
-//   warp 1, MMA issuer: per stage one wait (the converted barrier, which
-//     implies the loads), BK / 16 MMAs of K = 16 (A from the slot, B from the
-//     stage's token tile, K-major, 128-byte swizzle) into the accumulator (two
-//     of 128 columns, or one of 256 beside the slots), and one commit that
-//     frees the stage and its slot together.
+//     once a stage's codes landed and the slot of its token stage is free
+//     (the MMAs of that stage's previous round completed), the row's codes
+//     times their block scales -> bf16 pairs, stored into the slot (the MMA
+//     reads operand A from there: row m in lane m, column c holding elements
+//     2c and 2c + 1), then one arrive per warp on the stage's "converted"
+//     barrier and on the code stage's "empty" one.
+//   warp 1, MMA issuer: per stage a wait for the token tile and one for the
+//     converted slot, BK / 16 MMAs of K = 16 (A from the slot, B from the
+//     token stage, K-major, 128-byte swizzle) into the accumulator (two of 128
+//     columns, or one of 256 beside the slots), and one commit that frees the
+//     token stage and its slot together.
 //   warps 2-5, epilogue: GATED, silu(gate) * up, then each h row quantized per
 //     block of 32 features (the two threads holding a block's 16 + 16 values
 //     share their maximum) and stored as its bf16 values; DOWN, as the bf16
@@ -86,7 +91,7 @@ struct MxGemmArgs {
 
 namespace {
 
-template <bool GATED, int BN, int STAGES, int BK_ = 128>
+template <bool GATED, int BN, int STAGES, int CST, int BK_>
 struct MxCfg {
   static constexpr int BM = 128;                 // weight rows per unit (MMA M)
   static constexpr int WM = GATED ? 64 : 128;    // output features per unit
@@ -94,7 +99,7 @@ struct MxCfg {
   static constexpr int A8_BYTES = BM * BK;       // codes of one stage (BK-byte rows)
   static constexpr int NBH = BK / 64;            // token boxes per stage (64 bf16 elements each)
   static constexpr int B_HALF = BN * 128;
-  static constexpr int STAGE_BYTES = A8_BYTES + NBH * B_HALF;
+  static constexpr int STAGE_BYTES = NBH * B_HALF;  // token ring stage (STAGES of them)
   // A converted stage in tensor memory: one slot per shared-memory stage, so
   // a slot is free again exactly when its stage is (the same MMAs read both).
   static constexpr int SLOT_COLS = BK / 2;
@@ -105,18 +110,19 @@ struct MxCfg {
   static constexpr int ACC_COLS = NACC * BN;
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_FLOATS = GATED ? 128 * 33 : 2 * BN;
-  static constexpr int THREADS = 320;            // producer, MMA, 4 epilogue, 4 converter warps
+  // token producer, MMA, 4 epilogue, 4 converter warps, code producer
+  static constexpr int THREADS = 352;
   static constexpr int BOX1 = BN / 2 < 16 ? 16 : BN / 2;
-  // full, empty, cfull [STAGES]; pfull, pempty, tfull, tempty [2]; drain
-  static constexpr int NBARS = 3 * STAGES + 9;
+  // full, empty, cfull [STAGES]; afull, aempty [CST]; pfull, pempty, tfull, tempty [2]; drain
+  static constexpr int NBARS = 3 * STAGES + 2 * CST + 9;
   static_assert(ACC_COLS + STAGES * SLOT_COLS <= TMEM_COLS, "tensor memory");
   static_assert(BK == 64 || BK == 128, "stage depth");
   static_assert(BN % 32 == 0 && BN <= 256, "token tile");
-  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(STAGE_BYTES % 1024 == 0 && A8_BYTES % 1024 == 0, "stage alignment");
 
   static size_t smem_bytes(int E, int sk_max) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + 2 * (size_t)BM * sk_max + EPI_FLOATS * 4 +
-           NBARS * 8 + 16 + 3 * (size_t)(E + 2) * 4;
+    return 1024 + (size_t)STAGES * STAGE_BYTES + (size_t)CST * A8_BYTES +
+           2 * (size_t)BM * sk_max + EPI_FLOATS * 4 + NBARS * 8 + 16 + 3 * (size_t)(E + 2) * 4;
   }
 };
 
@@ -232,19 +238,20 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* st
   return __all_sync(0xffffffffu, ok);
 }
 
-template <bool GATED, int BN, int STAGES, int BK>
-__global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
+template <bool GATED, int BN, int STAGES, int CST, int BK>
+__global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, CST, BK>::THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ MxGemmArgs args) {
   pdl_trigger();
-  using C = MxCfg<GATED, BN, STAGES, BK>;
+  using C = MxCfg<GATED, BN, STAGES, CST, BK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int E = args.E;
   const int sk_max = args.sk_routed > args.sk_shared ? args.sk_routed : args.sk_shared;
   const int panel_bytes = C::BM * sk_max;
-  uint8_t* stages = smem;
-  uint8_t* panels = stages + (size_t)STAGES * C::STAGE_BYTES;
+  uint8_t* stages = smem;                                       // token ring
+  uint8_t* astages = stages + (size_t)STAGES * C::STAGE_BYTES;  // code ring
+  uint8_t* panels = astages + (size_t)CST * C::A8_BYTES;
   float* epi = reinterpret_cast<float*>(panels + 2 * (size_t)panel_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_FLOATS);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NBARS);
@@ -260,13 +267,16 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
   auto full_bar = [&](int s) { return bars_base + 8u * (uint32_t)s; };
   auto empty_bar = [&](int s) { return bars_base + 8u * (uint32_t)(STAGES + s); };
   auto cfull_bar = [&](int s) { return bars_base + 8u * (uint32_t)(2 * STAGES + s); };
-  constexpr int B0 = 3 * STAGES;
+  auto afull_bar = [&](int j) { return bars_base + 8u * (uint32_t)(3 * STAGES + j); };
+  auto aempty_bar = [&](int j) { return bars_base + 8u * (uint32_t)(3 * STAGES + CST + j); };
+  constexpr int B0 = 3 * STAGES + 2 * CST;
   auto pfull_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + p); };
   auto pempty_bar = [&](int p) { return bars_base + 8u * (uint32_t)(B0 + 2 + p); };
   auto tfull_bar = [&](int a) { return bars_base + 8u * (uint32_t)(B0 + 4 + a); };
   auto tempty_bar = [&](int a) { return bars_base + 8u * (uint32_t)(B0 + 6 + a); };
   const uint32_t drain_bar = bars_base + 8u * (uint32_t)(B0 + 8);
   const uint32_t stages_base = smem_u32(stages);
+  const uint32_t astages_base = smem_u32(astages);
   const uint32_t panels_base = smem_u32(panels);
 
   if (threadIdx.x == 0) {
@@ -274,6 +284,10 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(cfull_bar(s), 4);  // one arrive per converter warp
+    }
+    for (int j = 0; j < CST; ++j) {
+      mbar_init(afull_bar(j), 1);
+      mbar_init(aempty_bar(j), 4);  // one arrive per converter warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(pfull_bar(i), 1);
@@ -310,20 +324,68 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    const uint64_t pol_w = BN <= 64 ? l2_policy_evict_first() : l2_policy_evict_normal();
+    // ------------------------------------------------------------ token producer
     const uint64_t pol_t = l2_policy_evict_last();
-    // Test hook (MOE_FLAG_TEST_SKIP_SIGNAL): the first stage is never loaded,
-    // so the converters' wait on it runs out.
+    // Test hook (MOE_FLAG_TEST_SKIP_SIGNAL): the first token stage is never
+    // loaded, so the MMA issuer's wait on it runs out.
     const bool skip_first = (args.flags & MOE_FLAG_TEST_SKIP_SIGNAL) != 0;
     uint32_t it = skip_first ? 1u : 0u;
     int stg = (int)it;
     uint32_t ph = 0;
     int kb_first = skip_first ? 1 : 0;
     bool ok = true;
+    for (int u = cid; u < total && ok; u += ncl) {
+      const Tile tl = tile_of(u);
+      const bool shared = tl.g == E;
+      const int kdim = shared ? args.kdim_shared : args.kdim_routed;
+      const int n_mma = (tl.n_valid + 15) / 16 * 16;
+      const int bsel = n_mma <= 16 ? 2 : (n_mma <= C::BOX1 ? 1 : 0);
+      const int box_rows = bsel == 2 ? 16 : (bsel == 1 ? C::BOX1 : BN);
+      const uint32_t tx = (uint32_t)(C::NBH * box_rows * 128);
+      const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
+      const CUtensorMap* my_map = &args.tmB[(shared ? 3 : 0) + bsel];
+      const int nkb = kdim / C::BK;
+      const int kb0 = kb_first;
+      kb_first = 0;
+      for (int kb = kb0; kb < nkb; ++kb) {
+        const int s = stg;
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(empty_bar(s), ph ^ 1u, args.status, limit);
+        if (!__shfl_sync(0xffffffffu, wok, 0)) {
+          ok = false;
+          break;
+        }
+        ++it;
+        if (++stg == STAGES) {
+          stg = 0;
+          ph ^= 1u;
+        }
+        const uint32_t dst = stages_base + (uint32_t)s * C::STAGE_BYTES;
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
+        __syncwarp();
+        // Lane h: the tile's h-th box of 64 bf16 elements.
+        if (lane < C::NBH)
+          tma_load_2d(dst + (uint32_t)(lane * C::B_HALF), my_map, kb * C::BK + 64 * lane, b_row0,
+                      full_bar(s), pol_t);
+      }
+    }
+    // Let the last loads land before the CTA can exit (bounded, status ignored).
+    if (lane == 0) {
+      const uint32_t n_last = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+      for (uint32_t i = it - n_last; i < it; ++i)
+        mbar_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u, nullptr, 20000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ code producer
+    // Weight codes run ahead of the token tiles in their own ring, so their
+    // conversion is done before the MMA needs the slot.
+    const uint64_t pol_w = BN <= 64 ? l2_policy_evict_first() : l2_policy_evict_normal();
+    uint32_t it = 0, aph = 0;
+    int ast = 0;
+    bool ok = true;
     uint32_t lt = 0;
     constexpr int NA = GATED ? 2 : 1;
-    constexpr int NLOADS = NA + C::NBH;
     for (int u = cid; u < total && ok; u += ncl, ++lt) {
       const Tile tl = tile_of(u);
       const bool shared = tl.g == E;
@@ -346,59 +408,35 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
           tma_load_2d(pdst + (uint32_t)(lane * 64 * sk), &args.tmS[(shared ? 2 : 0) + lane], 0,
                       a_row0, pfull_bar(p), pol_w);
       }
-      const int n_mma = (tl.n_valid + 15) / 16 * 16;
-      const int bsel = n_mma <= 16 ? 2 : (n_mma <= C::BOX1 ? 1 : 0);
-      const int box_rows = bsel == 2 ? 16 : (bsel == 1 ? C::BOX1 : BN);
-      const uint32_t tx = C::A8_BYTES + (uint32_t)(C::NBH * box_rows * 128);
-      const int b_row0 = shared ? tl.p0 - offs[E] : tl.p0;
-      // Per-lane operands: lanes < NA weight codes (GATED: gate, up rows; one
-      // BK-byte box of 64 or 128 rows each), then the token tile's NBH boxes
-      // of 64 elements.
-      const CUtensorMap* my_map = &args.tmA[shared ? 2 : 0];
-      int my_row = a_row0, my_dx = 0;
-      uint32_t my_off = 0;
-      uint64_t my_pol = pol_w;
-      if (GATED && lane == 1) {
-        my_map = &args.tmA[shared ? 3 : 1];
-        my_off = 64 * C::BK;
-      }
-      if (lane >= NA && lane < NLOADS) {
-        const int h = lane - NA;
-        my_map = &args.tmB[(shared ? 3 : 0) + bsel];
-        my_row = b_row0;
-        my_dx = 64 * h;
-        my_off = C::A8_BYTES + (uint32_t)(h * C::B_HALF);
-        my_pol = pol_t;
-      }
+      // Lanes < NA: the weight codes (GATED: gate, up rows; one BK-byte box of
+      // 64 or 128 rows each).
+      const CUtensorMap* my_map = &args.tmA[(shared ? 2 : 0) + (GATED && lane == 1 ? 1 : 0)];
+      const uint32_t my_off = GATED && lane == 1 ? 64u * C::BK : 0u;
       const int nkb = kdim / C::BK;
-      const int kb0 = kb_first;
-      kb_first = 0;
-      for (int kb = kb0; kb < nkb; ++kb) {
-        const int s = stg;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int j = ast;
         int wok = 1;
-        if (lane == 0) wok = mbar_wait(empty_bar(s), ph ^ 1u, args.status, limit);
+        if (lane == 0) wok = mbar_wait(aempty_bar(j), aph ^ 1u, args.status, limit);
         if (!__shfl_sync(0xffffffffu, wok, 0)) {
           ok = false;
           break;
         }
         ++it;
-        if (++stg == STAGES) {
-          stg = 0;
-          ph ^= 1u;
+        if (++ast == CST) {
+          ast = 0;
+          aph ^= 1u;
         }
-        const uint32_t dst = stages_base + (uint32_t)s * C::STAGE_BYTES;
-        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
+        const uint32_t dst = astages_base + (uint32_t)j * C::A8_BYTES;
+        if (lane == 0) mbar_arrive_expect_tx(afull_bar(j), (uint32_t)C::A8_BYTES);
         __syncwarp();
-        // Codes: x in bytes; tokens: x in bf16 elements.
-        if (lane < NLOADS)
-          tma_load_2d(dst + my_off, my_map, kb * C::BK + my_dx, my_row, full_bar(s), my_pol);
+        if (lane < NA) tma_load_2d(dst + my_off, my_map, kb * C::BK, a_row0, afull_bar(j), pol_w);
       }
     }
     // Let the last loads land before the CTA can exit (bounded, status ignored).
     if (lane == 0) {
-      const uint32_t n_last = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+      const uint32_t n_last = it < (uint32_t)CST ? it : (uint32_t)CST;
       for (uint32_t i = it - n_last; i < it; ++i)
-        mbar_wait(full_bar((int)(i % STAGES)), (i / STAGES) & 1u, nullptr, 20000000ull);
+        mbar_wait(afull_bar((int)(i % CST)), (i / CST) & 1u, nullptr, 20000000ull);
       const uint32_t p_last = lt < 2u ? lt : 2u;
       for (uint32_t i = lt - p_last; i < lt; ++i)
         mbar_wait(pfull_bar((int)(i & 1u)), (i >> 1) & 1u, nullptr, 20000000ull);
@@ -420,10 +458,10 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
         const int n_mma = (tl.n_valid + 15) / 16 * 16;
         const uint32_t idesc = umma_idesc(1, C::BM, (uint32_t)n_mma);
         for (int kb = 0; kb < kdim / C::BK; ++kb) {
-          // One wait per stage: the converters arrive on cfull only after
-          // they saw the stage's loads (codes and token tile) complete.
+          // The stage's token tile and its converted weight slot.
           const int s = stg;
-          if (!mbar_wait(cfull_bar(s), ph, args.status, limit)) {
+          if (!mbar_wait(full_bar(s), ph, args.status, limit) ||
+              !mbar_wait(cfull_bar(s), ph, args.status, limit)) {
             ok = false;
             break;
           }
@@ -433,15 +471,14 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a_t = tmem_base + C::ACC_COLS + (uint32_t)(s * C::SLOT_COLS);
-          const uint32_t b_addr = stages_base + (uint32_t)s * C::STAGE_BYTES + C::A8_BYTES;
+          const uint32_t b_addr = stages_base + (uint32_t)s * C::STAGE_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
             umma_issue_tmem_a(d_tmem, a_t + (uint32_t)kk * 8u,
                               umma_desc_sw128(b_addr + (kk >> 2) * C::B_HALF + (kk & 3) * 32),
                               idesc, (kb | kk) != 0 ? 1u : 0u);
-          // Frees the stage and its slot: the producer refills the stage only
-          // after this, and the converters write the slot only after the
-          // refill's loads completed.
+          // Frees the token stage and its slot together (the converters wait
+          // on the same barrier before writing the slot again).
           umma_commit(empty_bar(s));
         }
         if (!ok) break;
@@ -451,13 +488,13 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
       mbar_wait(drain_bar, 0, nullptr, 20000000ull);
     }
     __syncwarp();
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------------------ converters
     const int q = warp & 3;
     const int r = q * 32 + lane;  // weight row of the unit = TMEM lane
     const uint32_t lane_field = (uint32_t)(q * 32) << 16;
-    uint32_t lt = 0, ph = 0;
-    int stg = 0;
+    uint32_t lt = 0, ph = 0, aph = 0;
+    int stg = 0, ast = 0;
     bool ok = true;
     for (int u = cid; u < total && ok; u += ncl, ++lt) {
       const Tile tl = tile_of(u);
@@ -468,10 +505,12 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
       if (!warp_wait(pfull_bar(p), (lt >> 1) & 1u, args.status, limit)) break;
       const uint8_t* srow = panels + (size_t)p * panel_bytes + (size_t)r * sk;
       for (int kb = 0; kb < kdim / C::BK; ++kb) {
-        // The stage's slot is free: the stage was refilled only after the
-        // MMAs that read its previous contents (and the slot) completed.
-        const int s = stg;
-        if (!warp_wait(full_bar(s), ph, args.status, limit)) {
+        // The codes of this k-block, and the slot of its token stage free:
+        // the MMAs of that stage's previous round completed (no later round
+        // can complete before this warp's arrival on cfull).
+        const int s = stg, j = ast;
+        if (!warp_wait(afull_bar(j), aph, args.status, limit) ||
+            !warp_wait(empty_bar(s), ph ^ 1u, args.status, limit)) {
           ok = false;
           break;
         }
@@ -479,13 +518,17 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
           stg = 0;
           ph ^= 1u;
         }
+        if (++ast == CST) {
+          ast = 0;
+          aph ^= 1u;
+        }
         tc_fence_after();
         // BK / 32 scale bytes per stage (blocks BK / 32 * kb ..).
         const uint32_t sw = C::BK == 128 ? *reinterpret_cast<const uint32_t*>(srow + kb * 4)
                                          : *reinterpret_cast<const uint16_t*>(srow + kb * 2);
         // BK-byte rows: 128-byte swizzle (chunk j of row r at j ^ (r & 7)) or
         // 64-byte swizzle (at j ^ ((r >> 1) & 3)).
-        const uint8_t* arow = stages + (size_t)s * C::STAGE_BYTES + (size_t)r * C::BK;
+        const uint8_t* arow = astages + (size_t)j * C::A8_BYTES + (size_t)r * C::BK;
         const int rsw = C::BK == 128 ? (r & 7) : ((r >> 1) & 3);
 #pragma unroll
         for (int h = 0; h < C::NBH; ++h) {
@@ -506,7 +549,10 @@ __global__ void __launch_bounds__(MxCfg<GATED, BN, STAGES, BK>::THREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(cfull_bar(s));
+        if (lane == 0) {
+          mbar_arrive(cfull_bar(s));
+          mbar_arrive(aempty_bar(j));
+        }
       }
       if (!ok) break;
       __syncwarp();
@@ -1073,15 +1119,15 @@ int smem_optin() {
   return cache[dev];
 }
 
-template <bool GATED, int BN, int STAGES, int BK>
+template <bool GATED, int BN, int STAGES, int CST, int BK>
 cudaError_t launch_mx_variant(const MxGemmArgs& a, int num_sms, size_t upper_units,
                               cudaStream_t st) {
-  using C = MxCfg<GATED, BN, STAGES, BK>;
+  using C = MxCfg<GATED, BN, STAGES, CST, BK>;
   const int sk_max = a.sk_routed > a.sk_shared ? a.sk_routed : a.sk_shared;
   const size_t smem = C::smem_bytes(a.E, sk_max);
   const int optin = smem_optin();
   if (smem > (size_t)optin) return cudaErrorInvalidValue;
-  auto fn = mx_gemm_kernel<GATED, BN, STAGES, BK>;
+  auto fn = mx_gemm_kernel<GATED, BN, STAGES, CST, BK>;
   cudaError_t e = ensure_smem_attr((const void*)fn, (size_t)optin);
   if (e != cudaSuccess) return e;
   size_t grid = (size_t)num_sms;
@@ -1090,24 +1136,27 @@ cudaError_t launch_mx_variant(const MxGemmArgs& a, int num_sms, size_t upper_uni
   return launch_chained(fn, dim3((unsigned)grid), dim3(C::THREADS), smem, st, 1, a);
 }
 
-// wide: 256-token tiles with K = 64 stages (4 of 40 KB; 3 or 2 if the scale
-// panels of a wide K or many experts leave no room); otherwise 128-token
-// tiles with K = 128 stages (3 of 48 KB, or 2). Decode-sized batches run
-// mx_dec_kernel.
+// wide: 256-token tiles with K = 64 stages (token ring of 4 stages of 32 KB,
+// code ring of 5 of 8 KB; fewer when the scale panels of a wide K or many
+// experts leave no room); otherwise 128-token tiles with K = 128 stages
+// (token ring of 4 stages of 32 KB, code ring of 3 of 16 KB; or fewer).
+// Decode-sized batches run mx_dec_kernel.
 template <bool GATED>
 cudaError_t launch_mx(const MxGemmArgs& a, bool wide, int num_sms, size_t ub, cudaStream_t st) {
   const int sk_max = a.sk_routed > a.sk_shared ? a.sk_routed : a.sk_shared;
   const size_t optin = (size_t)smem_optin();
   if (wide) {
-    if (MxCfg<GATED, 256, 4, 64>::smem_bytes(a.E, sk_max) <= optin)
-      return launch_mx_variant<GATED, 256, 4, 64>(a, num_sms, ub, st);
-    if (MxCfg<GATED, 256, 3, 64>::smem_bytes(a.E, sk_max) <= optin)
-      return launch_mx_variant<GATED, 256, 3, 64>(a, num_sms, ub, st);
-    return launch_mx_variant<GATED, 256, 2, 64>(a, num_sms, ub, st);
+    if (MxCfg<GATED, 256, 4, 5, 64>::smem_bytes(a.E, sk_max) <= optin)
+      return launch_mx_variant<GATED, 256, 4, 5, 64>(a, num_sms, ub, st);
+    if (MxCfg<GATED, 256, 3, 4, 64>::smem_bytes(a.E, sk_max) <= optin)
+      return launch_mx_variant<GATED, 256, 3, 4, 64>(a, num_sms, ub, st);
+    return launch_mx_variant<GATED, 256, 2, 3, 64>(a, num_sms, ub, st);
   }
-  if (MxCfg<GATED, 128, 3, 128>::smem_bytes(a.E, sk_max) <= optin)
-    return launch_mx_variant<GATED, 128, 3, 128>(a, num_sms, ub, st);
-  return launch_mx_variant<GATED, 128, 2, 128>(a, num_sms, ub, st);
+  if (MxCfg<GATED, 128, 4, 3, 128>::smem_bytes(a.E, sk_max) <= optin)
+    return launch_mx_variant<GATED, 128, 4, 3, 128>(a, num_sms, ub, st);
+  if (MxCfg<GATED, 128, 3, 3, 128>::smem_bytes(a.E, sk_max) <= optin)
+    return launch_mx_variant<GATED, 128, 3, 3, 128>(a, num_sms, ub, st);
+  return launch_mx_variant<GATED, 128, 2, 2, 128>(a, num_sms, ub, st);
 }
 
 // 256-token tiles when the experts average at least 256 routed rows (each
@@ -1285,10 +1334,10 @@ bool mx_problem_fits(const GemmProblem& p) {
     return MxDecCfg<true, 4>::smem_bytes(p.E, skH, p.H / 32) <= optin &&
            MxDecCfg<false, 4>::smem_bytes(p.E, skd, kd / 32) <= optin;
   }
-  return MxCfg<true, 256, 2, 64>::smem_bytes(p.E, skH) <= optin &&
-         MxCfg<false, 256, 2, 64>::smem_bytes(p.E, skd) <= optin &&
-         MxCfg<true, 128, 2, 128>::smem_bytes(p.E, skH) <= optin &&
-         MxCfg<false, 128, 2, 128>::smem_bytes(p.E, skd) <= optin;
+  return MxCfg<true, 256, 2, 3, 64>::smem_bytes(p.E, skH) <= optin &&
+         MxCfg<false, 256, 2, 3, 64>::smem_bytes(p.E, skd) <= optin &&
+         MxCfg<true, 128, 2, 2, 128>::smem_bytes(p.E, skH) <= optin &&
+         MxCfg<false, 128, 2, 2, 128>::smem_bytes(p.E, skd) <= optin;
 }
 
 cudaError_t launch_mx_swiglu_gemm(const GemmProblem& p, const MxWeights& w, const void* xq,
