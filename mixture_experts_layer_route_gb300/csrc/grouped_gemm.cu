@@ -5,9 +5,10 @@
 //     stages of 16 KB of weights; the gated GEMM gathers its token rows with
 //     TMA gather4, so no expert-ordered copy of x is made;
 //   otherwise: token tiles of up to 256 rows on CTA pairs (cta_group::2
-//     MMAs, M = 256, 6 stages of 32 KB per SM; MOE_TILE_MEDIUM: 128 rows, 8
-//     stages of 24 KB), every
-//     expert in the same launch, heaviest experts first; the gated GEMM reads
+//     MMAs, M = 256, 3 stages of two 128-byte K boxes, 64 KB per SM;
+//     MOE_TILE_MEDIUM: 128 rows, 4 stages of 48 KB; one box per stage, twice
+//     the stages, when a contraction length is not a multiple of two boxes),
+//     every expert in the same launch, heaviest experts first; the gated GEMM reads
 //     the routed rows from their expert-ordered copy and each tile loads the
 //     smallest token box (128, 64 or 16 rows per CTA) that covers it. Groups
 //     with an odd number of feature blocks fall back to single-CTA tiles.
@@ -132,12 +133,12 @@ cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
 
 namespace {
 
-template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1>
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1, int NBX = 1>
 cudaError_t launch_variant(const GroupedGemmArgs& a, int num_sms, int E, size_t upper_tiles,
                            cudaStream_t st) {
-  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>;
+  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL, NBX>;
   const size_t smem = C::smem_bytes(E);
-  auto fn = grouped_gemm_kernel<TIn, GATED, BN, STAGES, BMODE, CL>;
+  auto fn = grouped_gemm_kernel<TIn, GATED, BN, STAGES, BMODE, CL, NBX>;
   // Opt in once to what the largest supported expert count needs, so that a
   // later call with more experts than the first still fits.
   cudaError_t e = ensure_smem_attr((const void*)fn, C::smem_bytes(kMaxExperts));
@@ -192,8 +193,8 @@ bool use_decode_kernel(const GemmProblem& p) {
   return p.tile == MOE_TILE_DECODE || (p.tile == MOE_TILE_AUTO && p.T <= kSmallBatch);
 }
 
-// Token tile of the tiled kernel: 256 (6 stages of 32 KB per SM), or 128 (8
-// stages of 24 KB) when forced. 128-token tiles measured slower on every
+// Token tile of the tiled kernel: 256 (3 stages of 64 KB per SM), or 128 (4
+// stages of 48 KB) when forced. 128-token tiles measured slower on every
 // layer shape: a 256 x 128 pair MMA step is fed at ~94 B/clk per SM, and an
 // expert of 129..256 rows then streams its weights to the SMs twice.
 int tiled_tile_n(const GemmProblem& p) { return p.tile == MOE_TILE_MEDIUM ? 128 : 256; }
@@ -235,13 +236,27 @@ bool prefetch_first_units(const GemmProblem& p, bool dec) {
   return dec && p.Is == 0 && (int64_t)p.T * p.k >= 4 * (int64_t)p.E;
 }
 
+// CTA pairs take two 128-byte K boxes per stage (the MMA issuer then waits and
+// commits once per eight MMAs) when every contraction length is a multiple
+// of two boxes.
+template <typename TIn>
+bool two_box_stages(const GroupedGemmArgs& a) {
+  const int kb2 = 256 / (int)sizeof(TIn);
+  return a.kdim_routed % kb2 == 0 && a.kdim_shared % kb2 == 0;
+}
+
 template <typename TIn>
 cudaError_t launch_gated(const GroupedGemmArgs& a, const GemmProblem& p, bool dec, bool pair,
                          int tile_n, size_t ub, cudaStream_t st) {
   if (dec) return launch_variant<TIn, true, 32, 9, kGather4>(a, p.num_sms, p.E, ub, st);
+  const size_t pu = (ub + 1) / 2;
+  const bool two = two_box_stages<TIn>(a);
   if (pair && tile_n == 128)
-    return launch_variant<TIn, true, 128, 8, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2, st);
-  if (pair) return launch_variant<TIn, true, 256, 6, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2, st);
+    return two ? launch_variant<TIn, true, 128, 4, kTiled, 2, 2>(a, p.num_sms, p.E, pu, st)
+               : launch_variant<TIn, true, 128, 8, kTiled, 2>(a, p.num_sms, p.E, pu, st);
+  if (pair)
+    return two ? launch_variant<TIn, true, 256, 3, kTiled, 2, 2>(a, p.num_sms, p.E, pu, st)
+               : launch_variant<TIn, true, 256, 6, kTiled, 2>(a, p.num_sms, p.E, pu, st);
   return launch_variant<TIn, true, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
 }
 
@@ -249,10 +264,14 @@ template <typename TIn>
 cudaError_t launch_down(const GroupedGemmArgs& a, const GemmProblem& p, bool dec, bool pair,
                         int tile_n, size_t ub, cudaStream_t st) {
   if (dec) return launch_variant<TIn, false, 32, 9, kTiled>(a, p.num_sms, p.E, ub, st);
+  const size_t pu = (ub + 1) / 2;
+  const bool two = two_box_stages<TIn>(a);
   if (pair && tile_n == 128)
-    return launch_variant<TIn, false, 128, 8, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2, st);
+    return two ? launch_variant<TIn, false, 128, 4, kTiled, 2, 2>(a, p.num_sms, p.E, pu, st)
+               : launch_variant<TIn, false, 128, 8, kTiled, 2>(a, p.num_sms, p.E, pu, st);
   if (pair)
-    return launch_variant<TIn, false, 256, 6, kTiled, 2>(a, p.num_sms, p.E, (ub + 1) / 2, st);
+    return two ? launch_variant<TIn, false, 256, 3, kTiled, 2, 2>(a, p.num_sms, p.E, pu, st)
+               : launch_variant<TIn, false, 256, 6, kTiled, 2>(a, p.num_sms, p.E, pu, st);
   return launch_variant<TIn, false, 256, 4, kTiled>(a, p.num_sms, p.E, ub, st);
 }
 

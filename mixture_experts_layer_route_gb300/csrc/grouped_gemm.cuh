@@ -61,7 +61,8 @@
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (one thread) and
 // TMEM owner, warps 2-5 = epilogue (one 32-lane TMEM quarter each; the E4M3
 // down GEMM has warps 2-9, two per quarter).
-// A STAGES-deep shared-memory ring (full/empty mbarriers) feeds the MMA; two
+// A STAGES-deep shared-memory ring (full/empty mbarriers) feeds the MMA, each
+// stage one or two 128-byte K boxes of both operands (NBX); two
 // TMEM accumulators (tfull/tempty mbarriers) let the epilogue of one tile run
 // under the main loop of the next. Every wait is bounded (status word).
 #pragma once
@@ -118,18 +119,22 @@ struct GroupedGemmArgs {
 
 enum BMode : int { kGather4 = 0, kTiled = 2 };
 
-template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1>
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL = 1, int NBX = 1>
 struct GemmCfg {
   // E4M3 inputs (uint8_t codes) write bf16 h; other inputs write their own type.
   static constexpr bool F8 = sizeof(TIn) == 1;
   using TOut = std::conditional_t<F8, __nv_bfloat16, TIn>;
   static constexpr int BM = 128;                     // MMA M (weight rows)
   static constexpr int WM = GATED ? 64 : 128;        // output features per tile
-  static constexpr int BK = 128 / (int)sizeof(TIn);  // K per stage (one 128-byte row)
+  // K per stage: NBX boxes of one 128-byte row each. Two boxes give the MMA
+  // issuer eight MMAs per wait and commit instead of four.
+  static constexpr int BK = NBX * 128 / (int)sizeof(TIn);
   static constexpr int UMMA_K = 32 / (int)sizeof(TIn);  // K per instruction (32 bytes)
-  static constexpr int A_BYTES = BM * 128;             // per CTA
+  static constexpr int A_BOX = BM * 128;                // one K box of the CTA's weight rows
+  static constexpr int A_BYTES = NBX * A_BOX;
   static constexpr int B_ROWS = BN / CL;                 // token rows per CTA
-  static constexpr int B_BYTES = B_ROWS * 128;
+  static constexpr int B_BOX = B_ROWS * 128;             // one K box of the CTA's token rows
+  static constexpr int B_BYTES = NBX * B_BOX;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   // Epilogue staging: GATED, the 128 x 32 accumulator chunk (gate and up rows
@@ -145,6 +150,7 @@ struct GemmCfg {
   static constexpr int THREADS = 64 + EPI_THREADS;
   static_assert(CL == 1 || (CL == 2 && BMODE == kTiled && BN >= 64),
                 "CTA pairs split tiled token boxes of >= 64 rows");
+  static_assert(NBX == 1 || (NBX == 2 && BMODE == kTiled), "two boxes per stage: tiled tokens");
   // Pair MMAs round N up to 32 (each CTA's half a multiple of 16 rows).
   static constexpr int N_ROUND = CL == 2 ? 32 : 16;
   static constexpr int KIND = UmmaOf<TIn>::kind;
@@ -358,14 +364,15 @@ __device__ __forceinline__ void build_schedule(const int32_t* offsets_src, int E
 // keeps the CTA's right to allocate tensor memory unless last_alloc, and
 // invalidates its mbarriers at the end. Without FUSED none of this is compiled
 // in: the stand-alone kernels are the plain pass.
-template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL, bool FUSED = false>
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL, bool FUSED = false,
+          int NBX = 1>
 __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
                                                   uint8_t* smem_raw, int cid, int ncl,
                                                   bool prefetch,
                                                   const int32_t* offsets_in = nullptr,
                                                   const int32_t* gather_in = nullptr,
                                                   bool last_alloc = true) {
-  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>;
+  using C = GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL, NBX>;
   static_assert(!FUSED || CL == 1, "the fused passes run on single CTAs");
   const int32_t* const offsets_src = FUSED ? offsets_in : args.offsets;
   const int32_t* const gather_src = FUSED ? gather_in : args.gather_idx;
@@ -523,7 +530,7 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
       const int box_rows = bsel == 2 ? 16 : (bsel == 1 ? C::BOX1 : C::B_ROWS);
       // Bytes this stage's full barrier waits for: with a pair, the leader's
       // barrier counts both CTAs' loads.
-      uint32_t tx = CL * (C::A_BYTES + box_rows * 128);
+      uint32_t tx = CL * (C::A_BYTES + NBX * box_rows * 128);
       if constexpr (BMODE == kGather4) {
         n4 = (tl.n_valid + 3) / 4;
 #pragma unroll
@@ -540,23 +547,26 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
         tx = C::A_BYTES + n4 * 4 * 128;
       }
       const int b_row0 = (shared ? tl.p0 - offs[E] : tl.p0) + crank * (n_mma / 2);
-      // Per-lane operands of this tile's TMA loads (one SIMT step per stage):
-      // GATED: lanes 0, 1 = gate, up rows (+ lane 2 = token rows when tiled);
-      // DOWN: lane 0 = W_down rows, lane 1 = h rows.
+      // Per-lane operands of this tile's TMA loads (one SIMT step per stage),
+      // per K box h of the stage (lanes h * PER ..): GATED: gate, up rows (+
+      // token rows when tiled); DOWN: W_down rows, h rows.
       constexpr int NA = GATED ? 2 : 1;
-      constexpr int NLOADS = NA + (BMODE == kTiled ? 1 : 0);
+      constexpr int PER = NA + (BMODE == kTiled ? 1 : 0);
+      constexpr int NLOADS = NBX * PER;
+      const int bx = lane / PER, sub = lane - bx * PER;
       const CUtensorMap* my_map = mA0;
       int my_row = a_row0;
-      uint32_t my_off = 0;
+      const int my_dx = bx * (128 / (int)sizeof(TIn));
+      uint32_t my_off = (uint32_t)(bx * C::A_BOX);
       uint64_t my_pol = pol_w;
-      if (GATED && lane == 1) {
+      if (GATED && sub == 1) {
         my_map = mA1;
-        my_off = 64 * 128;
+        my_off += 64 * 128;
       }
-      if (BMODE == kTiled && lane == NA) {
+      if (BMODE == kTiled && sub == NA) {
         my_map = &args.tmB[(shared ? 3 : 0) + bsel];
         my_row = b_row0;
-        my_off = C::A_BYTES;
+        my_off = (uint32_t)(C::A_BYTES + bx * C::B_BOX);
         my_pol = pol_t;
       }
       const int nkb = kdim / C::BK;
@@ -583,12 +593,13 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
           if (leader && lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
           __syncwarp();
           if (lane < NLOADS)
-            tma_load_2d_pair(a_dst + my_off, my_map, kx, my_row, mapa_shared(full_bar(s), 0),
-                             my_pol);
+            tma_load_2d_pair(a_dst + my_off, my_map, kx + my_dx, my_row,
+                             mapa_shared(full_bar(s), 0), my_pol);
         } else {
           if (lane == 0) mbar_arrive_expect_tx(full_bar(s), tx);
           __syncwarp();
-          if (lane < NLOADS) tma_load_2d(a_dst + my_off, my_map, kx, my_row, full_bar(s), my_pol);
+          if (lane < NLOADS)
+            tma_load_2d(a_dst + my_off, my_map, kx + my_dx, my_row, full_bar(s), my_pol);
         }
         if constexpr (BMODE == kGather4) {
 #pragma unroll
@@ -645,8 +656,9 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
           const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-            const uint64_t ad = umma_desc_sw128(a_addr + kk * 32);
-            const uint64_t bd = umma_desc_sw128(b_addr + kk * 32);
+            // Four MMAs per 128-byte K box.
+            const uint64_t ad = umma_desc_sw128(a_addr + (kk >> 2) * C::A_BOX + (kk & 3) * 32);
+            const uint64_t bd = umma_desc_sw128(b_addr + (kk >> 2) * C::B_BOX + (kk & 3) * 32);
             const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
             if constexpr (PAIR)
               umma_issue_pair<C::KIND>(d_tmem, ad, bd, idesc, accum);
@@ -888,12 +900,12 @@ __device__ __forceinline__ void grouped_gemm_pass(const GroupedGemmArgs& args,
   }
 }
 
-template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL>
-__global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL>::THREADS, 1)
+template <typename TIn, bool GATED, int BN, int STAGES, int BMODE, int CL, int NBX = 1>
+__global__ void __launch_bounds__(GemmCfg<TIn, GATED, BN, STAGES, BMODE, CL, NBX>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GroupedGemmArgs args) {
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
-  grouped_gemm_pass<TIn, GATED, BN, STAGES, BMODE, CL>(args, smem_raw, blockIdx.x / CL,
+  grouped_gemm_pass<TIn, GATED, BN, STAGES, BMODE, CL, false, NBX>(args, smem_raw, blockIdx.x / CL,
                                                        gridDim.x / CL, true);
 }
 
